@@ -1,0 +1,479 @@
+// api.cu - the C ABI declared in include/mi.h.
+//
+// Host side: argument and shape checks, carving of the caller's workspace,
+// TMA descriptor encoding and kernel launches on the caller's stream.  No
+// device allocation, no synchronization (except mi_read_status), no state kept
+// between calls.  The attention variants are compiled in attn_kernels_*.cu.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attention.cuh"
+#include "block.cuh"
+#include "estimate.cuh"
+#include "select.cuh"
+#include "vs_index.cuh"
+
+using namespace mi;
+
+namespace {
+
+thread_local char g_msg[512];
+
+int cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_msg, sizeof(g_msg), "CUDA error in %s: %s", where, cudaGetErrorString(e));
+  return MI_ERR_CUDA;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// [heads, N, 128] bf16 as a 3-D tensor (d, N, heads); box = 64 columns x box_rows
+// rows, 128-byte swizzle (one box row = 128 bytes).  Rows past N read as zero.
+int make_map(CUtensorMap* m, const void* base, int heads, int N, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled is not available from the driver");
+    return MI_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(N) * kD * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MI_ERR_CUDA;
+  }
+  return MI_OK;
+}
+
+int check_device() {
+  static int verdict[64];  // 0 unknown, 1 sm_103, -1 other (benign race: same value)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return MI_ERR_DEVICE;
+  if (verdict[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    verdict[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (verdict[dev] < 0) {
+    snprintf(g_msg, sizeof(g_msg), "libmi.so is built for sm_103a only");
+    return MI_ERR_DEVICE;
+  }
+  return MI_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxHq = 4 * MI_MAX_HEADS;
+
+// Shape checks shared by every call; fills the head list.
+int check_common(const void* q, const void* k, int Hq, int Hkv, int N, int d,
+                 const int32_t* heads, int n_heads, HeadList* hl) {
+  if (!q || !k || !aligned16(q) || !aligned16(k)) return MI_ERR_ARG;
+  if (d != kD) return MI_ERR_SHAPE;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq > kMaxHq) return MI_ERR_SHAPE;
+  if (N < 64 || N % 64 != 0 || N > (1 << 21)) return MI_ERR_SHAPE;
+  if (n_heads <= 0 || n_heads > MI_MAX_HEADS || n_heads > Hq) return MI_ERR_ARG;
+  if (!heads && n_heads != Hq) return MI_ERR_ARG;
+  bool seen[kMaxHq] = {};
+  hl->n = n_heads;
+  for (int i = 0; i < n_heads; ++i) {
+    const int h = heads ? heads[i] : i;
+    if (h < 0 || h >= Hq || seen[h]) return MI_ERR_ARG;
+    seen[h] = true;
+    hl->h[i] = static_cast<int16_t>(h);
+  }
+  return MI_OK;
+}
+
+// ---------------------------------------------------------- workspace ----
+
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  }
+};
+
+struct EstLayout {
+  size_t status, part, stats, vsc, ssc, total;
+  int NC;
+};
+EstLayout est_layout(int n_heads, int N) {
+  EstLayout L;
+  Carve c;
+  L.NC = cdiv(N, kChunkKeys);
+  L.status = c.take(256);
+  L.part = c.take(sizeof(float) * (size_t)n_heads * kLastQ * L.NC * 2);
+  L.stats = c.take(sizeof(float) * (size_t)n_heads * kLastQ * 2);
+  L.vsc = c.take(sizeof(float) * (size_t)n_heads * N);
+  L.ssc = c.take(sizeof(float) * (size_t)n_heads * N);
+  L.total = c.off;
+  return L;
+}
+
+struct VsLayout {
+  size_t status, offbits, colbits, dbits, dlist, dcount, total;
+  int Nw, NT, NTw;
+};
+VsLayout vs_layout(int n_heads, int N) {
+  VsLayout L;
+  Carve c;
+  L.NT = cdiv(N, kBN);
+  L.Nw = 4 * L.NT;  // padded to whole 128-key tiles
+  L.NTw = cdiv(L.NT, 32);
+  L.status = c.take(256);
+  L.offbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.Nw);
+  L.colbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.Nw);
+  L.dbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.NTw);
+  L.dlist = c.take(sizeof(int) * (size_t)n_heads * L.NT);
+  L.dcount = c.take(sizeof(int) * (size_t)n_heads);
+  L.total = c.off;
+  return L;
+}
+
+struct BlockLayout {
+  size_t status, qbar, kbar, total;
+};
+BlockLayout block_layout(int n_heads, int Hkv, int N) {
+  BlockLayout L;
+  Carve c;
+  const int NB = N / kBlk;
+  L.status = c.take(256);
+  L.qbar = c.take(sizeof(float) * (size_t)n_heads * NB * kD);
+  L.kbar = c.take(sizeof(float) * (size_t)Hkv * NB * kD);
+  L.total = c.off;
+  return L;
+}
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < need) return MI_ERR_WORKSPACE;
+  return MI_OK;
+}
+
+int set_smem(const void* kernel, size_t bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "cudaFuncSetAttribute");
+}
+
+int launched(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, what);
+}
+
+const float kScaleLog2 = 1.4426950408889634f / std::sqrt(static_cast<float>(kD));
+
+int zero_status(int* status, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+// Shared by the four attention entry points: pattern-specific fields of `a` are set.
+template <int PAT>
+int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, int N,
+                  mi_bf16* out, float* lse, int* status, AttnArgs& a, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  int rc;
+  if ((rc = make_map(&mq, q, Hq, N, kBM)) || (rc = make_map(&mk, k, Hkv, N, kBN)) ||
+      (rc = make_map(&mv, v, Hkv, N, kBN)))
+    return rc;
+  a.N = N;
+  a.group = Hq / Hkv;
+  a.scale_log2 = kScaleLog2;
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.status = status;
+  a.wait_limit_ns = kWaitLimitNs;
+  a.kp = reinterpret_cast<const __nv_bfloat16*>(k);
+  a.vp = reinterpret_cast<const __nv_bfloat16*>(v);
+  cudaError_t e = launch_attn<PAT>(mq, mk, mv, a, cdiv(N, kBM), st);
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "attention kernel");
+}
+
+int attn_preamble(const void* q, const void* k, const void* v, int Hq, int Hkv, int N, int d,
+                  const int32_t* heads, int n_heads, const void* out, AttnArgs* a) {
+  int rc = check_device();
+  if (rc) return rc;
+  memset(a, 0, sizeof(*a));
+  if ((rc = check_common(q, k, Hq, Hkv, N, d, heads, n_heads, &a->heads))) return rc;
+  if (!v || !out || !aligned16(v) || !aligned16(out)) return MI_ERR_ARG;
+  return MI_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI ==
+
+extern "C" {
+
+size_t mi_workspace_bytes(int op, int n_heads, int Hkv, int N, int k_v, int k_s, int topk) {
+  (void)k_v;
+  (void)k_s;
+  (void)topk;
+  if (n_heads <= 0 || N <= 0) return 0;
+  switch (op) {
+    case MI_OP_VS_ESTIMATE: return est_layout(n_heads, N).total;
+    case MI_OP_VS_SPARSE_ATTN: return vs_layout(n_heads, N).total;
+    case MI_OP_BLOCK_SPARSE_ATTN: return Hkv > 0 ? block_layout(n_heads, Hkv, N).total : 0;
+    case MI_OP_ASHAPE_ATTN:
+    case MI_OP_DENSE_CAUSAL_ATTN: return 256;
+    default: return 0;
+  }
+}
+
+int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
+                   const int32_t* heads, int n_heads, int last_q, int k_v, int k_s,
+                   int32_t* v_idx, int32_t* s_idx, void* workspace, size_t ws_bytes,
+                   mi_stream_t stream) {
+  int rc = check_device();
+  if (rc) return rc;
+  EstArgs a;
+  memset(&a, 0, sizeof(a));
+  if ((rc = check_common(q, k, Hq, Hkv, N, d, heads, n_heads, &a.heads))) return rc;
+  if (last_q != kLastQ) return MI_ERR_SHAPE;
+  if (k_v < 0 || k_s < 0) return MI_ERR_ARG;
+  if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
+  const EstLayout L = est_layout(n_heads, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+
+  // pair up listed heads that share a KV head (two heads fill one 128-row UMMA)
+  const int group = Hq / Hkv;
+  int pending[kMaxHq];
+  for (int g = 0; g < Hkv; ++g) pending[g] = -1;
+  int np = 0;
+  for (int i = 0; i < n_heads; ++i) {
+    const int g = a.heads.h[i] / group;
+    if (pending[g] < 0) {
+      pending[g] = i;
+    } else {
+      a.pair_a[np] = static_cast<int16_t>(pending[g]);
+      a.pair_b[np] = static_cast<int16_t>(i);
+      ++np;
+      pending[g] = -1;
+    }
+  }
+  for (int g = 0; g < Hkv; ++g)
+    if (pending[g] >= 0) {
+      a.pair_a[np] = static_cast<int16_t>(pending[g]);
+      a.pair_b[np] = -1;
+      ++np;
+    }
+  a.N = N;
+  a.group = group;
+  a.n_pairs = np;
+  a.NC = L.NC;
+  a.scale_log2 = kScaleLog2;
+  a.part = reinterpret_cast<float*>(ws + L.part);
+  a.stats = reinterpret_cast<float*>(ws + L.stats);
+  a.vsc = reinterpret_cast<float*>(ws + L.vsc);
+  a.ssc = reinterpret_cast<float*>(ws + L.ssc);
+  a.status = status;
+  a.wait_limit_ns = kWaitLimitNs;
+
+  static std::once_flag once;
+  static int once_rc = MI_OK;
+  std::call_once(once, [] {
+    once_rc = set_smem(reinterpret_cast<const void*>(est_kernel<1>), kEstSmem1);
+    if (once_rc == MI_OK) once_rc = set_smem(reinterpret_cast<const void*>(est_kernel<2>), kEstSmem2);
+  });
+  if (once_rc) return once_rc;
+
+  CUtensorMap mq, mk;
+  if ((rc = make_map(&mq, q, Hq, N, kLastQ)) || (rc = make_map(&mk, k, Hkv, N, kBN))) return rc;
+  if ((rc = zero_status(status, st))) return rc;
+  const dim3 grid(np, L.NC);
+  est_kernel<1><<<grid, 256, kEstSmem1, st>>>(mq, mk, a);
+  if ((rc = launched("estimation pass 1"))) return rc;
+  est_combine<<<n_heads, kLastQ, 0, st>>>(a.part, a.stats, L.NC);
+  if ((rc = launched("estimation combine"))) return rc;
+  est_kernel<2><<<grid, 256, kEstSmem2, st>>>(mq, mk, a);
+  if ((rc = launched("estimation pass 2"))) return rc;
+  if (k_v > 0 || k_s > 0) {
+    vs_topk_kernel<<<dim3(n_heads, 2), 1024, 0, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx);
+    if ((rc = launched("top-k"))) return rc;
+  }
+  return MI_OK;
+}
+
+int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
+                      int N, int d, const int32_t* heads, int n_heads, const int32_t* v_idx,
+                      int k_v, const int32_t* s_idx, int k_s, mi_bf16* out, float* lse,
+                      void* workspace, size_t ws_bytes, mi_stream_t stream) {
+  AttnArgs a;
+  int rc = attn_preamble(q, k, v, Hq, Hkv, N, d, heads, n_heads, out, &a);
+  if (rc) return rc;
+  if (k_v < 0 || k_s < 0 || k_v > MI_MAX_KV) return MI_ERR_ARG;
+  if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
+  const VsLayout L = vs_layout(n_heads, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+
+  VsIndexArgs ia;
+  ia.N = N;
+  ia.k_v = k_v;
+  ia.k_s = k_s;
+  ia.Nw = L.Nw;
+  ia.NT = L.NT;
+  ia.NTw = L.NTw;
+  ia.v_idx = v_idx;
+  ia.s_idx = s_idx;
+  ia.offbits = reinterpret_cast<uint32_t*>(ws + L.offbits);
+  ia.colbits = reinterpret_cast<uint32_t*>(ws + L.colbits);
+  ia.dbits = reinterpret_cast<uint32_t*>(ws + L.dbits);
+  ia.dlist = reinterpret_cast<int*>(ws + L.dlist);
+  ia.dcount = reinterpret_cast<int*>(ws + L.dcount);
+  ia.status = status;
+  vs_index_kernel<<<n_heads, 512, 0, st>>>(ia);
+  if ((rc = launched("vertical-slash index build"))) return rc;
+
+  a.offbits = ia.offbits;
+  a.colbits = ia.colbits;
+  a.dbits = ia.dbits;
+  a.dlist = ia.dlist;
+  a.dcount = ia.dcount;
+  a.v_idx = v_idx;
+  a.k_v = k_v;
+  a.Nw = L.Nw;
+  a.NT = L.NT;
+  a.NTw = L.NTw;
+  return run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
+}
+
+int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
+                         int N, int d, const int32_t* heads, int n_heads, int block, int topk,
+                         int32_t* blk_idx, int flags, mi_bf16* out, float* lse, void* workspace,
+                         size_t ws_bytes, mi_stream_t stream) {
+  AttnArgs a;
+  int rc = attn_preamble(q, k, v, Hq, Hkv, N, d, heads, n_heads, out, &a);
+  if (rc) return rc;
+  if (block != kBlk) return MI_ERR_SHAPE;
+  if (topk < 1 || topk > MI_MAX_KV / 2 || !blk_idx) return MI_ERR_ARG;
+  if (flags & ~MI_IDX_GIVEN) return MI_ERR_UNIMPLEMENTED;
+  const BlockLayout L = block_layout(n_heads, Hkv, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+  const int NB = N / kBlk;
+  if (!(flags & MI_IDX_GIVEN)) {
+    float* qbar = reinterpret_cast<float*>(ws + L.qbar);
+    float* kbar = reinterpret_cast<float*>(ws + L.kbar);
+    const int wq = n_heads * NB, wk = Hkv * NB;
+    block_pool_kernel<<<cdiv(wq, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), N,
+                                                   n_heads, NB, a.heads, 1, qbar);
+    if ((rc = launched("block pooling (q)"))) return rc;
+    block_pool_kernel<<<cdiv(wk, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k), N,
+                                                   Hkv, NB, a.heads, 0, kbar);
+    if ((rc = launched("block pooling (k)"))) return rc;
+    static std::once_flag once;
+    static int once_rc = MI_OK;
+    std::call_once(once, [] {
+      once_rc = set_smem(reinterpret_cast<const void*>(block_select_kernel), 160 * 1024);
+    });
+    if (once_rc) return once_rc;
+    block_select_kernel<<<dim3(NB, n_heads), 256, sizeof(float) * NB, st>>>(
+        qbar, kbar, NB, Hq / Hkv, a.heads, topk, blk_idx);
+    if ((rc = launched("block selection"))) return rc;
+  } else {
+    const int rows = n_heads * NB;
+    block_validate_kernel<<<cdiv(rows, 256), 256, 0, st>>>(blk_idx, NB, topk, rows, status);
+    if ((rc = launched("block index validation"))) return rc;
+  }
+  a.blk_idx = blk_idx;
+  a.topk = topk;
+  return run_attention<kPatBlock>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
+}
+
+int mi_ashape_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N,
+                   int d, const int32_t* heads, int n_heads, int n_init, int window, mi_bf16* out,
+                   float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream) {
+  AttnArgs a;
+  int rc = attn_preamble(q, k, v, Hq, Hkv, N, d, heads, n_heads, out, &a);
+  if (rc) return rc;
+  if (n_init < 0 || window < 1) return MI_ERR_ARG;
+  if ((rc = check_ws(workspace, ws_bytes, 256))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  if ((rc = zero_status(status, st))) return rc;
+  a.n_init = n_init < N ? n_init : N;
+  a.window = window < N ? window : N;
+  return run_attention<kPatAShape>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
+}
+
+int mi_dense_causal_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
+                         int N, int d, const int32_t* heads, int n_heads, mi_bf16* out,
+                         float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream) {
+  AttnArgs a;
+  int rc = attn_preamble(q, k, v, Hq, Hkv, N, d, heads, n_heads, out, &a);
+  if (rc) return rc;
+  if ((rc = check_ws(workspace, ws_bytes, 256))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  if ((rc = zero_status(status, st))) return rc;
+  return run_attention<kPatDense>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
+}
+
+int mi_read_status(const void* workspace, mi_stream_t stream) {
+  if (!workspace) return MI_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+  return v;
+}
+
+const char* mi_strerror(int code) {
+  switch (code) {
+    case MI_OK: return "success";
+    case MI_ERR_ARG: return "invalid argument (null/misaligned pointer, head list or budget)";
+    case MI_ERR_SHAPE:
+      return "unsupported shape (d must be 128, N a multiple of 64 in [64, 2^21], Hq % Hkv == 0, "
+             "last_q 64, block 64)";
+    case MI_ERR_WORKSPACE: return "workspace missing, not 256-byte aligned or too small";
+    case MI_ERR_CUDA: return g_msg[0] ? g_msg : "CUDA error";
+    case MI_ERR_INDEX:
+      return "index out of range, not strictly ascending, or a value after -1 padding";
+    case MI_ERR_TIMEOUT: return "a bounded pipeline wait in a kernel expired";
+    case MI_ERR_UNIMPLEMENTED: return "option not supported by this build";
+    case MI_ERR_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,573 @@
+// attention.cuh - the tcgen05 sparse/dense causal attention engine.
+//
+// One CTA computes 128 query rows (one row block r) of one head.  Its key
+// range is a list of 128-key tiles chosen by the head's pattern:
+//   - contiguous tiles, TMA-loaded from K/V ([Hkv, N, 128] bf16, 128-byte
+//     swizzle), masked element-wise by the pattern's rule;
+//   - for vertical-slash heads, "gathered" tiles of up to 128 scattered key
+//     columns that no contiguous tile covers, copied row by row into the same
+//     swizzled layout (the permutation-invariant gathering idea of PIT, which
+//     the MInference pages name as the basis of their kernels: README mirror,
+//     gittoolsai.com, "TL;DR" and the PIT note; talk slides, boteman.cn,
+//     "Dynamic Sparse Attention Calculation with PIT, FlashAttention").
+//
+// Warp roles (256 threads):
+//   warp 0      TMEM allocation and the single-thread tcgen05.mma issuer
+//   warp 1      Q (once) and K tiles (TMA, or cp.async gather)
+//   warp 2      V tiles (TMA, or cp.async gather)
+//   warp 3      idle after the prologue
+//   warps 4-7   softmax: thread t owns query row t (TMEM lane t)
+//
+// Per tile i: S_i = Q K_i^T (M=128, N=128, K=128) into one of two TMEM
+// buffers; softmax warps load S_i, mask, update a running maximum, write
+// P_i = exp2(x - m) as bf16 into shared memory (128-byte swizzled, K-major);
+// then O += P_i V_i accumulates in TMEM.  The running maximum is only moved
+// (and O rescaled in TMEM) when a tile's maximum exceeds it by more than 8
+// (log2 units), so P stays below 2^8 and most tiles need no O correction.
+// Every mbarrier wait is bounded; on a timeout the CTA stops issuing work,
+// waits for what it already issued, frees TMEM and records MI_ERR_TIMEOUT.
+#pragma once
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mi {
+
+enum Pattern : int { kPatDense = 0, kPatVS = 1, kPatBlock = 2, kPatAShape = 3 };
+
+struct AttnArgs {
+  int N;
+  int group;         // Hq / Hkv
+  float scale_log2;  // log2(e) / sqrt(d)
+  __nv_bfloat16* out;
+  float* lse;
+  int* status;
+  uint64_t wait_limit_ns;
+  // raw K/V for gathered tiles
+  const __nv_bfloat16* kp;
+  const __nv_bfloat16* vp;
+  // vertical-slash index structures (per listed head)
+  const uint32_t* offbits;  // [n_heads, Nw]   bit o: offset o selected
+  const uint32_t* colbits;  // [n_heads, Nw]   bit j: column j selected
+  const uint32_t* dbits;    // [n_heads, NTw]  bit t: tile distance t touched by a diagonal
+  const int* dlist;         // [n_heads, NT]   the set bits of dbits, ascending
+  const int* dcount;        // [n_heads]
+  const int* v_idx;         // [n_heads, k_v]
+  int k_v;
+  int Nw, NT, NTw;
+  // block-sparse
+  const int* blk_idx;  // [n_heads, N/64, topk]
+  int topk;
+  // A-shape
+  int n_init, window;
+  HeadList heads;
+};
+
+struct AttnSmem {
+  alignas(1024) uint8_t q[2][16384];
+  alignas(1024) uint8_t k[2][2][16384];
+  alignas(1024) uint8_t v[2][2][16384];
+  alignas(1024) uint8_t p[2][16384];
+  int list[MI_MAX_KV];  // VS: residual columns; block: (tile << 4) | sub-block mask
+  int scan[256];
+  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_empty[2], p_full, pv_done, mma_done;
+  uint32_t tmem;
+  int abort;
+  int n_list;    // entries in list
+  int n_tiles;   // tiles this CTA processes
+  int n_contig;  // leading contiguous tiles (VS)
+  int has_t0;    // VS: tile 0 is prepended
+  int d_cnt;     // VS: number of tile distances <= r
+};
+
+constexpr size_t kAttnSmemBytes = sizeof(AttnSmem) + 1024;
+constexpr uint32_t kTmemCols = 512;  // S0 @0, S1 @128, O @256
+
+// ------------------------------------------------------------ tile list ----
+
+struct TileRef {
+  int kind;  // 0 contiguous, 1 gathered
+  int t;     // contiguous: key tile index; gathered: chunk of the residual list
+  int sub;   // block pattern: 4-bit mask (bit = rowhalf*2 + colhalf)
+};
+
+template <int PAT>
+__device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a, int n, int r,
+                                           int i) {
+  TileRef ref{0, 0, 0xF};
+  if (PAT == kPatDense) {
+    ref.t = i;
+  } else if (PAT == kPatVS) {
+    if (i < s.n_contig) {
+      if (s.has_t0 && i == 0) {
+        ref.t = 0;
+      } else {
+        const int idx = s.d_cnt - 1 - (i - s.has_t0);
+        ref.t = r - __ldg(a.dlist + (size_t)n * a.NT + idx);
+      }
+    } else {
+      ref.kind = 1;
+      ref.t = i - s.n_contig;
+    }
+  } else if (PAT == kPatBlock) {
+    const int e = s.list[i];
+    ref.t = e >> 4;
+    ref.sub = e & 0xF;
+  } else {  // A-shape: sink tiles then the window tiles
+    const int t_lo = max(0, r * kBM - a.window + 1) / kBN;
+    const int n_sink = min(cdiv(a.n_init, kBN), t_lo);
+    ref.t = (i < n_sink) ? i : t_lo + (i - n_sink);
+  }
+  return ref;
+}
+
+// Bits [lo, hi) of a 32-bit word whose bit 0 is position `base`.
+__device__ __forceinline__ uint32_t range_bits(int base, int lo, int hi) {
+  lo = max(lo - base, 0);
+  hi = min(hi - base, 32);
+  if (hi <= lo) return 0u;
+  const uint32_t up = (hi >= 32) ? 0xFFFFFFFFu : ((1u << hi) - 1u);
+  return up & ~((1u << lo) - 1u);
+}
+
+// 32 bits of `bits` starting at bit position `pos` (may be negative: zeros).
+__device__ __forceinline__ uint32_t load_bits32(const uint32_t* bits, int pos, int nbits) {
+  if (pos >= nbits || pos + 32 <= 0) return 0u;
+  const int w = pos >> 5;  // arithmetic shift: floor
+  const int sh = pos & 31;
+  const uint32_t lo = (w >= 0 && (w << 5) < nbits) ? __ldg(bits + w) : 0u;
+  const uint32_t hi = ((w + 1) >= 0 && ((w + 1) << 5) < nbits) ? __ldg(bits + w + 1) : 0u;
+  return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
+}
+
+// Keep-mask of query row q over the 128 keys of tile `ref` (bit c of m[c/32]).
+template <int PAT>
+__device__ __forceinline__ void row_mask(const AttnSmem& s, const AttnArgs& a, int n, int r,
+                                         const TileRef& ref, int q, uint32_t m[4]) {
+  if (PAT == kPatVS && ref.kind == 1) {
+    const int valid = min(kBN, s.n_list - ref.t * kBN);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) m[w] = range_bits(32 * w, 0, valid);
+    return;
+  }
+  const int j0 = ref.t * kBN;
+  if (PAT == kPatDense) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) m[w] = 0xFFFFFFFFu;
+  } else if (PAT == kPatVS) {
+    const uint32_t* off = a.offbits + (size_t)n * a.Nw;
+    const uint32_t* col = a.colbits + (size_t)n * a.Nw;
+    // offsets q - j0 - c for c = 0..127 are the 128 bits starting at q - j0 - 127, reversed
+    const int base = q - j0 - 127;
+    const int lb = (q >> 6) << 6;  // start of the query's own 64-block
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t sl = __brev(load_bits32(off, base + 32 * (3 - w), a.N));
+      const uint32_t cl = __ldg(col + (j0 >> 5) + w);
+      m[w] = sl | cl | range_bits(j0 + 32 * w, 0, kBlk) | range_bits(j0 + 32 * w, lb, lb + kBlk);
+    }
+  } else if (PAT == kPatBlock) {
+    const int half = (q >> 6) & 1;
+    const uint32_t lo = ((ref.sub >> (half * 2)) & 1) ? 0xFFFFFFFFu : 0u;
+    const uint32_t hi = ((ref.sub >> (half * 2 + 1)) & 1) ? 0xFFFFFFFFu : 0u;
+    m[0] = lo;
+    m[1] = lo;
+    m[2] = hi;
+    m[3] = hi;
+  } else {  // A-shape
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      m[w] = range_bits(j0 + 32 * w, 0, a.n_init) |
+             range_bits(j0 + 32 * w, q - a.window + 1, q + 1);
+  }
+  if (ref.t == r) {  // the diagonal tile: causal
+#pragma unroll
+    for (int w = 0; w < 4; ++w) m[w] &= range_bits(j0 + 32 * w, 0, q + 1);
+  }
+}
+
+// ------------------------------------------------------------- prologue ----
+
+// Block-wide exclusive scan of one int per thread (256 threads); returns the
+// exclusive prefix and writes the total to *total.
+__device__ __forceinline__ int block_excl_scan_256(int x, int* scratch, int* total) {
+  const int tid = threadIdx.x;
+  scratch[tid] = x;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    const int y = (tid >= off) ? scratch[tid - off] : 0;
+    __syncthreads();
+    scratch[tid] += y;
+    __syncthreads();
+  }
+  const int incl = scratch[tid];
+  *total = scratch[255];
+  __syncthreads();
+  return incl - x;
+}
+
+// A vertical column that no contiguous tile of row block r covers.
+__device__ __forceinline__ bool residual_column(int j, int N, int r, const uint32_t* db) {
+  const int t = j >> 7;
+  if (j < 0 || j >= N || t < 1 || t >= r) return false;
+  const int d = r - t;
+  return !((__ldg(db + (d >> 5)) >> (d & 31)) & 1u);
+}
+
+template <int PAT>
+__device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, int n, int r) {
+  const int tid = threadIdx.x;
+  if (PAT == kPatDense) {
+    if (tid == 0) s.n_tiles = r + 1;
+  } else if (PAT == kPatAShape) {
+    if (tid == 0) {
+      const int t_lo = max(0, r * kBM - a.window + 1) / kBN;
+      const int n_sink = min(cdiv(a.n_init, kBN), t_lo);
+      s.n_tiles = n_sink + (r - t_lo + 1);
+    }
+  } else if (PAT == kPatVS) {
+    // contiguous tiles: r - delta for the tile distances delta <= r, plus tile 0
+    const int* dl = a.dlist + (size_t)n * a.NT;
+    const int dc = __ldg(a.dcount + n);
+    if (tid == 0) {
+      int lo = 0, hi = dc;  // first index with dl[idx] > r
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(dl + mid) <= r) lo = mid + 1;
+        else hi = mid;
+      }
+      s.d_cnt = lo;
+      s.has_t0 = (lo == 0 || __ldg(dl + lo - 1) != r) ? 1 : 0;
+      s.n_contig = lo + s.has_t0;
+    }
+    // residual columns: selected keys in tiles 1..r-1 that no contiguous tile covers
+    const int* vi = a.v_idx + (size_t)n * a.k_v;
+    const uint32_t* db = a.dbits + (size_t)n * a.NTw;
+    const int per = cdiv(a.k_v, 256);
+    const int beg = min(tid * per, a.k_v), end = min(beg + per, a.k_v);
+    int cnt = 0;
+    for (int e = beg; e < end; ++e) cnt += residual_column(__ldg(vi + e), a.N, r, db) ? 1 : 0;
+    int total;
+    int pos = block_excl_scan_256(cnt, s.scan, &total);
+    for (int e = beg; e < end; ++e) {
+      const int j = __ldg(vi + e);
+      if (residual_column(j, a.N, r, db)) s.list[pos++] = j;
+    }
+    if (tid == 0) {
+      s.n_list = total;
+      s.n_tiles = s.n_contig + cdiv(total, kBN);
+    }
+  } else {  // block-sparse: union of the two 64-row halves' selected blocks, as 128-key tiles
+    if (tid == 0) {
+      const int NB = a.N / kBlk;
+      const int* b0 = a.blk_idx + ((size_t)n * NB + 2 * r) * a.topk;
+      const bool has1 = (2 * r + 1) < NB;
+      const int* b1 = b0 + a.topk;
+      int i0 = 0, i1 = 0, cnt = 0;
+      auto valid = [&](const int* b, int i, int row) {
+        if (i >= a.topk) return false;
+        const int c = __ldg(b + i);
+        return c >= 0 && c <= row;
+      };
+      while (true) {
+        const bool v0 = valid(b0, i0, 2 * r);
+        const bool v1 = has1 && valid(b1, i1, 2 * r + 1);
+        if (!v0 && !v1) break;
+        const int c0 = v0 ? __ldg(b0 + i0) : 0x7FFFFFFF;
+        const int c1 = v1 ? __ldg(b1 + i1) : 0x7FFFFFFF;
+        const int t = min(c0, c1) >> 1;
+        int sub = 0;
+        while (valid(b0, i0, 2 * r) && (__ldg(b0 + i0) >> 1) == t) {
+          sub |= 1 << (__ldg(b0 + i0) & 1);
+          ++i0;
+        }
+        while (has1 && valid(b1, i1, 2 * r + 1) && (__ldg(b1 + i1) >> 1) == t) {
+          sub |= 4 << (__ldg(b1 + i1) & 1);
+          ++i1;
+        }
+        if (cnt < MI_MAX_KV) s.list[cnt++] = (t << 4) | sub;
+      }
+      s.n_list = cnt;
+      s.n_tiles = cnt;
+    }
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------- loaders ----
+
+// Copy up to 128 gathered key rows (256 bytes each) into a swizzled [2][128][128B]
+// tile; rows past `valid` are zero-filled.  One warp.
+__device__ __forceinline__ void gather_tile(uint8_t (*dst)[16384], const __nv_bfloat16* src_head,
+                                            const int* cols, int valid) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < kBN * 16; e += 32) {
+    const int row = e >> 4, u = e & 15;
+    uint8_t* d = dst[u >> 3] + sw128_offset(row, u & 7);
+    if (row < valid) {
+      cp_async_16(d, src_head + (size_t)cols[row] * kD + u * 8);
+    } else {
+      *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  cp_async_wait_all();
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------- kernel ----
+
+template <int PAT>
+__global__ void __launch_bounds__(256, 1)
+attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  AttnSmem& s = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int NRB = cdiv(a.N, kBM);
+  const int r = NRB - 1 - static_cast<int>(blockIdx.x);  // heaviest row blocks first
+  const int n = blockIdx.y;
+  const int h = a.heads.h[n];
+  const int g = h / a.group;
+
+  if (tid == 0) {
+    mbar_init(&s.q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.k_full[b], 1);
+      mbar_init(&s.k_empty[b], 1);
+      mbar_init(&s.v_full[b], 1);
+      mbar_init(&s.v_empty[b], 1);
+      mbar_init(&s.s_full[b], 1);
+      mbar_init(&s.s_empty[b], 128);
+    }
+    mbar_init(&s.p_full, 128);
+    mbar_init(&s.pv_done, 1);
+    mbar_init(&s.mma_done, 1);
+    s.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&s.tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    tma_prefetch_map(&map_q);
+    tma_prefetch_map(&map_k);
+    tma_prefetch_map(&map_v);
+  }
+  tc_fence_before();
+  attn_prologue<PAT>(s, a, n, r);  // ends with __syncthreads
+  tc_fence_after();
+  const uint32_t tmem = s.tmem;
+  const int T = s.n_tiles;
+  volatile int* abort = &s.abort;
+  const uint64_t lim = a.wait_limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ MMA ----
+    if (lane_id() == 0) {
+      const uint32_t id_qk = idesc_bf16(kBM, kBN, 0);
+      const uint32_t id_pv = idesc_bf16(kBM, kD, 1);
+      bool ok = mbar_wait(&s.q_full, 0, abort, lim);
+      auto issue_pv = [&](int u) {
+        if (!ok) return;
+        ok = mbar_wait(&s.p_full, u & 1, abort, lim) &&
+             mbar_wait(&s.v_full[u & 1], (u >> 1) & 1, abort, lim);
+        if (!ok) return;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(smem_u32(s.p[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(smem_u32(s.v[u & 1][0]) + kk * 2048, 16384, 1024);
+          umma_bf16_ss(tmem + 256, ad, bd, id_pv, (u > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&s.pv_done);
+        umma_commit(&s.v_empty[u & 1]);
+      };
+      for (int t = 0; t < T && ok; ++t) {
+        const int b = t & 1;
+        ok = mbar_wait(&s.k_full[b], (t >> 1) & 1, abort, lim);
+        if (ok && t >= 2) ok = mbar_wait(&s.s_empty[b], ((t - 2) >> 1) & 1, abort, lim);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(smem_u32(s.q[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(smem_u32(s.k[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          umma_bf16_ss(tmem + b * 128, ad, bd, id_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s.s_full[b]);
+        umma_commit(&s.k_empty[b]);
+        if (t >= 1) issue_pv(t - 1);
+      }
+      if (ok && T > 0) issue_pv(T - 1);
+      umma_commit(&s.mma_done);  // completes when everything issued above is done
+      mbar_wait_drain(&s.mma_done, 0, lim);
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == 2) {
+    // --------------------------------------------------------- loaders ----
+    const bool is_k = (warp == 1);
+    const CUtensorMap* map = is_k ? &map_k : &map_v;
+    uint64_t* full = is_k ? s.k_full : s.v_full;
+    uint64_t* empty = is_k ? s.k_empty : s.v_empty;
+    uint8_t(*buf)[2][16384] = is_k ? s.k : s.v;
+    const __nv_bfloat16* src_head = (is_k ? a.kp : a.vp) + (size_t)g * a.N * kD;
+    if (is_k && lane_id() == 0) {
+      mbar_arrive_expect_tx(&s.q_full, 2 * 16384);
+      tma_load_3d(s.q[0], &map_q, &s.q_full, 0, r * kBM, h);
+      tma_load_3d(s.q[1], &map_q, &s.q_full, 64, r * kBM, h);
+    }
+    int issued = 0;
+    for (int t = 0; t < T; ++t) {
+      const int b = t & 1;
+      if (t >= 2 && !mbar_wait_warp(&empty[b], ((t - 2) >> 1) & 1, abort, lim)) break;
+      const TileRef ref = tile_at<PAT>(s, a, n, r, t);
+      if (ref.kind == 0) {
+        if (lane_id() == 0) {
+          mbar_arrive_expect_tx(&full[b], 2 * 16384);
+          tma_load_3d(buf[b][0], map, &full[b], 0, ref.t * kBN, g);
+          tma_load_3d(buf[b][1], map, &full[b], 64, ref.t * kBN, g);
+        }
+      } else {
+        const int valid = min(kBN, s.n_list - ref.t * kBN);
+        gather_tile(buf[b], src_head, s.list + ref.t * kBN, valid);
+        if (lane_id() == 0) mbar_arrive(&full[b]);
+      }
+      issued = t + 1;
+      __syncwarp();
+    }
+    // drain: the last (up to two) loads must land before the CTA can exit
+    if (lane_id() == 0) {
+      if (is_k) mbar_wait_drain(&s.q_full, 0, lim);
+      for (int t = max(0, issued - 2); t < issued; ++t)
+        mbar_wait_drain(&full[t & 1], (t >> 1) & 1, lim);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // --------------------------------------------------------- softmax ----
+    const int row = tid - 128;  // TMEM lane and row within the block
+    const int q = r * kBM + row;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int b = t & 1;
+      ok = mbar_wait_warp(&s.s_full[b], (t >> 1) & 1, abort, lim);
+      if (!ok) break;
+      tc_fence_after();
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + b * 128 + c * 32, x + c * 32);
+      tc_fence_before();
+      mbar_arrive(&s.s_empty[b]);
+
+      const TileRef ref = tile_at<PAT>(s, a, n, r, t);
+      uint32_t mk[4];
+      row_mask<PAT>(s, a, n, r, ref, q, mk);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const bool keep = (mk[c >> 5] >> (c & 31)) & 1u;
+        x[c] = keep ? x[c] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, x[c]);
+      }
+      // the P buffer and O are free once the previous tile's P.V is done
+      if (t >= 1) {
+        ok = mbar_wait_warp(&s.pv_done, (t - 1) & 1, abort, lim);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      // move the reference maximum only when the tile's maximum exceeds it by > 8
+      const bool upd = mx > m_ref + 8.0f;
+      const bool rescale_o = upd && (m_ref != -INFINITY);
+      float alpha = 1.f;
+      if (rescale_o) alpha = fast_exp2(m_ref - mx);
+      if (upd) {
+        l *= alpha;
+        m_ref = mx;
+      }
+      if (__any_sync(0xffffffffu, rescale_o)) {  // tcgen05.ld/st are warp-collective
+        float o[32];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tmem + lane_base + 256 + c * 32, o);
+        }
+      }
+      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float rs = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = fast_exp2(x[u * 8 + 2 * e] - mb);
+          const float p1 = fast_exp2(x[u * 8 + 2 * e + 1] - mb);
+          rs += p0 + p1;
+          __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
+          pk[e] = *reinterpret_cast<uint32_t*>(&bb);
+        }
+        *reinterpret_cast<uint4*>(s.p[u >> 3] + sw128_offset(row, u & 7)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      l += rs;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.p_full);
+    }
+    // epilogue: O / l
+    if (ok && T > 0) ok = mbar_wait_warp(&s.pv_done, (T - 1) & 1, abort, lim);
+    if (ok) {
+      tc_fence_after();
+      const bool in_range = q < a.N;
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = a.out + ((size_t)h * a.N + q) * kD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+        if (in_range) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 bb =
+                  __floats2bfloat162_rn(o[u * 8 + 2 * e] * inv, o[u * 8 + 2 * e + 1] * inv);
+              pk[e] = *reinterpret_cast<uint32_t*>(&bb);
+            }
+            *reinterpret_cast<uint4*>(orow + c * 32 + u * 8) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      }
+      if (in_range && a.lse)
+        a.lse[(size_t)h * a.N + q] =
+            (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (s.abort && tid == 0) set_status(a.status, MI_ERR_TIMEOUT);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace mi
+
+namespace mi {
+
+// Host launcher, explicitly instantiated in attn_kernels_*.cu so that the four
+// pattern variants compile in parallel.
+template <int PAT>
+cudaError_t launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const AttnArgs& a, int n_row_blocks, cudaStream_t st);
+
+}  // namespace mi

@@ -1,0 +1,263 @@
+// estimate.cuh - online estimation of vertical-slash indices.
+//
+// Method (MInference talk slides, boteman.cn, "Step 2: Online Estimation of
+// Sparsity Indices"; README mirror, gittoolsai.com, "TL;DR"): the last 64
+// queries of each head are scored against every key with a causal softmax;
+// the probabilities are summed per key column (vertical score v) and per
+// diagonal offset o = q - j (slash score s).
+//
+// Layout of the work: one CTA takes a pair of q-heads that share a KV head
+// (128 query rows = 2 x 64, one UMMA M) and a chunk of 1024 keys, and runs
+// S = Q K^T per 128-key tile on the tensor cores (TMEM accumulator), so each
+// K tile is read once for both heads.
+//   pass 1  per row: running max m and sum z = sum exp2(x - m) over the chunk
+//   combine per row: merge the chunk partials in chunk order -> (m, 1/z)
+//   pass 2  per tile: a = exp2(x - m) / z into shared memory; column sums give
+//           v[j] for the tile's keys; sums along each diagonal give s[o].
+// A diagonal d (the key its row 63 meets) spans keys d-63..d, so it may start
+// in the previous tile: partial diagonal sums are carried from tile to tile,
+// and each pass-2 CTA also scores the 128 keys before its chunk (a halo tile
+// whose own outputs are discarded) so that every diagonal it writes is
+// complete.  Every output element is written by exactly one thread with a
+// fixed summation order: the scores are deterministic.
+#pragma once
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mi {
+
+struct EstArgs {
+  int N, group, n_pairs, NC;
+  float scale_log2;
+  float* part;   // [n_heads, 64, NC, 2]  pass-1 partials (m, z)
+  float* stats;  // [n_heads, 64, 2]      (m, 1/z)
+  float* vsc;    // [n_heads, N]          vertical scores
+  float* ssc;    // [n_heads, N]          slash scores, indexed by offset
+  int* status;
+  uint64_t wait_limit_ns;
+  HeadList heads;
+  int16_t pair_a[MI_MAX_HEADS];  // list slots; pair_b = -1: single head
+  int16_t pair_b[MI_MAX_HEADS];
+};
+
+struct EstSmem {
+  alignas(1024) uint8_t q[2][16384];
+  alignas(1024) uint8_t k[2][2][16384];
+  uint64_t q_full, k_full[2], k_empty[2], s_full[2], s_empty[2], mma_done;
+  uint32_t tmem;
+  int abort;
+  float carry[2][2][64];  // [buffer][head of pair][diagonal]
+};
+constexpr int kEstPitch = 129;  // fp32 row pitch of the probability tile
+constexpr size_t kEstSmem1 = sizeof(EstSmem) + 1024;
+constexpr size_t kEstSmem2 = sizeof(EstSmem) + 1024 + sizeof(float) * 128 * kEstPitch;
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+template <int PASS>
+__global__ void __launch_bounds__(256, 1)
+est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+           const __grid_constant__ EstArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  EstSmem& s = *reinterpret_cast<EstSmem*>(base);
+  float* A = reinterpret_cast<float*>(base + sizeof(EstSmem));  // pass 2 only: [128][kEstPitch]
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int pr = blockIdx.x, chunk = blockIdx.y;
+  const int slot_a = a.pair_a[pr], slot_b = a.pair_b[pr];
+  const int ha = a.heads.h[slot_a];
+  const int hb = slot_b >= 0 ? a.heads.h[slot_b] : ha;
+  const int g = ha / a.group;
+  const int N = a.N;
+  const int k_lo = chunk * kChunkKeys - ((PASS == 2 && chunk > 0) ? kBN : 0);
+  const int k_hi = min(N, (chunk + 1) * kChunkKeys);
+  const int T = cdiv(k_hi - k_lo, kBN);
+  const bool has_halo = (PASS == 2 && chunk > 0);
+
+  if (tid == 0) {
+    mbar_init(&s.q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.k_full[b], 1);
+      mbar_init(&s.k_empty[b], 1);
+      mbar_init(&s.s_full[b], 1);
+      mbar_init(&s.s_empty[b], 128);
+    }
+    mbar_init(&s.mma_done, 1);
+    s.abort = 0;
+    fence_mbar_init();
+  }
+  if (tid < 128) (&s.carry[0][0][0])[tid + 128] = 0.f;  // buffer 1 = carry into tile 0
+  if (warp == 0) {
+    tmem_alloc(&s.tmem, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem;
+  volatile int* abort = &s.abort;
+  const uint64_t lim = a.wait_limit_ns;
+
+  if (warp == 0) {
+    if (lane_id() == 0) {
+      const uint32_t id = idesc_bf16(128, kBN, 0);
+      bool ok = mbar_wait(&s.q_full, 0, abort, lim);
+      for (int t = 0; t < T && ok; ++t) {
+        const int b = t & 1;
+        ok = mbar_wait(&s.k_full[b], (t >> 1) & 1, abort, lim);
+        if (ok && t >= 2) ok = mbar_wait(&s.s_empty[b], ((t - 2) >> 1) & 1, abort, lim);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(smem_u32(s.q[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(smem_u32(s.k[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          umma_bf16_ss(tmem + b * 128, ad, bd, id, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s.s_full[b]);
+        umma_commit(&s.k_empty[b]);
+      }
+      umma_commit(&s.mma_done);
+      mbar_wait_drain(&s.mma_done, 0, lim);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane_id() == 0) {
+      mbar_arrive_expect_tx(&s.q_full, 4 * 8192);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(s.q[c], &map_q, &s.q_full, 64 * c, N - kLastQ, ha);
+        tma_load_3d(s.q[c] + 8192, &map_q, &s.q_full, 64 * c, N - kLastQ, hb);
+      }
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int b = t & 1;
+        if (t >= 2 && !mbar_wait(&s.k_empty[b], ((t - 2) >> 1) & 1, abort, lim)) break;
+        mbar_arrive_expect_tx(&s.k_full[b], 2 * 16384);
+        tma_load_3d(s.k[b][0], &map_k, &s.k_full[b], 0, k_lo + t * kBN, g);
+        tma_load_3d(s.k[b][1], &map_k, &s.k_full[b], 64, k_lo + t * kBN, g);
+        issued = t + 1;
+      }
+      mbar_wait_drain(&s.q_full, 0, lim);
+      for (int t = max(0, issued - 2); t < issued; ++t)
+        mbar_wait_drain(&s.k_full[t & 1], (t >> 1) & 1, lim);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int row = tid - 128;  // TMEM lane; rows 0-63 head a, 64-127 head b
+    const int hs = row >> 6, i = row & 63;
+    const int slot = hs ? slot_b : slot_a;
+    const int p_i = N - kLastQ + i;  // position of this query row
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float m = -INFINITY, z = 0.f, invz = 0.f;
+    if (PASS == 2 && slot >= 0) {
+      m = a.stats[((size_t)slot * kLastQ + i) * 2 + 0];
+      invz = a.stats[((size_t)slot * kLastQ + i) * 2 + 1];
+    }
+    for (int t = 0; t < T; ++t) {
+      const int b = t & 1;
+      // On a failed (timed-out) wait the loop still runs to the end with zeros, so
+      // that the four row warps keep meeting at the named barriers below.
+      const bool ok = mbar_wait_warp(&s.s_full[b], (t >> 1) & 1, abort, lim);
+      float x[128];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + b * 128 + c * 32, x + c * 32);
+        tc_fence_before();
+        mbar_arrive(&s.s_empty[b]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = 0.f;
+      }
+      const int j0 = k_lo + t * kBN;
+      // keys j0 + c with c <= lim_c are causal; rows of an absent second head are dropped
+      const int lim_c = (slot >= 0) ? p_i - j0 : -1;
+      if (PASS == 1) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          x[c] = (c <= lim_c) ? x[c] * a.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, x[c]);
+        }
+        const float mn = fmaxf(m, mx);
+        const float mb = (mn == -INFINITY) ? 0.f : mn;
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) acc += fast_exp2(x[c] - mb);
+        z = z * fast_exp2(m - mb) + acc;
+        m = mn;
+      } else {
+        float* Ar = A + row * kEstPitch;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          Ar[c] = (c <= lim_c) ? fast_exp2(x[c] * a.scale_log2 - m) * invz : 0.f;
+        named_bar_sync(1, 128);
+        const bool halo = has_halo && t == 0;
+        const float* cin = &s.carry[(t + 1) & 1][0][0];
+        float* cout = &s.carry[t & 1][0][0];
+        for (int J = row; J < 2 * 128 + 2 * 191; J += 128) {
+          if (J < 256) {  // column sums
+            const int hh = J >> 7, c = J & 127;
+            const int sl = hh ? slot_b : slot_a;
+            if (halo || sl < 0 || j0 + c >= N) continue;
+            const float* col = A + hh * 64 * kEstPitch + c;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < 64; ++r) acc += col[r * kEstPitch];
+            a.vsc[(size_t)sl * N + j0 + c] = acc;
+          } else {  // diagonal sums; diagonal e of the tile meets key j0 + e at row 63
+            const int Jd = J - 256;
+            const int hh = Jd / 191, e = Jd - hh * 191;
+            const int sl = hh ? slot_b : slot_a;
+            const int i_lo = max(0, 63 - e), i_hi = min(63, 190 - e);
+            const float* At = A + hh * 64 * kEstPitch;
+            float acc = 0.f;
+            for (int r = i_lo; r <= i_hi; ++r) acc += At[r * kEstPitch + (e - 63 + r)];
+            if (e < 63) acc += cin[hh * 64 + e];
+            if (e < 128) {
+              const int d = j0 + e;
+              if (!halo && sl >= 0 && d < N) a.ssc[(size_t)sl * N + (N - 1 - d)] = acc;
+            } else {
+              cout[hh * 64 + (e - 128)] = acc;
+            }
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+    }
+    if (PASS == 1 && slot >= 0) {
+      float* pp = a.part + (((size_t)slot * kLastQ + i) * a.NC + chunk) * 2;
+      pp[0] = m;
+      pp[1] = z;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (s.abort && tid == 0) set_status(a.status, MI_ERR_TIMEOUT);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// Merge the per-chunk (m, z) partials of every estimation row, in chunk order.
+__global__ void est_combine(const float* part, float* stats, int NC) {
+  const int slot = blockIdx.x, i = threadIdx.x;
+  const float* pp = part + ((size_t)slot * kLastQ + i) * NC * 2;
+  float m = -INFINITY;
+  for (int c = 0; c < NC; ++c) m = fmaxf(m, pp[2 * c]);
+  float z = 0.f;
+  for (int c = 0; c < NC; ++c) {
+    const float mc = pp[2 * c];
+    if (mc != -INFINITY) z += pp[2 * c + 1] * fast_exp2(mc - m);
+  }
+  stats[((size_t)slot * kLastQ + i) * 2 + 0] = m;
+  stats[((size_t)slot * kLastQ + i) * 2 + 1] = 1.f / z;
+}
+
+}  // namespace mi

@@ -1,0 +1,96 @@
+// vs_index.cuh - index structures of a vertical-slash head (one CTA per head).
+//
+// From the sorted column list V and offset list S the sparse attention kernel
+// needs, per head:
+//   offbits  bit o set for o in S             (element mask of diagonal tiles)
+//   colbits  bit j set for j in V             (columns inside contiguous tiles)
+//   dbits    bit delta set when some diagonal of S reaches key tile r - delta
+//            from query row block r (128-row blocks, 128-key tiles); an offset
+//            o = 128a + b touches distances a and, if b > 0, a + 1; distance 0
+//            (the local block) is always set
+//   dlist    the set distances in ascending order, dcount of them.
+// All are O(N/32 + k) words per head, the same for every row block.  The
+// entries are validated here: a value out of [0, N) or not strictly above its
+// predecessor raises MI_ERR_INDEX in the status word and is skipped; -1 is
+// padding, and a value after padding is invalid.
+#pragma once
+
+#include "common.cuh"
+
+namespace mi {
+
+struct VsIndexArgs {
+  int N, k_v, k_s, Nw, NT, NTw;
+  const int32_t* v_idx;
+  const int32_t* s_idx;
+  uint32_t* offbits;
+  uint32_t* colbits;
+  uint32_t* dbits;
+  int* dlist;
+  int* dcount;
+  int* status;
+};
+
+// 0: padding, 1: valid, -1: invalid.
+__device__ __forceinline__ int classify_entry(const int32_t* idx, int e, int N) {
+  const int v = idx[e];
+  if (v == -1) return 0;
+  if (v < 0 || v >= N) return -1;
+  if (e > 0) {
+    const int p = idx[e - 1];
+    if (p == -1 || p >= v) return -1;
+  }
+  return 1;
+}
+
+__global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ VsIndexArgs a) {
+  __shared__ uint32_t db[512];
+  __shared__ int scan[512];
+  const int n = blockIdx.x, tid = threadIdx.x;
+  uint32_t* off = a.offbits + (size_t)n * a.Nw;
+  uint32_t* col = a.colbits + (size_t)n * a.Nw;
+  for (int w = tid; w < a.Nw; w += 512) {
+    off[w] = 0u;
+    col[w] = 0u;
+  }
+  db[tid] = 0u;
+  __syncthreads();
+  const int32_t* si = a.s_idx + (size_t)n * a.k_s;
+  for (int e = tid; e < a.k_s; e += 512) {
+    const int c = classify_entry(si, e, a.N);
+    if (c < 0) set_status(a.status, MI_ERR_INDEX);
+    if (c != 1) continue;
+    const int o = si[e];
+    atomicOr(off + (o >> 5), 1u << (o & 31));
+    const int d0 = o >> 7;
+    atomicOr(&db[d0 >> 5], 1u << (d0 & 31));
+    if ((o & 127) && d0 + 1 < a.NT) atomicOr(&db[(d0 + 1) >> 5], 1u << ((d0 + 1) & 31));
+  }
+  const int32_t* vi = a.v_idx + (size_t)n * a.k_v;
+  for (int e = tid; e < a.k_v; e += 512) {
+    const int c = classify_entry(vi, e, a.N);
+    if (c < 0) set_status(a.status, MI_ERR_INDEX);
+    if (c != 1) continue;
+    const int j = vi[e];
+    atomicOr(col + (j >> 5), 1u << (j & 31));
+  }
+  if (tid == 0) atomicOr(&db[0], 1u);
+  __syncthreads();
+  // dbits to global, then the ascending list of set distances
+  const uint32_t word = (tid < a.NTw) ? db[tid] : 0u;
+  if (tid < a.NTw) a.dbits[(size_t)n * a.NTw + tid] = word;
+  scan[tid] = __popc(word);
+  __syncthreads();
+  for (int o = 1; o < 512; o <<= 1) {
+    const int y = (tid >= o) ? scan[tid - o] : 0;
+    __syncthreads();
+    scan[tid] += y;
+    __syncthreads();
+  }
+  int pos = scan[tid] - __popc(word);
+  int* dl = a.dlist + (size_t)n * a.NT;
+  for (uint32_t w = word; w; w &= w - 1) dl[pos++] = tid * 32 + (__ffs(w) - 1);
+  if (tid == 511) a.dcount[n] = scan[511];
+}
+
+}  // namespace mi

@@ -1,0 +1,186 @@
+/*
+ * mi.h - C ABI of libmi.so: dynamic sparse prefill attention on one GB300 (sm_103a).
+ *
+ * The method (MInference): every attention head follows one of three sparse
+ * patterns, fixed per head offline; for vertical-slash heads the concrete
+ * indices are estimated online from the input, and sparse kernels then compute
+ * only the kept part of causal attention.
+ *   - MInference README mirror, gittoolsai.com, "TL;DR" (offline pattern per
+ *     head, online approximation of the sparse indices, custom kernels) and
+ *     "Kernel-only usage" (vertical_slash_sparse_attention(q, k, v,
+ *     vertical_topk, slash), block_sparse_attention(q, k, v, topk),
+ *     streaming_forward(q, k, v, init_num, local_window_num)).
+ *   - MInference talk slides, boteman.cn (H. Jiang, "System-Algorithm
+ *     Co-design"): the A-shape, Vertical-Slash and block-sparse patterns;
+ *     "Step 2: Online Estimation of Sparsity Indices"; "Dynamic Sparse
+ *     Attention Calculation with PIT, FlashAttention".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  Tensors.  q: [Hq, N, d], k and v: [Hkv, N, d], out: [Hq, N, d]; all bf16
+ *    (mi_bf16 = raw bf16 bits), row-major and contiguous, DEVICE pointers owned
+ *    by the caller.  d must be 128 and N a multiple of 64 in [64, 2^21].
+ *    Grouped-query attention: q-head h reads KV head h / (Hq / Hkv);
+ *    Hq % Hkv == 0.  q, k, v, out must be 16-byte aligned.
+ *  Heads.  `heads` is a HOST array of n_heads distinct q-head indices in
+ *    [0, Hq) (at most MI_MAX_HEADS); NULL means all heads 0..Hq-1 and then
+ *    n_heads must equal Hq.  Per-head index arrays (v_idx, s_idx, blk_idx) are
+ *    laid out in the order of this list.  Only the listed heads' rows of
+ *    `out` (and `lse`) are written, so three pattern calls with disjoint head
+ *    lists fill one layer's output.
+ *  lse.  Optional DEVICE float [Hq, N]: natural-log sum of exp(q.k/sqrt(d))
+ *    over the kept keys of each row (NULL = not written).
+ *  Softmax scale is 1/sqrt(d) everywhere.
+ *  Workspace.  Every call takes caller-owned DEVICE scratch of at least
+ *    mi_workspace_bytes(op, ...) bytes, 256-byte aligned; its first word is the
+ *    call's device status.  The library allocates no device memory, keeps no
+ *    state between calls and never synchronizes inside a compute call: all
+ *    work is queued on `stream` (0 = legacy default stream).  Calls that share
+ *    a workspace must not overlap on the GPU.
+ *  Errors.  A call returns MI_OK or a negative MI_ERR_* at launch time
+ *    (argument, shape, workspace, CUDA launch errors); nothing crosses the ABI
+ *    as an exception.  Errors that depend on data (an index out of range or
+ *    unsorted, a pipeline wait that timed out) are written to the workspace
+ *    status word; mi_read_status() reads it.  mi_strerror() describes a code.
+ */
+#ifndef MI_H
+#define MI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mi_bf16;
+typedef struct CUstream_st* mi_stream_t; /* a cudaStream_t */
+
+#define MI_OK 0
+#define MI_ERR_ARG (-1)           /* NULL/misaligned pointer, bad head list, k < 0, ... */
+#define MI_ERR_SHAPE (-2)         /* d != 128, N % 64 != 0, Hq % Hkv != 0, last_q != 64, ... */
+#define MI_ERR_WORKSPACE (-3)     /* workspace NULL, misaligned or smaller than required */
+#define MI_ERR_CUDA (-4)          /* a CUDA call or kernel launch failed */
+#define MI_ERR_INDEX (-5)         /* device status: index out of range or not strictly ascending */
+#define MI_ERR_TIMEOUT (-6)       /* device status: a bounded pipeline wait expired */
+#define MI_ERR_UNIMPLEMENTED (-7) /* option not supported by this build */
+#define MI_ERR_DEVICE (-8)        /* current device is not an sm_103 GPU */
+
+#define MI_MAX_HEADS 256
+#define MI_HEAD_DIM 128
+#define MI_LAST_Q 64
+#define MI_BLOCK 64
+#define MI_MAX_KV 4096 /* largest vertical budget the sparse attention kernel accepts */
+
+/* ops for mi_workspace_bytes */
+#define MI_OP_VS_ESTIMATE 1
+#define MI_OP_VS_SPARSE_ATTN 2
+#define MI_OP_BLOCK_SPARSE_ATTN 3
+#define MI_OP_ASHAPE_ATTN 4
+#define MI_OP_DENSE_CAUSAL_ATTN 5
+
+/* flags for mi_block_sparse_attn */
+#define MI_IDX_GIVEN 1
+
+/*
+ * Bytes of workspace `op` needs.  Unused arguments may be 0.  Returns 0 for an
+ * unknown op or impossible sizes.
+ */
+size_t mi_workspace_bytes(int op, int n_heads, int Hkv, int N, int k_v, int k_s, int topk);
+
+/*
+ * Online estimation of vertical-slash indices for the listed heads.
+ * Slides: "Step 2: Online Estimation of Sparsity Indices"; README mirror,
+ * "Kernel-only usage" (vertical_topk, slash).
+ *
+ * For each listed q-head h with KV head g and the query rows
+ * p_i = N - last_q + i (i < last_q):
+ *   l_ij = q[h,p_i].k[g,j] / sqrt(d) for j <= p_i, a_ij = softmax_j(l_ij),
+ *   vertical score  v[j] = sum_i a_ij,
+ *   slash score     s[o] = sum_i a_{i, p_i - o}   (diagonal offset o = q - j).
+ * v_idx[n, 0..k_v') receives the k_v' = min(k_v, N) columns with the largest
+ * v and s_idx[n, 0..k_s') the k_s' = min(k_s, N) offsets with the largest s
+ * (ties: lower index first), each sorted ascending.  v_idx is [n_heads, k_v]
+ * and s_idx [n_heads, k_s] int32 DEVICE arrays; entries beyond k_v' / k_s'
+ * are set to -1.  last_q must be 64; k_v, k_s >= 0 (0 is legal).
+ * Scores are accumulated in fp32 from bf16 tensor-core products.
+ */
+int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
+                   const int32_t* heads, int n_heads, int last_q, int k_v, int k_s,
+                   int32_t* v_idx, int32_t* s_idx, void* workspace, size_t ws_bytes,
+                   mi_stream_t stream);
+
+/*
+ * Vertical-slash sparse attention with given indices.
+ * Slides: "Vertical-Slash" pattern and "Dynamic Sparse Attention Calculation
+ * with PIT, FlashAttention"; README mirror: vertical_slash_sparse_attention.
+ *
+ * Row q of head h keeps key j iff j <= q and (j < 64 or j/64 == q/64 or
+ * j in v_idx[n] or q - j in s_idx[n]); a key kept by several rules counts
+ * once.  out[h, q] = softmax over kept keys of q.k/sqrt(d), times V.
+ * v_idx: [n_heads, k_v] and s_idx: [n_heads, k_s] int32 DEVICE arrays, each row
+ * strictly ascending, values in [0, N); a trailing run of -1 is allowed and
+ * ignored (the layout mi_vs_estimate writes).  An entry out of range or out of
+ * order sets MI_ERR_INDEX in the status word and is skipped.  k_v <= MI_MAX_KV.
+ */
+int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
+                      int N, int d, const int32_t* heads, int n_heads, const int32_t* v_idx,
+                      int k_v, const int32_t* s_idx, int k_s, mi_bf16* out, float* lse,
+                      void* workspace, size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * Block-sparse attention over 64x64 blocks.
+ * Slides: "block-sparse" pattern; README mirror: block_sparse_attention(q, k, v, topk).
+ *
+ * Query block r (rows 64r..64r+63) keeps key blocks c <= r.  Unless
+ * (flags & MI_IDX_GIVEN), the blocks are chosen here: the top-min(topk, r+1)
+ * blocks by sigma[r, c] = mean(q rows of block r) . mean(k rows of block c)
+ * (ties: lower c), and written to blk_idx.  With MI_IDX_GIVEN, blk_idx is read
+ * (a row that is not ascending, exceeds r or has a value after -1 padding
+ * sets MI_ERR_INDEX).  blk_idx: [n_heads, N/64, topk] int32 DEVICE array; each
+ * row ascending, padded with -1 after the last selected block.  Row q keeps j
+ * iff j <= q and j/64 is selected for q/64.  block must be 64,
+ * 1 <= topk <= MI_MAX_KV / 2.
+ */
+int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
+                         int N, int d, const int32_t* heads, int n_heads, int block, int topk,
+                         int32_t* blk_idx, int flags, mi_bf16* out, float* lse, void* workspace,
+                         size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * A-shape attention: attention sinks plus a local window.
+ * Slides: "A-shape" pattern; README mirror: streaming_forward(q, k, v,
+ * init_num, local_window_num).
+ *
+ * Row q keeps j iff j <= q and (j < n_init or q - j < window); both sizes in
+ * tokens, n_init >= 0, window >= 1.
+ */
+int mi_ashape_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N,
+                   int d, const int32_t* heads, int n_heads, int n_init, int window, mi_bf16* out,
+                   float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * Dense causal attention (row q keeps every j <= q): the FlashAttention
+ * baseline the pages measure the sparse kernels against (slides: "Latency at
+ * 1M tokens on a single A100: FlashAttn 30 mins vs MInference 3 mins").
+ */
+int mi_dense_causal_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
+                         int N, int d, const int32_t* heads, int n_heads, mi_bf16* out,
+                         float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then returns the status word of the last call that
+ * used `workspace` (MI_OK, MI_ERR_INDEX or MI_ERR_TIMEOUT), or MI_ERR_CUDA if
+ * the synchronization or the read failed.
+ */
+int mi_read_status(const void* workspace, mi_stream_t stream);
+
+/* Static description of an MI_* code; for MI_ERR_CUDA the text of the last
+ * CUDA error seen by this thread is returned (thread-local buffer). */
+const char* mi_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MI_H */

@@ -1,0 +1,51 @@
+"""libmi.so loads on a GPU-less host and exports every entry point of include/mi.h."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dynamic_sparse_attention_vertical_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "mi.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(mi_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return B.load()
+
+
+def test_header_declares_the_five_calls():
+    names = _declared()
+    for n in ("mi_vs_estimate", "mi_vs_sparse_attn", "mi_block_sparse_attn", "mi_ashape_attn",
+              "mi_dense_causal_attn"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(names) == set(B.SYMBOLS)
+    raw = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_strerror_and_workspace_sizes_need_no_gpu(lib):
+    assert B.mi_strerror(0) == "success"
+    for code in range(-8, 0):
+        assert B.mi_strerror(code) and "unknown" not in B.mi_strerror(code)
+    assert B.mi_workspace_bytes(B.MI_OP_DENSE_CAUSAL_ATTN, 32, 8, 4096) == 256
+    est = B.mi_workspace_bytes(B.MI_OP_VS_ESTIMATE, 32, 8, 131072)
+    assert est >= 2 * 32 * 131072 * 4 and est % 256 == 0
+    vs = B.mi_workspace_bytes(B.MI_OP_VS_SPARSE_ATTN, 24, 8, 131072)
+    assert vs >= 2 * 24 * 131072 // 8
+    assert B.mi_workspace_bytes(99, 1, 1, 64) == 0

@@ -1,0 +1,278 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Outputs: max-abs <= 2e-2, mean-abs <= 2e-3 and relative Frobenius <= 1e-2 per
+head, bf16 GPU against the fp64 oracle.  Indices: bit-exact on margin-planted
+inputs; elsewhere equal up to elements scoring at the top-k boundary.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from dynamic_sparse_attention_vertical_gb300 import binding as B
+from dynamic_sparse_attention_vertical_gb300 import inputs as I
+from tests.parity import REL_FRO, assert_close, band_agree, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()
+
+
+def _dev(x):
+    return x.q.to(DEV), x.k.to(DEV), x.v.to(DEV)
+
+
+def _rand_inputs(Hq, Hkv, N, seed):
+    return I.literal_inputs(Hq, Hkv, N, n_cols=0, n_offsets=0, seed=seed)
+
+
+# ----------------------------------------------------------------- dense ----
+
+@pytest.mark.parametrize("N", [128, 320, 1024])
+def test_dense_matches_oracle(N):
+    Hq, Hkv = 2, 1
+    x = _rand_inputs(Hq, Hkv, N, seed=N)
+    q, k, v = _dev(x)
+    lse = torch.full((Hq, N), float("nan"), device=DEV)
+    out = B.mi_dense_causal_attn(q, k, v, lse=lse)
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    rows = np.arange(N)
+    for h in range(Hq):
+        g = O.kv_head(h, Hq, Hkv)
+        ref, rl = O.attention_rows(x.q[h], x.k[g], x.v[g], rows,
+                                   lambda r: O.causal_mask_rows(N, r))
+        assert_close(o[h], ref, f"dense h{h}")
+        assert np.abs(l[h] - rl).max() < 1e-3
+
+
+def test_dense_writes_only_listed_heads():
+    Hq, Hkv, N = 4, 2, 256
+    x = _rand_inputs(Hq, Hkv, N, seed=3)
+    q, k, v = _dev(x)
+    out = torch.full_like(q, 7.0)
+    B.mi_dense_causal_attn(q, k, v, heads=[3, 0], out=out)
+    o = out.float().cpu().numpy()
+    assert np.all(o[1] == 7.0) and np.all(o[2] == 7.0)
+    for h in (3, 0):
+        g = O.kv_head(h, Hq, Hkv)
+        ref, _ = O.attention_rows(x.q[h], x.k[g], x.v[g], np.arange(N),
+                                  lambda r: O.causal_mask_rows(N, r))
+        assert_close(o[h], ref, f"dense subset h{h}")
+
+
+# --------------------------------------------------------------- A-shape ----
+
+@pytest.mark.parametrize("N,n_init,window",
+                         [(640, 128, 256), (2048, 100, 300), (1024, 0, 1), (512, 64, 4096)])
+def test_ashape_matches_oracle(N, n_init, window):
+    Hq, Hkv = 2, 2
+    x = _rand_inputs(Hq, Hkv, N, seed=N + window)
+    q, k, v = _dev(x)
+    out = B.mi_ashape_attn(q, k, v, n_init=n_init, window=window)
+    o = out.float().cpu().numpy()
+    for h in range(Hq):
+        ref, _ = O.attention_rows(x.q[h], x.k[h], x.v[h], np.arange(N),
+                                  lambda r: O.ashape_mask_rows(N, r, n_init, window))
+        assert_close(o[h], ref, f"ashape h{h}")
+    if n_init == 0 and window == 1:  # every row keeps only itself
+        assert torch.equal(out.cpu(), x.v)
+
+
+# ------------------------------------------------------- vertical-slash ----
+
+def _vs_check(x, heads, v_idx, s_idx, out, rows=None):
+    Hq, N = x.q.shape[0], x.q.shape[1]
+    Hkv = x.k.shape[0]
+    o = out.float().cpu().numpy()
+    rows = np.arange(N) if rows is None else rows
+    for n, h in enumerate(heads):
+        g = O.kv_head(h, Hq, Hkv)
+        vi = np.asarray(v_idx[n])
+        vi = vi[vi >= 0]
+        si = np.asarray(s_idx[n])
+        si = si[si >= 0]
+        ref, _ = O.attention_rows(x.q[h], x.k[g], x.v[g], rows,
+                                  lambda r: O.vs_mask_rows(N, r, vi, si))
+        assert_close(o[h][rows], ref, f"vs h{h}")
+
+
+@pytest.mark.parametrize("N", [2112, 4096])
+def test_vs_attention_with_oracle_indices(N):
+    Hq, Hkv = 2, 1
+    x = I.literal_inputs(Hq, Hkv, N, n_cols=8, n_offsets=4, seed=N)
+    vis, sis = [], []
+    for h in range(Hq):
+        vi, si, _, _ = O.vs_estimate(x.q[h], x.k[0], 64, 64, 32)
+        vis.append(vi)
+        sis.append(si)
+    q, k, v = _dev(x)
+    v_idx = torch.tensor(np.stack(vis), dtype=torch.int32, device=DEV)
+    s_idx = torch.tensor(np.stack(sis), dtype=torch.int32, device=DEV)
+    out = B.mi_vs_sparse_attn(q, k, v, v_idx, s_idx)
+    _vs_check(x, range(Hq), vis, sis, out)
+
+
+def test_vs_attention_gathered_columns():
+    """Many columns outside the diagonal tiles: several gathered column tiles per block."""
+    N, Hq, Hkv = 4096, 2, 1
+    x = _rand_inputs(Hq, Hkv, N, seed=11)
+    rng = np.random.default_rng(5)
+    vis = [np.sort(rng.choice(np.arange(N), size=300, replace=False)) for _ in range(Hq)]
+    sis = [np.array([5, 700, 2000]), np.array([0, 1, 2, 3, 129, 4000])]
+    q, k, v = _dev(x)
+    v_idx = torch.tensor(np.stack(vis), dtype=torch.int32, device=DEV)
+    s_idx = torch.full((Hq, 6), -1, dtype=torch.int32)
+    for h in range(Hq):
+        s_idx[h, : len(sis[h])] = torch.tensor(sis[h])
+    out = B.mi_vs_sparse_attn(q, k, v, v_idx, s_idx.to(DEV))
+    _vs_check(x, range(Hq), vis, sis, out)
+
+
+def test_vs_full_budget_is_dense():
+    N, Hq, Hkv = 384, 1, 1
+    x = _rand_inputs(Hq, Hkv, N, seed=2)
+    q, k, v = _dev(x)
+    v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=N, k_s=N)
+    assert v_idx.cpu().tolist() == [list(range(N))] and s_idx.cpu().tolist() == [list(range(N))]
+    out = B.mi_vs_sparse_attn(q, k, v, v_idx, s_idx)
+    dense = B.mi_dense_causal_attn(q, k, v)
+    ref, _ = O.attention_rows(x.q[0], x.k[0], x.v[0], np.arange(N),
+                              lambda r: O.causal_mask_rows(N, r))
+    assert_close(out.float().cpu().numpy()[0], ref, "vs full budget")
+    assert_close(dense.float().cpu().numpy()[0], ref, "dense")
+
+
+@pytest.mark.parametrize("Hq,Hkv,N,k_v,k_s",
+                         [(4, 2, 2048, 64, 32), (2, 1, 4160, 100, 50), (1, 1, 4096, 64, 32)])
+def test_vs_estimate_margin_planted_exact(Hq, Hkv, N, k_v, k_s):
+    x = I.margin_inputs(Hq, Hkv, N, k_v, k_s, seed=N + k_v)
+    q, k, _ = _dev(x)
+    v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=k_v, k_s=k_s)
+    vi, si = v_idx.cpu().numpy(), s_idx.cpu().numpy()
+    for h in range(Hq):
+        g = O.kv_head(h, Hq, Hkv)
+        assert vi[h].tolist() == x.planted_cols[g].tolist()
+        assert si[h].tolist() == x.planted_offsets[g].tolist()
+
+
+def test_vs_estimate_literal_band():
+    """The single-head 4K configuration: planted indices found, the rest up to boundary ties."""
+    N = 4096
+    x = I.literal_inputs(1, 1, N, n_cols=8, n_offsets=4, seed=1)
+    q, k, _ = _dev(x)
+    v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=64, k_s=32)
+    vi_ref, si_ref, v, s = O.vs_estimate(x.q[0], x.k[0], 64, 64, 32)
+    band_agree(v_idx.cpu().numpy()[0], vi_ref, v, 64, must_have=x.planted_cols[0].numpy())
+    band_agree(s_idx.cpu().numpy()[0], si_ref, s, 32, must_have=x.planted_offsets[0].numpy())
+
+
+def test_vs_estimate_budget_edges():
+    N = 256
+    x = _rand_inputs(2, 1, N, seed=9)
+    q, k, _ = _dev(x)
+    v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=0, k_s=5)
+    assert v_idx.shape == (2, 0) and s_idx.shape == (2, 5)
+    v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=N + 10, k_s=3)
+    vi = v_idx.cpu().numpy()
+    assert vi[:, :N].tolist() == [list(range(N))] * 2 and np.all(vi[:, N:] == -1)
+    for h in range(2):
+        _, si_ref, _, s = O.vs_estimate(x.q[h], x.k[0], 64, 0, 3)
+        band_agree(s_idx.cpu().numpy()[h], si_ref, s, 3)
+
+
+def test_vs_end_to_end_and_mutation():
+    """Estimate + attention; removing one selected column must break the tolerance."""
+    N, Hq, Hkv = 4096, 2, 1
+    x = I.literal_inputs(Hq, Hkv, N, n_cols=8, n_offsets=4, seed=21)
+    g = torch.Generator().manual_seed(77)
+    x.v = torch.randn(x.v.shape, generator=g).to(torch.bfloat16)  # V ~ N(0, 1)
+    q, k, v = _dev(x)
+    v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=64, k_s=32)
+    out = B.mi_vs_sparse_attn(q, k, v, v_idx, s_idx)
+    vi, si = v_idx.cpu().numpy(), s_idx.cpu().numpy()
+    _vs_check(x, range(Hq), vi, si, out)
+    # mutation: drop a planted column from head 0's list
+    col = int(x.planted_cols[0][0])
+    keep = vi[0][vi[0] != col]
+    assert len(keep) == len(vi[0]) - 1
+    mut = torch.full_like(v_idx[:1], -1)
+    mut[0, : len(keep)] = torch.tensor(keep, dtype=torch.int32, device=DEV)
+    out_m = B.mi_vs_sparse_attn(q, k, v, mut, s_idx[:1].contiguous(), heads=[0])
+    rows = np.arange(((col // 128) + 1) * 128, N)
+    ref, _ = O.attention_rows(x.q[0], x.k[0], x.v[0], rows,
+                              lambda r: O.vs_mask_rows(N, r, vi[0], si[0]))
+    assert rel_fro(out_m.float().cpu().numpy()[0][rows], ref) > REL_FRO
+
+
+# ----------------------------------------------------------- block-sparse ----
+
+def test_block_sparse_select_and_attention():
+    N, Hq, Hkv, topk = 2048, 2, 1, 8
+    x = I.literal_inputs(Hq, Hkv, N, n_cols=4, n_offsets=2, seed=31)
+    q, k, v = _dev(x)
+    out, blk = B.mi_block_sparse_attn(q, k, v, topk=topk)
+    bl = blk.cpu().numpy()
+    o = out.float().cpu().numpy()
+    for h in range(Hq):
+        sig = O.block_scores(x.q[h], x.k[0])
+        ref_sel = O.block_sparse_select(x.q[h], x.k[0], topk)
+        for r in range(N // 64):
+            got = bl[h, r][bl[h, r] >= 0]
+            assert np.all(np.diff(got) > 0) and got.max() <= r
+            band_agree(got, ref_sel[r], sig[r, : r + 1], min(topk, r + 1), rel_band=1e-3)
+        sel = [row[row >= 0] for row in bl[h]]
+        ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], np.arange(N),
+                                  lambda r: O.block_sparse_mask_rows(N, r, sel))
+        assert_close(o[h], ref, f"block h{h}")
+    # the same with the oracle's own selection passed in
+    given = np.full((Hq, N // 64, topk), -1, dtype=np.int32)
+    refs = []
+    for h in range(Hq):
+        ref_sel = O.block_sparse_select(x.q[h], x.k[0], topk)
+        refs.append(ref_sel)
+        for r, s in enumerate(ref_sel):
+            given[h, r, : len(s)] = s
+    out2, _ = B.mi_block_sparse_attn(q, k, v, topk=topk, blk_idx=torch.tensor(given, device=DEV),
+                                     given=True)
+    for h in range(Hq):
+        ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], np.arange(N),
+                                  lambda r: O.block_sparse_mask_rows(N, r, refs[h]))
+        assert_close(out2.float().cpu().numpy()[h], ref, f"block given h{h}")
+
+
+# ----------------------------------------------------------------- errors ----
+
+def test_argument_and_index_errors():
+    N = 256
+    x = _rand_inputs(2, 1, N, seed=4)
+    q, k, v = _dev(x)
+    with pytest.raises(B.MIError) as e:
+        B.mi_dense_causal_attn(q[:, :200].contiguous(), k[:, :200].contiguous(),
+                               v[:, :200].contiguous())
+    assert e.value.code == B.MI_ERR_SHAPE
+    with pytest.raises(B.MIError) as e:
+        B.mi_dense_causal_attn(q, k, v, heads=[0, 0])
+    assert e.value.code == B.MI_ERR_ARG
+    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    with pytest.raises(B.MIError) as e:
+        B.mi_dense_causal_attn(q, k, v, workspace=ws[1:257])
+    assert e.value.code == B.MI_ERR_WORKSPACE
+    # unsorted / out-of-range indices: reported through the status word, no fault
+    bad_v = torch.tensor([[5, 3, 9], [1, 2, 3]], dtype=torch.int32, device=DEV)
+    s_idx = torch.tensor([[0, 7], [1, N + 5]], dtype=torch.int32, device=DEV)
+    ws = torch.empty(B.mi_workspace_bytes(B.MI_OP_VS_SPARSE_ATTN, 2, 1, N), dtype=torch.uint8,
+                     device=DEV)
+    B.mi_vs_sparse_attn(q, k, v, bad_v, s_idx, workspace=ws)
+    assert B.mi_read_status(ws) == B.MI_ERR_INDEX
+    good_v = torch.tensor([[3, 5, 9], [1, 2, 3]], dtype=torch.int32, device=DEV)
+    good_s = torch.tensor([[0, 7], [1, -1]], dtype=torch.int32, device=DEV)
+    B.mi_vs_sparse_attn(q, k, v, good_v, good_s, workspace=ws)
+    assert B.mi_read_status(ws) == B.MI_OK

@@ -45,7 +45,7 @@ block_select_kernel(const float* qbar, const float* kbar, int NB, int group, Hea
                     int topk, int32_t* blk_idx) {
   extern __shared__ float sig[];  // [NB]
   __shared__ SelectSmem sm;
-  __shared__ float qrow[kD];
+  __shared__ __align__(16) float qrow[kD];
   const int r = blockIdx.x, slot = blockIdx.y;
   const int g = heads.h[slot] / group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -61,9 +61,10 @@ block_select_kernel(const float* qbar, const float* kbar, int NB, int group, Hea
   }
   __syncthreads();
   int32_t* out = blk_idx + ((size_t)slot * NB + r) * topk;
+  const int kk = min(topk, r + 1);  // >= 1
   const float* sp = sig;
-  topk_select_sorted<256>([sp](int i) { return float_key(sp[i]); }, r + 1, min(topk, r + 1), out,
-                          topk, sm);
+  topk_select_sorted<256>([sp](int i) { return float_key(sp[i]); }, r + 1, kk, out, sm);
+  for (int i = kk + tid; i < topk; i += 256) out[i] = -1;
 }
 
 // With caller-given block lists: flag any row that is not ascending, out of

@@ -24,17 +24,13 @@ struct SelectSmem {
 };
 
 // key_at(i) -> order-preserving uint32 key of element i (see float_key).
-// Writes the k' = min(k, n) selected indices ascending to out[0..k'), and -1 to
-// out[k'..out_len).  All NT threads of the block must call it.
+// Requires 1 <= k <= n.  Writes the k selected indices ascending to out[0..k).
+// All NT threads of the block must call it.  The function has no early exit:
+// every thread runs every block barrier in it.
 template <int NT, class F>
-__device__ void topk_select_sorted(F key_at, int n, int k, int* out, int out_len, SelectSmem& sm) {
+__device__ void topk_select_sorted(F key_at, int n, int k, int* out, SelectSmem& sm) {
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  k = max(0, min(k, n));
-  if (k == 0 || k == n) {
-    for (int i = tid; i < out_len; i += NT) out[i] = (i < k) ? i : -1;
-    return;
-  }
   uint32_t prefix = 0, pmask = 0;
   int rem = k;
   for (int pass = 0; pass < 4; ++pass) {
@@ -125,11 +121,11 @@ __device__ void topk_select_sorted(F key_at, int n, int k, int* out, int out_len
     gb += __popc(bg);
     eb += __popc(be);
   }
-  for (int i = k + tid; i < out_len; i += NT) out[i] = -1;
   __syncthreads();
 }
 
-// T1: top-k of the vertical (y = 0) or slash (y = 1) scores of every listed head.
+// T1: top-k of the vertical (y = 0) or slash (y = 1) scores of every listed head;
+// k > N keeps all N indices, and the row is padded with -1 up to k.
 __global__ void __launch_bounds__(1024)
 vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int32_t* v_idx,
                int32_t* s_idx) {
@@ -138,9 +134,10 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
   const bool vert = blockIdx.y == 0;
   const float* x = (vert ? vsc : ssc) + (size_t)slot * N;
   const int k = vert ? k_v : k_s;
-  if (k == 0) return;
+  const int kk = min(k, N);
   int32_t* out = (vert ? v_idx : s_idx) + (size_t)slot * k;
-  topk_select_sorted<1024>([x](int i) { return float_key(__ldg(x + i)); }, N, k, out, k, sm);
+  if (kk > 0) topk_select_sorted<1024>([x](int i) { return float_key(__ldg(x + i)); }, N, kk, out, sm);
+  for (int i = kk + threadIdx.x; i < k; i += 1024) out[i] = -1;
 }
 
 }  // namespace mi

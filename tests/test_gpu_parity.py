@@ -170,8 +170,14 @@ def test_vs_estimate_literal_band():
     q, k, _ = _dev(x)
     v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=64, k_s=32)
     vi_ref, si_ref, v, s = O.vs_estimate(x.q[0], x.k[0], 64, 64, 32)
-    band_agree(v_idx.cpu().numpy()[0], vi_ref, v, 64, must_have=x.planted_cols[0].numpy())
-    band_agree(s_idx.cpu().numpy()[0], si_ref, s, 32, must_have=x.planted_offsets[0].numpy())
+    # literal planting does not force every planted index into the top-k (the
+    # oracle ranks some planted columns in the hundreds); the ones the oracle
+    # keeps must be kept by the GPU too
+    pc = [c for c in x.planted_cols[0].tolist() if c in set(vi_ref.tolist())]
+    po = [o for o in x.planted_offsets[0].tolist() if o in set(si_ref.tolist())]
+    assert len(po) == len(x.planted_offsets[0])  # planted diagonals do rank first here
+    band_agree(v_idx.cpu().numpy()[0], vi_ref, v, 64, must_have=pc)
+    band_agree(s_idx.cpu().numpy()[0], si_ref, s, 32, must_have=po)
 
 
 def test_vs_estimate_budget_edges():

@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark: one long-context decoder layer of dynamic sparse prefill attention.
+
+A step is one pass of the whole hot path over one layer's attention: online
+estimation of the vertical-slash heads' indices, vertical-slash sparse
+attention, block-sparse selection + attention and A-shape attention, all
+through the C ABI of libmi.so.  The default workload is the mixed-pattern
+layer at 128K tokens (32 q heads / 8 KV heads, d = 128; 24 vertical-slash
+heads with 1000 columns / 6096 diagonals, 4 block-sparse heads keeping 100
+blocks per row block, 4 A-shape heads with 128 sink tokens and a 4096-token
+window) on seeded synthetic inputs.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead, on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "ms/layer & dense-equivalent speedup at 128K/1M tokens; % of bf16 tensor peak"
+
+WORKLOADS = {
+    "mixed-128k": dict(Hq=32, Hkv=8, N=131072, n_vs=24, n_block=4, n_ashape=4, k_v=1000, k_s=6096,
+                       topk=100, n_init=128, window=4096, n_cols=16, n_offsets=8, seed=3),
+    "vs-32k": dict(Hq=32, Hkv=8, N=32768, n_vs=32, n_block=0, n_ashape=0, k_v=1000, k_s=6096,
+                   topk=100, n_init=128, window=4096, n_cols=16, n_offsets=8, seed=2),
+    "vs-1m": dict(Hq=32, Hkv=8, N=1048576, n_vs=32, n_block=0, n_ashape=0, k_v=1000, k_s=6096,
+                  topk=100, n_init=128, window=4096, n_cols=16, n_offsets=8, seed=4),
+    "vs-4k": dict(Hq=1, Hkv=1, N=4096, n_vs=1, n_block=0, n_ashape=0, k_v=64, k_s=32, topk=100,
+                  n_init=128, window=4096, n_cols=8, n_offsets=4, seed=1),
+}
+KERNELS_PER_STEP = {"vs": 6, "block": 4, "ashape": 1}  # estimate 4 + index 1 + attention 1, ...
+
+
+def describe(w):
+    parts = [f"{w['Hq']}q/{w['Hkv']}kv heads, d=128, N={w['N']}"]
+    if w["n_vs"]:
+        parts.append(f"{w['n_vs']} vertical-slash heads (top {w['k_v']} columns / {w['k_s']} diagonals)")
+    if w["n_block"]:
+        parts.append(f"{w['n_block']} block-sparse heads (top {w['topk']} 64x64 blocks)")
+    if w["n_ashape"]:
+        parts.append(f"{w['n_ashape']} A-shape heads ({w['n_init']} sink + {w['window']} window)")
+    return "; ".join(parts)
+
+
+def head_patterns(w):
+    g = torch.Generator().manual_seed(w["seed"])
+    perm = torch.randperm(w["Hq"], generator=g).tolist()
+    a, b = w["n_vs"], w["n_vs"] + w["n_block"]
+    return sorted(perm[:a]), sorted(perm[a:b]), sorted(perm[b:b + w["n_ashape"]])
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks ----
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for ln in f:
+                    p = [x.strip() for x in ln.split(",")]
+                    if len(p) >= 9:
+                        rows.append(p)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        load = [s for s in sm if mx and s > 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- the layer ----
+
+class Layer:
+    """Device tensors, index buffers and workspaces for one layer; step() runs the hot path."""
+
+    def __init__(self, B, w, q, k, v):
+        self.B, self.w = B, w
+        self.q, self.k, self.v = q, k, v
+        dev = q.device
+        N, Hkv = w["N"], w["Hkv"]
+        self.vs, self.blk, self.ash = head_patterns(w)
+        self.out = torch.zeros_like(q)
+        nv, nb = len(self.vs), len(self.blk)
+        self.v_idx = torch.empty((max(nv, 1), w["k_v"]), dtype=torch.int32, device=dev)
+        self.s_idx = torch.empty((max(nv, 1), w["k_s"]), dtype=torch.int32, device=dev)
+        self.blk_idx = torch.empty((max(nb, 1), N // 64, w["topk"]), dtype=torch.int32, device=dev)
+
+        def ws(op, n):
+            return torch.empty(max(256, B.mi_workspace_bytes(op, max(n, 1), Hkv, N, w["k_v"], w["k_s"], w["topk"])),
+                               dtype=torch.uint8, device=dev)
+        self.ws_est = ws(B.MI_OP_VS_ESTIMATE, nv)
+        self.ws_vs = ws(B.MI_OP_VS_SPARSE_ATTN, nv)
+        self.ws_blk = ws(B.MI_OP_BLOCK_SPARSE_ATTN, nb)
+        self.ws_ash = ws(B.MI_OP_ASHAPE_ATTN, 1)
+        self.ws_dense = ws(B.MI_OP_DENSE_CAUSAL_ATTN, 1)
+        self.kernels_per_step = (KERNELS_PER_STEP["vs"] if nv else 0) + (KERNELS_PER_STEP["block"] if nb else 0) \
+            + (KERNELS_PER_STEP["ashape"] if self.ash else 0)
+
+    def step(self, ev=None):
+        B, w = self.B, self.w
+        if ev:
+            ev[0].record()
+        if self.vs:
+            B.mi_vs_estimate(self.q, self.k, heads=self.vs, k_v=w["k_v"], k_s=w["k_s"], v_idx=self.v_idx,
+                             s_idx=self.s_idx, workspace=self.ws_est)
+            if ev:
+                ev[1].record()
+            B.mi_vs_sparse_attn(self.q, self.k, self.v, self.v_idx, self.s_idx, heads=self.vs, out=self.out,
+                                workspace=self.ws_vs)
+        elif ev:
+            ev[1].record()
+        if ev:
+            ev[2].record()
+        if self.blk:
+            B.mi_block_sparse_attn(self.q, self.k, self.v, topk=w["topk"], heads=self.blk, blk_idx=self.blk_idx,
+                                   out=self.out, workspace=self.ws_blk)
+        if ev:
+            ev[3].record()
+        if self.ash:
+            B.mi_ashape_attn(self.q, self.k, self.v, n_init=w["n_init"], window=w["window"], heads=self.ash,
+                             out=self.out, workspace=self.ws_ash)
+        if ev:
+            ev[4].record()
+
+    def dense(self):
+        self.B.mi_dense_causal_attn(self.q, self.k, self.v, out=self.out, workspace=self.ws_dense)
+
+    def check_status(self):
+        for ws in (self.ws_est, self.ws_vs, self.ws_blk, self.ws_ash):
+            st = self.B.mi_read_status(ws)
+            if st not in (0,):
+                raise RuntimeError(f"device status {st}: {self.B.mi_strerror(st)}")
+
+    def work(self):
+        """(algorithmic FLOPs per head group, executed tile FLOPs) of one step, from the indices."""
+        from dynamic_sparse_attention_vertical_gb300 import flops as F
+        w, N = self.w, self.w["N"]
+        dev = self.q.device
+        alg = {"vs": 0, "block": 0, "ashape": 0}
+        tiles = {"vs": 0, "block": 0, "ashape": 0}
+        vi = self.v_idx.cpu().numpy()
+        si = self.s_idx.cpu().numpy()
+        for n in range(len(self.vs)):
+            alg["vs"] += int(F.vs_kept_per_row(N, vi[n], si[n], device=dev).sum())
+            tiles["vs"] += F.vs_tiles(N, vi[n], si[n])
+        bl = self.blk_idx.cpu().numpy()
+        for n in range(len(self.blk)):
+            sel = [r[r >= 0] for r in bl[n]]
+            alg["block"] += int(F.block_kept_per_row(N, sel).sum())
+            tiles["block"] += F.block_tiles(sel)
+        if self.ash:
+            alg["ashape"] = len(self.ash) * int(F.ashape_kept_per_row(N, w["n_init"], w["window"]).sum())
+            tiles["ashape"] = len(self.ash) * F.ashape_tiles(N, w["n_init"], w["window"])
+        return ({k2: 4 * F.D * v2 for k2, v2 in alg.items()}, {k2: F.TILE_FLOPS * v2 for k2, v2 in tiles.items()})
+
+
+def make_inputs(w, variant, device):
+    from dynamic_sparse_attention_vertical_gb300 import inputs as I
+    kw = dict(n_cols=w["n_cols"], n_offsets=w["n_offsets"], seed=w["seed"], device=device)
+    if variant == "local":
+        return I.local_inputs(w["Hq"], w["Hkv"], w["N"], **kw)
+    return I.literal_inputs(w["Hq"], w["Hkv"], w["N"], **kw)
+
+
+def timed(fn, K, events_per_step=0):
+    """Run fn K times between two events on the current stream; returns (ms per step, per-step events)."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(events_per_step)] for _ in range(K)]
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(K):
+        fn(evs[i] if events_per_step else None)
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / K, evs
+
+
+# -------------------------------------------------------------- CPU oracle ----
+
+def oracle_sample(w, x, rows_per_sample, rng):
+    """Time the oracle on one vertical-slash head: full estimation + sampled attention rows.
+
+    Returns (extrapolated ms per layer, description).  The per-layer figure scales
+    the estimation to every vertical-slash head and the per-row attention cost to
+    every row of every head.
+    """
+    import oracle as O
+    vs, _, _ = head_patterns(w)
+    h = vs[0] if vs else 0
+    g = h // (w["Hq"] // w["Hkv"])
+    N = w["N"]
+    qh, kh, vh = x.q[h].cpu(), x.k[g].cpu(), x.v[g].cpu()
+    t0 = time.perf_counter()
+    vi, si, _, _ = O.vs_estimate(qh, kh, 64, w["k_v"], w["k_s"])
+    t1 = time.perf_counter()
+    rows = np.sort(rng.choice(N, size=min(rows_per_sample, N), replace=False))
+    O.attention_rows(qh, kh, vh, rows, lambda r: O.vs_mask_rows(N, r, vi, si), chunk=64)
+    t2 = time.perf_counter()
+    per_row = (t2 - t1) / len(rows)
+    ms = ((t1 - t0) * max(len(vs), 1) + per_row * w["Hq"] * N) * 1e3
+    desc = (f"oracle on q-head {h}: full estimation (extrapolated x{max(len(vs), 1)} heads) + "
+            f"{len(rows)} sampled attention rows (extrapolated to {w['Hq']} heads x {N} rows)")
+    return ms, desc
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    from dynamic_sparse_attention_vertical_gb300 import inputs as I
+    x = I.literal_inputs(w["Hq"], w["Hkv"], w["N"], n_cols=w["n_cols"], n_offsets=w["n_offsets"],
+                         seed=w["seed"], device="cuda" if torch.cuda.is_available() else "cpu")
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle_sample(w, x, 32, rng)
+    vals, desc = [], ""
+    for _ in range(args.steps):
+        v, desc = oracle_sample(w, x, 64, rng)
+        vals.append(v)
+    value = statistics.mean(vals)
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "ms/layer", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {describe(w)}", "input": "literal", "seq_len": w["N"]},
+        "cpu_baseline": {"value": value, "unit": "ms/layer", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "ms/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- main ----
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixed-128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--variants", default="literal,local", help="input variants; the first is the headline")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+    w = WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    from dynamic_sparse_attention_vertical_gb300 import binding as B
+    B.load()
+    burst, sustained, hbm, peak_src = measured_peaks()
+    dev = torch.device("cuda", local_rank)
+    variants = [v for v in args.variants.split(",") if v]
+    results = {}
+    dense_ms = None
+    e2e = None
+    cpu = None
+    clocks = None
+    for vi_, variant in enumerate(variants):
+        x = make_inputs(w, variant, dev)
+        L = Layer(B, w, x.q, x.k, x.v)
+        for _ in range(args.warmup):
+            L.step()
+        torch.cuda.synchronize()
+        L.check_status()
+        barrier()
+        headline = vi_ == 0
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        smi_id = vis.split(",")[local_rank] if vis else str(local_rank)
+        sampler = ClockSampler(smi_id) if headline else None
+        if sampler:
+            sampler.__enter__()
+        ms, evs = timed(L.step, args.steps, events_per_step=5)
+        if sampler:
+            sampler.__exit__(None, None, None)
+            clocks = sampler.summary()
+        barrier()
+        ms_max = max_over_ranks(ms)
+        stage = lambda a, b: statistics.mean(e[a].elapsed_time(e[b]) for e in evs)
+        st = {"estimate_ms": stage(0, 1), "vs_attention_ms": stage(1, 2), "block_sparse_ms": stage(2, 3),
+              "ashape_ms": stage(3, 4)}
+        alg, exe = L.work()
+        res = {"ms_per_layer": ms_max / world, "ms_per_step": ms_max, "stages": st,
+               "alg_tflop_per_layer": sum(alg.values()) / 1e12, "exec_tflop_per_layer": sum(exe.values()) / 1e12,
+               "vs_attention_alg_tflops": alg["vs"] / (st["vs_attention_ms"] * 1e-3) / 1e12 if alg["vs"] else None,
+               "vs_attention_exec_tflops": exe["vs"] / (st["vs_attention_ms"] * 1e-3) / 1e12 if exe["vs"] else None}
+        if headline:
+            if not args.no_dense:
+                for _ in range(1):
+                    L.dense()
+                dms, _ = timed(lambda e: L.dense(), 2)
+                dense_ms = max_over_ranks(dms)
+            if not args.no_e2e:
+                qh, kh, vh = (t.cpu().pin_memory() for t in (L.q, L.k, L.v))
+                oh = torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory()
+
+                def e2e_step(_):
+                    L.q.copy_(qh, non_blocking=True)
+                    L.k.copy_(kh, non_blocking=True)
+                    L.v.copy_(vh, non_blocking=True)
+                    L.step()
+                    oh.copy_(L.out, non_blocking=True)
+                e2e_step(None)
+                barrier()
+                ems, _ = timed(e2e_step, args.steps)
+                barrier()
+                ems = max_over_ranks(ems)
+                e2e = {"value": ems / world, "unit": "ms/layer",
+                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (qh, kh, vh)),
+                       "d2h_bytes_per_step": oh.numel() * oh.element_size()}
+                del qh, kh, vh, oh
+            if not args.no_cpu and rank == 0 and world == 1:
+                v_ms, desc = oracle_sample(w, x, 256, np.random.default_rng(1))
+                cpu = {"value": v_ms, "unit": "ms/layer", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                       "sample": desc}
+            kernels = L.kernels_per_step * args.steps
+        results[variant] = res
+        del L, x
+        torch.cuda.empty_cache()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    head = results[variants[0]]
+    Hq, N = w["Hq"], w["N"]
+    f_dense = 4 * 128 * Hq * N * (N + 1) / 2
+    ach = head["vs_attention_alg_tflops"]
+    line = {
+        "metric": METRIC, "value": head["ms_per_layer"], "unit": "ms/layer", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {describe(w)}", "input": variants[0], "seq_len": N,
+                   "heads": {"q": Hq, "kv": w["Hkv"]},
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "no flush: the inputs (Q 1 GiB, K and V 256 MiB each at 128K) exceed the 129 MB L2"},
+        "dense_equiv_tflops": f_dense / (head["ms_per_layer"] * 1e-3) / 1e12,
+        "dense_ms_per_layer": dense_ms,
+        "dense_equiv_speedup": (dense_ms / head["ms_per_layer"]) if dense_ms else None,
+        "dense_tflops": (f_dense / (dense_ms * 1e-3) / 1e12) if dense_ms else None,
+        "stages": head["stages"],
+        "roofline": {"bound": "tensor", "kernel": "vertical-slash sparse attention (tcgen05)",
+                     "achieved": ach, "peak": sustained, "unit": "TFLOP/s",
+                     "frac": (ach / sustained) if ach else None, "traffic": None,
+                     "flops": "algorithmic: 4*d per kept (q, j) pair; time = the mi_vs_sparse_attn call",
+                     "peak_source": f"bf16_tflops_sustained ({peak_src})",
+                     "executed_tflops": head["vs_attention_exec_tflops"],
+                     "executed_frac": (head["vs_attention_exec_tflops"] / sustained)
+                     if head["vs_attention_exec_tflops"] else None},
+        "pct_bf16_peak_exec": (head["vs_attention_exec_tflops"] / sustained * 100)
+        if head["vs_attention_exec_tflops"] else None,
+        "work": {"alg_tflop_per_layer": head["alg_tflop_per_layer"],
+                 "exec_tflop_per_layer": head["exec_tflop_per_layer"],
+                 "dense_tflop_per_layer": f_dense / 1e12},
+        "variants": {k2: {kk: vv for kk, vv in r.items() if kk != "ms_per_step"} for k2, r in results.items()},
+        "e2e": e2e,
+        "gpu_launches": kernels,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if dense_ms:
+        for r in line["variants"].values():
+            r["dense_equiv_speedup"] = dense_ms / r["ms_per_layer"]
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

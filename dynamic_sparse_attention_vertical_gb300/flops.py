@@ -1,0 +1,140 @@
+"""Work counts used to report throughput: kept keys per query row and executed tiles.
+
+Measurement helpers for the benchmark, not part of the compute path.
+
+* Algorithmic FLOPs of a head = 4 * d * (number of (q, j) pairs the pattern
+  keeps): one multiply-add for q.k and one for p.v per kept pair and dim.
+* Executed FLOPs = 4 * 128^3 per 128x128 tile the attention kernel issues,
+  masked elements included (the tensor cores run whole tiles).
+
+Vertical-slash row counts: with A(q) the first block [0, 64) and B(q) the
+query's own block [64*(q//64), q] (both always kept), a row keeps
+|A u B| + |V outside A u B| + |diagonals outside A u B| - |V and diagonals
+both hitting the same key outside A u B|; the last term is a correlation of
+the column and offset indicators, done with one FFT.
+"""
+from __future__ import annotations
+
+import torch
+
+D = 128
+TILE_FLOPS = 4 * 128 * 128 * 128
+
+
+def _indicator(idx, N, device):
+    x = torch.zeros(N, dtype=torch.float64, device=device)
+    idx = torch.as_tensor(idx, device=device).long()
+    idx = idx[(idx >= 0) & (idx < N)]
+    x[idx] = 1.0
+    return x
+
+
+def _prefix(x):
+    return torch.cat([torch.zeros(1, dtype=x.dtype, device=x.device), torch.cumsum(x, 0)])
+
+
+def vs_kept_per_row(N: int, v_idx, s_idx, blk: int = 64, device="cpu") -> torch.Tensor:
+    """Kept keys of every row of a vertical-slash head (int64 [N])."""
+    V = _indicator(v_idx, N, device)
+    S = _indicator(s_idx, N, device)
+    q = torch.arange(N, device=device)
+    lb = (q // blk) * blk
+    ab = torch.clamp(q + 1, max=blk) + torch.where(q >= blk, q - lb + 1, torch.zeros_like(q))
+    PV, PS = _prefix(V), _prefix(S)
+    c_out = torch.where(q >= blk, PV[lb] - PV[blk], torch.zeros_like(PV[lb]))
+    hi = torch.clamp(q - blk + 1, min=0)
+    lo = torch.clamp(q - lb + 1, min=0)
+    d_out = torch.where(q >= 2 * blk, PS[hi] - PS[torch.minimum(lo, hi)], torch.zeros_like(PV[lb]))
+    L = 1 << (2 * N - 1).bit_length()
+    full = torch.fft.irfft(torch.fft.rfft(V, L) * torch.fft.rfft(S, L), L)[:N]
+    first = torch.zeros(N, dtype=torch.float64, device=device)
+    for j in range(min(blk, N)):
+        if V[j] > 0:
+            first[j:] += S[: N - j]
+    local = torch.zeros(N, dtype=torch.float64, device=device)
+    for t in range(blk):
+        j = lb + t
+        ok = (j <= q) & (j >= blk)
+        jj = torch.where(ok, j, torch.zeros_like(j))
+        local += torch.where(ok, V[jj] * S[torch.where(ok, q - jj, torch.zeros_like(q))],
+                             torch.zeros_like(local))
+    mid = torch.round(full) - first - local
+    return (ab.double() + c_out + d_out - mid).round().long()
+
+
+def block_kept_per_row(N: int, sel_rows, blk: int = 64) -> torch.Tensor:
+    """Kept keys per row of a block-sparse head; sel_rows[r] = selected blocks of query block r."""
+    out = torch.zeros(N, dtype=torch.int64)
+    for r, sel in enumerate(sel_rows):
+        sel = [int(c) for c in sel if int(c) >= 0]
+        full = sum(1 for c in sel if c < r)
+        rows = torch.arange(r * blk, min(N, r * blk + blk))
+        out[rows] = full * blk + ((rows - r * blk + 1) if r in sel else 0)
+    return out
+
+
+def ashape_kept_per_row(N: int, n_init: int, window: int) -> torch.Tensor:
+    q = torch.arange(N)
+    sink = torch.clamp(q + 1, max=n_init)
+    w_lo = torch.clamp(q - window + 1, min=0)
+    win = q + 1 - w_lo
+    overlap = torch.clamp(sink - w_lo, min=0)
+    return sink + win - overlap
+
+
+def dense_kept_per_row(N: int) -> torch.Tensor:
+    return torch.arange(1, N + 1, dtype=torch.int64)
+
+
+# ------------------------------------------------------ executed tiles ----
+
+def vs_tiles(N: int, v_idx, s_idx) -> int:
+    """128x128 tiles the vertical-slash kernel issues for one head (all row blocks)."""
+    NT = (N + 127) // 128
+    d = torch.zeros(NT + 1, dtype=torch.bool)
+    s = torch.as_tensor(s_idx).long()
+    s = s[(s >= 0) & (s < N)]
+    d[(s >> 7)] = True
+    d[torch.clamp((s >> 7) + 1, max=NT)[(s & 127) > 0]] = True
+    d[0] = True
+    d = d[:NT]
+    dcum = torch.cumsum(d.long(), 0)                      # distances <= r
+    r = torch.arange(NT)
+    has_t0 = ~d[r]                                        # tile 0 added unless distance r is set
+    contig = dcum + has_t0.long()
+    v = torch.as_tensor(v_idx).long()
+    v = v[(v >= 0) & (v < N)]
+    cols = torch.bincount(v >> 7, minlength=NT).double()  # selected columns per key tile
+    notd = (~d).double()
+    notd[0] = 0.0
+    # residual columns of row block r: sum_t cols[t] * notd[r - t] over 1 <= t < r
+    L = 1 << (2 * NT).bit_length()
+    colsx = cols.clone()
+    colsx[0] = 0.0
+    resid = torch.fft.irfft(torch.fft.rfft(colsx, L) * torch.fft.rfft(notd, L), L)[:NT].round().long()
+    return int((contig + (resid + 127) // 128).sum())
+
+
+def dense_tiles(N: int) -> int:
+    NT = (N + 127) // 128
+    return NT * (NT + 1) // 2
+
+
+def ashape_tiles(N: int, n_init: int, window: int) -> int:
+    total = 0
+    for r in range((N + 127) // 128):
+        t_lo = max(0, r * 128 - window + 1) // 128
+        total += min((n_init + 127) // 128, t_lo) + (r - t_lo + 1)
+    return total
+
+
+def block_tiles(sel_rows) -> int:
+    """Tiles of the block-sparse kernel: per 128-row block, the union of both halves' 128-key tiles."""
+    total = 0
+    for r in range(0, len(sel_rows), 2):
+        tiles = set()
+        for rr in (r, r + 1):
+            if rr < len(sel_rows):
+                tiles |= {int(c) >> 1 for c in sel_rows[rr] if int(c) >= 0}
+        total += len(tiles)
+    return total

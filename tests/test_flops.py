@@ -1,0 +1,56 @@
+"""Work counts used by the benchmark, checked against explicit oracle masks (no GPU)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+from dynamic_sparse_attention_vertical_gb300 import flops as F
+
+
+@pytest.mark.parametrize("N,kv,ks,seed", [(700, 30, 40, 0), (1024, 200, 5, 1), (2048, 64, 300, 2), (64, 3, 3, 3)])
+def test_vs_kept_counts_match_oracle_mask(N, kv, ks, seed):
+    rng = np.random.default_rng(seed)
+    v = np.sort(rng.choice(N, size=min(kv, N), replace=False))
+    s = np.sort(rng.choice(N, size=min(ks, N), replace=False))
+    ref = O.vs_mask_rows(N, np.arange(N), v, s).sum(axis=1)
+    np.testing.assert_array_equal(F.vs_kept_per_row(N, v, s).numpy(), ref)
+
+
+def test_block_ashape_dense_counts_match_oracle_masks():
+    N = 640
+    rng = np.random.default_rng(4)
+    sel = [np.sort(rng.choice(r + 1, size=min(3, r + 1), replace=False)) for r in range(N // 64)]
+    np.testing.assert_array_equal(F.block_kept_per_row(N, sel).numpy(),
+                                  O.block_sparse_mask_rows(N, np.arange(N), sel).sum(1))
+    for n_init, w in [(128, 100), (0, 1), (64, 4096), (100, 300)]:
+        np.testing.assert_array_equal(F.ashape_kept_per_row(N, n_init, w).numpy(),
+                                      O.ashape_mask_rows(N, np.arange(N), n_init, w).sum(1))
+    np.testing.assert_array_equal(F.dense_kept_per_row(N).numpy(), O.causal_mask_rows(N, np.arange(N)).sum(1))
+
+
+def _vs_tiles_brute(N, v, s):
+    NT = (N + 127) // 128
+    D = {0} | {o >> 7 for o in s} | {(o >> 7) + 1 for o in s if o & 127}
+    total = 0
+    for r in range(NT):
+        contig = {0} | {r - d for d in D if d <= r}
+        resid = [j for j in v if 1 <= (j >> 7) < r and (j >> 7) not in contig]
+        total += len(contig) + math.ceil(len(resid) / 128)
+    return total
+
+
+@pytest.mark.parametrize("N,kv,ks,seed", [(4096, 300, 7, 0), (8192, 1000, 40, 1), (2112, 50, 0, 2)])
+def test_vs_tile_count_matches_enumeration(N, kv, ks, seed):
+    rng = np.random.default_rng(seed)
+    v = np.sort(rng.choice(N, size=kv, replace=False))
+    s = np.sort(rng.choice(N, size=ks, replace=False)) if ks else np.zeros(0, dtype=np.int64)
+    assert F.vs_tiles(N, v, s) == _vs_tiles_brute(N, v.tolist(), s.tolist())
+
+
+def test_dense_and_ashape_tiles():
+    assert F.dense_tiles(1024) == 8 * 9 // 2
+    assert F.ashape_tiles(1024, 128, 4096) == F.dense_tiles(1024)
+    # n_init=128, window=128, 16 row blocks: block 0 one tile, block 1 two,
+    # blocks 2..15 the sink tile plus two window tiles
+    assert F.ashape_tiles(2048, 128, 128) == 1 + 2 + 14 * 3

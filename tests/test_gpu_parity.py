@@ -254,6 +254,24 @@ def test_block_sparse_select_and_attention():
         assert_close(out2.float().cpu().numpy()[h], ref, f"block given h{h}")
 
 
+def test_block_select_many_candidates():
+    """Up to 256 candidate blocks per query block and top-100, against the oracle's ranking."""
+    N, Hq, Hkv, topk = 16384, 1, 1, 100
+    x = I.literal_inputs(Hq, Hkv, N, n_cols=4, n_offsets=2, seed=41)
+    q, k, v = _dev(x)
+    _, blk = B.mi_block_sparse_attn(q, k, v, topk=topk)
+    bl = blk.cpu().numpy()[0]
+    sig = O.block_scores(x.q[0], x.k[0])
+    ref_sel = O.block_sparse_select(x.q[0], x.k[0], topk)
+    diffs = 0
+    for r in range(N // 64):
+        got = bl[r][bl[r] >= 0]
+        assert len(got) == min(topk, r + 1) and np.all(np.diff(got) > 0) and got.max() <= r
+        assert np.all(bl[r][len(got):] == -1)
+        diffs += band_agree(got, ref_sel[r], sig[r, : r + 1], min(topk, r + 1), rel_band=1e-3)
+    assert diffs <= N // 64  # near-ties only
+
+
 # ----------------------------------------------------------------- errors ----
 
 def test_argument_and_index_errors():

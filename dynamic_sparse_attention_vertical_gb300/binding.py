@@ -38,6 +38,7 @@ MI_IDX_GIVEN = 1
 SYMBOLS = (
     "mi_workspace_bytes",
     "mi_vs_estimate",
+    "mi_vs_estimate_noalloc",
     "mi_vs_sparse_attn",
     "mi_block_sparse_attn",
     "mi_ashape_attn",
@@ -71,6 +72,8 @@ def load() -> ctypes.CDLL:
     lib.mi_workspace_bytes.restype = S
     lib.mi_vs_estimate.argtypes = [P, P, I, I, I, I, P, I, I, I, I, P, P, P, S, P]
     lib.mi_vs_estimate.restype = I
+    lib.mi_vs_estimate_noalloc.argtypes = [P, P, I, I, I, I, P, I, I, I, I, P, P, P]
+    lib.mi_vs_estimate_noalloc.restype = I
     lib.mi_vs_sparse_attn.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, I, P, P, P, S, P]
     lib.mi_vs_sparse_attn.restype = I
     lib.mi_block_sparse_attn.argtypes = [P, P, P, I, I, I, I, P, I, I, I, P, I, P, P, P, S, P]
@@ -166,6 +169,28 @@ def mi_vs_estimate(q, k, heads=None, last_q: int = 64, k_v: int = 1000, k_s: int
     rc = load().mi_vs_estimate(_ptr(q), _ptr(k), Hq, Hkv, N, d, harr, n, last_q, k_v, k_s,
                                _ptr(v_idx), _ptr(s_idx), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "mi_vs_estimate")
+    return v_idx, s_idx
+
+
+def mi_vs_estimate_noalloc(q, k, heads=None, last_q: int = 64, k_v: int = 1000, k_s: int = 6096,
+                           v_idx=None, s_idx=None, stream=None):
+    """mi_vs_estimate with the library's own fixed scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory at call time; the index outputs
+    are allocated here only when not passed in.
+    """
+    _check_qkv(q, k)
+    _check_idx(v_idx, s_idx)
+    Hq, N, d = q.shape
+    Hkv = k.shape[0]
+    harr, n = _heads(heads, Hq)
+    if v_idx is None:
+        v_idx = torch.empty((n, k_v), dtype=torch.int32, device=q.device)
+    if s_idx is None:
+        s_idx = torch.empty((n, k_s), dtype=torch.int32, device=q.device)
+    rc = load().mi_vs_estimate_noalloc(_ptr(q), _ptr(k), Hq, Hkv, N, d, harr, n, last_q, k_v, k_s,
+                                       _ptr(v_idx), _ptr(s_idx), _stream(stream))
+    _raise(rc, "mi_vs_estimate_noalloc")
     return v_idx, s_idx
 
 

@@ -169,6 +169,35 @@ int mi_dense_causal_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
                          float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream);
 
 /*
+ * mi_vs_estimate_noalloc: mi_vs_estimate for callers that cannot allocate device
+ * memory (for instance an engine whose memory pool owns the whole device, or a
+ * plugin running where cudaMalloc is not allowed).  The pages have no
+ * counterpart; this is a packaging variant of the call above.
+ *
+ * Same arguments, results and errors as mi_vs_estimate, minus the workspace: the
+ * scratch is a fixed array of MI_NOALLOC_SCRATCH_BYTES in device memory owned by
+ * libmi.so, present on every GPU that loads the library until the process
+ * exits.  The call allocates nothing.
+ *  - Size limit: the job must fit the array, i.e.
+ *    mi_workspace_bytes(MI_OP_VS_ESTIMATE, n_heads, Hkv, N, 0, 0, 0)
+ *    <= MI_NOALLOC_SCRATCH_BYTES (about 8 * n_heads * N bytes: 32 heads at 128K
+ *    tokens fit); a larger job returns MI_ERR_WORKSPACE before any work is queued.
+ *  - Set-up: the first call on a device, with that device current, looks up the
+ *    array's device address (once per device).  Make that first call before any
+ *    stream capture begins.
+ *  - Sharing: every call uses the same array and leaves its contents behind; the
+ *    call clears what has to start at zero.  Calls that overlap on the GPU (on
+ *    different streams or from different threads) race on the array and must be
+ *    serialised by the caller.
+ *  - The device status word lives in the shared array and cannot be read back
+ *    with mi_read_status; use mi_vs_estimate with a workspace when it matters.
+ */
+#define MI_NOALLOC_SCRATCH_BYTES (32u << 20)
+int mi_vs_estimate_noalloc(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
+                           const int32_t* heads, int n_heads, int last_q, int k_v, int k_s,
+                           int32_t* v_idx, int32_t* s_idx, mi_stream_t stream);
+
+/*
  * Synchronizes `stream`, then returns the status word of the last call that
  * used `workspace` (MI_OK, MI_ERR_INDEX or MI_ERR_TIMEOUT), or MI_ERR_CUDA if
  * the synchronization or the read failed.

@@ -191,7 +191,9 @@ class Layer:
         self.B.mi_dense_causal_attn(self.q, self.k, self.v, out=self.out, workspace=self.ws_dense)
 
     def check_status(self):
-        for ws in (self.ws_est, self.ws_vs, self.ws_blk, self.ws_ash):
+        used = ([self.ws_est, self.ws_vs] if self.vs else []) + ([self.ws_blk] if self.blk else []) \
+            + ([self.ws_ash] if self.ash else [])
+        for ws in used:
             st = self.B.mi_read_status(ws)
             if st not in (0,):
                 raise RuntimeError(f"device status {st}: {self.B.mi_strerror(st)}")

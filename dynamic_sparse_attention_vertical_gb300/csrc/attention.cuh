@@ -11,19 +11,22 @@
 //     gittoolsai.com, "TL;DR" and the PIT note; talk slides, boteman.cn,
 //     "Dynamic Sparse Attention Calculation with PIT, FlashAttention").
 //
-// Warp roles (256 threads):
-//   warp 0      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warp 1      Q (once) and K tiles (TMA, or cp.async gather)
-//   warp 2      V tiles (TMA, or cp.async gather)
-//   warp 3      idle after the prologue
-//   warps 4-7   softmax: thread t owns query row t (TMEM lane t)
+// Warp roles (256 threads, two CTAs per SM):
+//   warps 0-3   softmax: thread t owns query row t (TMEM lane t)
+//   warp 4      TMEM allocation and the single-thread tcgen05.mma issuer
+//   warp 5      Q (once) and K tiles (TMA, or cp.async gather)
+//   warp 6      V tiles (TMA, or cp.async gather)
+//   warp 7      idle after the prologue
 //
-// Per tile i: S_i = Q K_i^T (M=128, N=128, K=128) into one of two TMEM
-// buffers; softmax warps load S_i, mask, update a running maximum, write
-// P_i = exp2(x - m) as bf16 into shared memory (128-byte swizzled, K-major);
-// then O += P_i V_i accumulates in TMEM.  The running maximum is only moved
-// (and O rescaled in TMEM) when a tile's maximum exceeds it by more than 8
-// (log2 units), so P stays below 2^8 and most tiles need no O correction.
+// Tensor memory (256 columns): S = Q K^T (fp32, columns 0-127) and O (fp32,
+// columns 128-255).  Per tile: the MMA warp issues S = Q K_i^T; the softmax
+// warps read S in two passes (row maximum, then exp2 and pack), and write
+// P_i = exp2(x - m) as bf16 pairs over the S columns they have consumed; the
+// MMA warp then issues O += P_i V_i with P read from tensor memory.  The
+// running maximum moves (and O is rescaled in tensor memory) only when a
+// tile's maximum exceeds it by more than 8 (log2 units), so P stays below 2^8.
+// Shared memory holds one Q tile and one K and one V stage (about 105 KB), so
+// two CTAs share an SM and one CTA's softmax overlaps the other's MMAs.
 // Every mbarrier wait is bounded; on a timeout the CTA stops issuing work,
 // waits for what it already issued, frees TMEM and records MI_ERR_TIMEOUT.
 #pragma once
@@ -65,13 +68,11 @@ struct AttnArgs {
 
 struct AttnSmem {
   alignas(1024) uint8_t q[2][16384];
-  alignas(1024) uint8_t k[2][2][16384];
-  alignas(1024) uint8_t v[2][2][16384];
-  alignas(1024) uint8_t p[2][16384];
+  alignas(1024) uint8_t k[2][16384];
+  alignas(1024) uint8_t v[2][16384];
   int list[MI_MAX_KV];  // VS: residual columns; block: (tile << 4) | sub-block mask
   int scan[256];
-  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_empty[2], p_full, pv_done, mma_done;
+  uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, mma_done;
   uint32_t tmem;
   int abort;
   int n_list;    // entries in list
@@ -82,7 +83,8 @@ struct AttnSmem {
 };
 
 constexpr size_t kAttnSmemBytes = sizeof(AttnSmem) + 1024;
-constexpr uint32_t kTmemCols = 512;  // S0 @0, S1 @128, O @256
+constexpr uint32_t kTmemCols = 256;  // S (and P over it) at 0, O at 128
+constexpr uint32_t kTmemO = 128;
 
 // ------------------------------------------------------------ tile list ----
 
@@ -318,8 +320,25 @@ __device__ __forceinline__ void gather_tile(uint8_t (*dst)[16384], const __nv_bf
 
 // ---------------------------------------------------------------- kernel ----
 
+// One pass over the 128 S values of this thread's row, 32 columns at a time.
+// Masked elements read as -inf.
+template <class F>
+__device__ __forceinline__ void for_s_chunks(uint32_t taddr, const uint32_t mk[4], bool full, F f) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float x[32];
+    tmem_ld32(taddr + c * 32, x);
+    if (!full) {
+      const uint32_t w = c == 0 ? mk[0] : c == 1 ? mk[1] : c == 2 ? mk[2] : mk[3];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] = ((w >> e) & 1u) ? x[e] : -INFINITY;
+    }
+    f(c, x);
+  }
+}
+
 template <int PAT>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
 attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -334,25 +353,22 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 
   if (tid == 0) {
     mbar_init(&s.q_full, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s.k_full[b], 1);
-      mbar_init(&s.k_empty[b], 1);
-      mbar_init(&s.v_full[b], 1);
-      mbar_init(&s.v_empty[b], 1);
-      mbar_init(&s.s_full[b], 1);
-      mbar_init(&s.s_empty[b], 128);
-    }
+    mbar_init(&s.k_full, 1);
+    mbar_init(&s.k_empty, 1);
+    mbar_init(&s.v_full, 1);
+    mbar_init(&s.v_empty, 1);
+    mbar_init(&s.s_full, 1);
     mbar_init(&s.p_full, 128);
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.mma_done, 1);
     s.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == 4) {
     tmem_alloc(&s.tmem, kTmemCols);
     tmem_relinquish();
   }
-  if (tid == 32) {
+  if (tid == 160) {
     tma_prefetch_map(&map_q);
     tma_prefetch_map(&map_k);
     tma_prefetch_map(&map_v);
@@ -365,55 +381,48 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   volatile int* abort = &s.abort;
   const uint64_t lim = a.wait_limit_ns;
 
-  if (warp == 0) {
+  if (warp == 4) {
     // ------------------------------------------------------------ MMA ----
     if (lane_id() == 0) {
       const uint32_t id_qk = idesc_bf16(kBM, kBN, 0);
       const uint32_t id_pv = idesc_bf16(kBM, kD, 1);
       bool ok = mbar_wait(&s.q_full, 0, abort, lim);
-      auto issue_pv = [&](int u) {
-        if (!ok) return;
-        ok = mbar_wait(&s.p_full, u & 1, abort, lim) &&
-             mbar_wait(&s.v_full[u & 1], (u >> 1) & 1, abort, lim);
-        if (!ok) return;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(smem_u32(s.p[kk >> 2]) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(smem_u32(s.v[u & 1][0]) + kk * 2048, 16384, 1024);
-          umma_bf16_ss(tmem + 256, ad, bd, id_pv, (u > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&s.pv_done);
-        umma_commit(&s.v_empty[u & 1]);
-      };
       for (int t = 0; t < T && ok; ++t) {
-        const int b = t & 1;
-        ok = mbar_wait(&s.k_full[b], (t >> 1) & 1, abort, lim);
-        if (ok && t >= 2) ok = mbar_wait(&s.s_empty[b], ((t - 2) >> 1) & 1, abort, lim);
+        ok = mbar_wait(&s.k_full, t & 1, abort, lim);
+        // S is overwritten: P of the previous tile must have been consumed
+        if (ok && t >= 1) ok = mbar_wait(&s.pv_done, (t - 1) & 1, abort, lim);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = sdesc_sw128(smem_u32(s.q[kk >> 2]) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(smem_u32(s.k[b][kk >> 2]) + (kk & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + b * 128, ad, bd, id_qk, kk > 0 ? 1u : 0u);
+          const uint64_t bd = sdesc_sw128(smem_u32(s.k[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          umma_bf16_ss(tmem, ad, bd, id_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s.s_full[b]);
-        umma_commit(&s.k_empty[b]);
-        if (t >= 1) issue_pv(t - 1);
+        umma_commit(&s.s_full);
+        umma_commit(&s.k_empty);
+        ok = mbar_wait(&s.p_full, t & 1, abort, lim) && mbar_wait(&s.v_full, t & 1, abort, lim);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = sdesc_sw128(smem_u32(s.v[0]) + kk * 2048, 16384, 1024);
+          umma_bf16_ts(tmem + kTmemO, tmem + kk * 8, bd, id_pv, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&s.pv_done);
+        umma_commit(&s.v_empty);
       }
-      if (ok && T > 0) issue_pv(T - 1);
       umma_commit(&s.mma_done);  // completes when everything issued above is done
       mbar_wait_drain(&s.mma_done, 0, lim);
     }
     __syncwarp();
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp == 5 || warp == 6) {
     // --------------------------------------------------------- loaders ----
-    const bool is_k = (warp == 1);
+    const bool is_k = (warp == 5);
     const CUtensorMap* map = is_k ? &map_k : &map_v;
-    uint64_t* full = is_k ? s.k_full : s.v_full;
-    uint64_t* empty = is_k ? s.k_empty : s.v_empty;
-    uint8_t(*buf)[2][16384] = is_k ? s.k : s.v;
+    uint64_t* full = is_k ? &s.k_full : &s.v_full;
+    uint64_t* empty = is_k ? &s.k_empty : &s.v_empty;
+    uint8_t(*buf)[16384] = is_k ? s.k : s.v;
     const __nv_bfloat16* src_head = (is_k ? a.kp : a.vp) + (size_t)g * a.N * kD;
     if (is_k && lane_id() == 0) {
       mbar_arrive_expect_tx(&s.q_full, 2 * 16384);
@@ -422,65 +431,54 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     }
     int issued = 0;
     for (int t = 0; t < T; ++t) {
-      const int b = t & 1;
-      if (t >= 2 && !mbar_wait_warp(&empty[b], ((t - 2) >> 1) & 1, abort, lim)) break;
+      if (t >= 1 && !mbar_wait_warp(empty, (t - 1) & 1, abort, lim)) break;
       const TileRef ref = tile_at<PAT>(s, a, n, r, t);
       if (ref.kind == 0) {
         if (lane_id() == 0) {
-          mbar_arrive_expect_tx(&full[b], 2 * 16384);
-          tma_load_3d(buf[b][0], map, &full[b], 0, ref.t * kBN, g);
-          tma_load_3d(buf[b][1], map, &full[b], 64, ref.t * kBN, g);
+          mbar_arrive_expect_tx(full, 2 * 16384);
+          tma_load_3d(buf[0], map, full, 0, ref.t * kBN, g);
+          tma_load_3d(buf[1], map, full, 64, ref.t * kBN, g);
         }
       } else {
         const int valid = min(kBN, s.n_list - ref.t * kBN);
-        gather_tile(buf[b], src_head, s.list + ref.t * kBN, valid);
-        if (lane_id() == 0) mbar_arrive(&full[b]);
+        gather_tile(buf, src_head, s.list + ref.t * kBN, valid);
+        if (lane_id() == 0) mbar_arrive(full);
       }
       issued = t + 1;
       __syncwarp();
     }
-    // drain: the last (up to two) loads must land before the CTA can exit
+    // drain: the last load must land before the CTA can exit
     if (lane_id() == 0) {
       if (is_k) mbar_wait_drain(&s.q_full, 0, lim);
-      for (int t = max(0, issued - 2); t < issued; ++t)
-        mbar_wait_drain(&full[t & 1], (t >> 1) & 1, lim);
+      if (issued > 0) mbar_wait_drain(full, (issued - 1) & 1, lim);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
     // --------------------------------------------------------- softmax ----
-    const int row = tid - 128;  // TMEM lane and row within the block
+    const int row = tid;  // TMEM lane and row within the block
     const int q = r * kBM + row;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base, o_addr = tmem + lane_base + kTmemO;
+    const float sl = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    // the mask of the next tile is loaded while the current one is processed
+    uint32_t mk[4], mk_next[4];
+    if (T > 0) row_mask<PAT>(s, a, n, r, tile_at<PAT>(s, a, n, r, 0), q, mk_next);
     for (int t = 0; t < T; ++t) {
-      const int b = t & 1;
-      ok = mbar_wait_warp(&s.s_full[b], (t >> 1) & 1, abort, lim);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) mk[w] = mk_next[w];
+      ok = mbar_wait_warp(&s.s_full, t & 1, abort, lim);
       if (!ok) break;
       tc_fence_after();
-      float x[128];
+      const bool full = (mk[0] & mk[1] & mk[2] & mk[3]) == 0xFFFFFFFFu;
+      // pass 1: row maximum of the kept raw scores
+      float mraw = -INFINITY;
+      for_s_chunks(s_addr, mk, full, [&](int, const float* x) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + b * 128 + c * 32, x + c * 32);
-      tc_fence_before();
-      mbar_arrive(&s.s_empty[b]);
-
-      const TileRef ref = tile_at<PAT>(s, a, n, r, t);
-      uint32_t mk[4];
-      row_mask<PAT>(s, a, n, r, ref, q, mk);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const bool keep = (mk[c >> 5] >> (c & 31)) & 1u;
-        x[c] = keep ? x[c] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[c]);
-      }
-      // the P buffer and O are free once the previous tile's P.V is done
-      if (t >= 1) {
-        ok = mbar_wait_warp(&s.pv_done, (t - 1) & 1, abort, lim);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      // move the reference maximum only when the tile's maximum exceeds it by > 8
+        for (int e = 0; e < 32; ++e) mraw = fmaxf(mraw, x[e]);
+      });
+      const float mx = mraw * sl;  // sl > 0: the maximum commutes with the scale
       const bool upd = mx > m_ref + 8.0f;
       const bool rescale_o = upd && (m_ref != -INFINITY);
       float alpha = 1.f;
@@ -489,36 +487,36 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         l *= alpha;
         m_ref = mx;
       }
+      // O holds P.V of tiles < t (that P.V completed before S of tile t was written)
       if (__any_sync(0xffffffffu, rescale_o)) {  // tcgen05.ld/st are warp-collective
-        float o[32];
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+          float o[32];
+          tmem_ld32(o_addr + c * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tmem + lane_base + 256 + c * 32, o);
+          tmem_st32(o_addr + c * 32, o);
         }
       }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // pass 2: P = exp2(x * sl - m) as bf16 pairs over the consumed S columns
       float rs = 0.f;
+      for_s_chunks(s_addr, mk, full, [&](int c, const float* x) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(x[u * 8 + 2 * e] - mb);
-          const float p1 = fast_exp2(x[u * 8 + 2 * e + 1] - mb);
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = fast_exp2(fmaf(x[2 * e], sl, -mb));
+          const float p1 = fast_exp2(fmaf(x[2 * e + 1], sl, -mb));
           rs += p0 + p1;
           __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
           pk[e] = *reinterpret_cast<uint32_t*>(&bb);
         }
-        *reinterpret_cast<uint4*>(s.p[u >> 3] + sw128_offset(row, u & 7)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
+        tmem_st16(s_addr + c * 16, pk);
+      });
       l += rs;
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&s.p_full);
+      if (t + 1 < T) row_mask<PAT>(s, a, n, r, tile_at<PAT>(s, a, n, r, t + 1), q, mk_next);
     }
     // epilogue: O / l
     if (ok && T > 0) ok = mbar_wait_warp(&s.pv_done, (T - 1) & 1, abort, lim);
@@ -530,7 +528,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float o[32];
-        tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+        tmem_ld32(o_addr + c * 32, o);
         if (in_range) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -554,7 +552,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   tc_fence_before();
   __syncthreads();
   if (s.abort && tid == 0) set_status(a.status, MI_ERR_TIMEOUT);
-  if (warp == 0) {
+  if (warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -70,7 +70,7 @@ typedef struct CUstream_st* mi_stream_t; /* a cudaStream_t */
 #define MI_HEAD_DIM 128
 #define MI_LAST_Q 64
 #define MI_BLOCK 64
-#define MI_MAX_KV 4096 /* largest vertical budget the sparse attention kernel accepts */
+#define MI_MAX_KV 2048 /* largest vertical budget the sparse attention kernel accepts */
 
 /* ops for mi_workspace_bytes */
 #define MI_OP_VS_ESTIMATE 1

@@ -143,49 +143,79 @@ __device__ __forceinline__ uint32_t load_bits32(const uint32_t* bits, int pos, i
   return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
 }
 
-// Keep-mask of query row q over the 128 keys of tile `ref` (bit c of m[c/32]).
+// Raw words a row's keep-mask depends on, loaded a tile ahead of their use.
+struct MaskRaw {
+  TileRef ref;
+  int base;          // VS: first offset bit of the window (q - j0 - 127)
+  uint32_t off[5];   // VS: offset-bitmap words covering [base, base + 128)
+  uint32_t col[4];   // VS: column-bitmap words of the tile's keys
+};
+
 template <int PAT>
-__device__ __forceinline__ void row_mask(const AttnSmem& s, const AttnArgs& a, int n, int r,
-                                         const TileRef& ref, int q, uint32_t m[4]) {
+__device__ __forceinline__ MaskRaw mask_fetch(const AttnArgs& a, int n, const TileRef& ref, int q) {
+  MaskRaw m;
+  m.ref = ref;
+  m.base = 0;
+  if (PAT == kPatVS && ref.kind == 0) {
+    const uint32_t* off = a.offbits + (size_t)n * a.Nw;
+    const uint32_t* col = a.colbits + (size_t)n * a.Nw;
+    const int j0 = ref.t * kBN;
+    m.base = q - j0 - 127;
+    const int w0 = m.base >> 5;  // floor; >= -4
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      const int wi = w0 + i;  // < Nw: q - j0 < NT * 128
+      m.off[i] = (wi >= 0) ? __ldg(off + wi) : 0u;
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) m.col[w] = __ldg(col + (j0 >> 5) + w);
+  }
+  return m;
+}
+
+// Keep-mask of query row q over the 128 keys of tile m.ref (bit c of out[c/32]).
+template <int PAT>
+__device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a, int r,
+                                            const MaskRaw& m, int q, uint32_t out[4]) {
+  const TileRef& ref = m.ref;
   if (PAT == kPatVS && ref.kind == 1) {
     const int valid = min(kBN, s.n_list - ref.t * kBN);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) m[w] = range_bits(32 * w, 0, valid);
+    for (int w = 0; w < 4; ++w) out[w] = range_bits(32 * w, 0, valid);
     return;
   }
   const int j0 = ref.t * kBN;
   if (PAT == kPatDense) {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) m[w] = 0xFFFFFFFFu;
+    for (int w = 0; w < 4; ++w) out[w] = 0xFFFFFFFFu;
   } else if (PAT == kPatVS) {
-    const uint32_t* off = a.offbits + (size_t)n * a.Nw;
-    const uint32_t* col = a.colbits + (size_t)n * a.Nw;
-    // offsets q - j0 - c for c = 0..127 are the 128 bits starting at q - j0 - 127, reversed
-    const int base = q - j0 - 127;
+    // offsets q - j0 - c for c = 0..127 are the 128 bits starting at base, reversed
+    const int sh = m.base & 31;
     const int lb = (q >> 6) << 6;  // start of the query's own 64-block
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const uint32_t sl = __brev(load_bits32(off, base + 32 * (3 - w), a.N));
-      const uint32_t cl = __ldg(col + (j0 >> 5) + w);
-      m[w] = sl | cl | range_bits(j0 + 32 * w, 0, kBlk) | range_bits(j0 + 32 * w, lb, lb + kBlk);
+      const int k = 3 - w;
+      const uint32_t win = sh ? ((m.off[k] >> sh) | (m.off[k + 1] << (32 - sh))) : m.off[k];
+      out[w] = __brev(win) | m.col[w] | range_bits(j0 + 32 * w, 0, kBlk) |
+               range_bits(j0 + 32 * w, lb, lb + kBlk);
     }
   } else if (PAT == kPatBlock) {
     const int half = (q >> 6) & 1;
     const uint32_t lo = ((ref.sub >> (half * 2)) & 1) ? 0xFFFFFFFFu : 0u;
     const uint32_t hi = ((ref.sub >> (half * 2 + 1)) & 1) ? 0xFFFFFFFFu : 0u;
-    m[0] = lo;
-    m[1] = lo;
-    m[2] = hi;
-    m[3] = hi;
+    out[0] = lo;
+    out[1] = lo;
+    out[2] = hi;
+    out[3] = hi;
   } else {  // A-shape
 #pragma unroll
     for (int w = 0; w < 4; ++w)
-      m[w] = range_bits(j0 + 32 * w, 0, a.n_init) |
-             range_bits(j0 + 32 * w, q - a.window + 1, q + 1);
+      out[w] = range_bits(j0 + 32 * w, 0, a.n_init) |
+               range_bits(j0 + 32 * w, q - a.window + 1, q + 1);
   }
   if (ref.t == r) {  // the diagonal tile: causal
 #pragma unroll
-    for (int w = 0; w < 4; ++w) m[w] &= range_bits(j0 + 32 * w, 0, q + 1);
+    for (int w = 0; w < 4; ++w) out[w] &= range_bits(j0 + 32 * w, 0, q + 1);
   }
 }
 
@@ -320,20 +350,24 @@ __device__ __forceinline__ void gather_tile(uint8_t (*dst)[16384], const __nv_bf
 
 // ---------------------------------------------------------------- kernel ----
 
-// One pass over the 128 S values of this thread's row, 32 columns at a time.
-// Masked elements read as -inf.
+// One pass over the 128 S values of this thread's row, 64 columns per TMEM
+// wait.  Masked elements read as -inf.
 template <class F>
-__device__ __forceinline__ void for_s_chunks(uint32_t taddr, const uint32_t mk[4], bool full, F f) {
+__device__ __forceinline__ void for_s_halves(uint32_t taddr, const uint32_t mk[4], bool full, F f) {
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    float x[32];
-    tmem_ld32(taddr + c * 32, x);
+  for (int hh = 0; hh < 2; ++hh) {
+    float x[64];
+    tmem_ld64(taddr + hh * 64, x);
     if (!full) {
-      const uint32_t w = c == 0 ? mk[0] : c == 1 ? mk[1] : c == 2 ? mk[2] : mk[3];
+      const uint32_t w0 = hh ? mk[2] : mk[0];
+      const uint32_t w1 = hh ? mk[3] : mk[1];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] = ((w >> e) & 1u) ? x[e] : -INFINITY;
+      for (int e = 0; e < 32; ++e) {
+        x[e] = ((w0 >> e) & 1u) ? x[e] : -INFINITY;
+        x[32 + e] = ((w1 >> e) & 1u) ? x[32 + e] : -INFINITY;
+      }
     }
-    f(c, x);
+    f(hh, x);
   }
 }
 
@@ -462,21 +496,25 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const float sl = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // the mask of the next tile is loaded while the current one is processed
-    uint32_t mk[4], mk_next[4];
-    if (T > 0) row_mask<PAT>(s, a, n, r, tile_at<PAT>(s, a, n, r, 0), q, mk_next);
+    // mask words are fetched one tile ahead and tile references two tiles ahead,
+    // so their global loads overlap the wait for S
+    TileRef ref_next2 = (T > 1) ? tile_at<PAT>(s, a, n, r, 1) : TileRef{0, 0, 0};
+    MaskRaw raw_next = mask_fetch<PAT>(a, n, (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0}, q);
     for (int t = 0; t < T; ++t) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) mk[w] = mk_next[w];
+      const MaskRaw raw = raw_next;
+      if (t + 1 < T) raw_next = mask_fetch<PAT>(a, n, ref_next2, q);
+      if (t + 2 < T) ref_next2 = tile_at<PAT>(s, a, n, r, t + 2);
       ok = mbar_wait_warp(&s.s_full, t & 1, abort, lim);
       if (!ok) break;
       tc_fence_after();
+      uint32_t mk[4];
+      mask_finish<PAT>(s, a, r, raw, q, mk);
       const bool full = (mk[0] & mk[1] & mk[2] & mk[3]) == 0xFFFFFFFFu;
       // pass 1: row maximum of the kept raw scores
       float mraw = -INFINITY;
-      for_s_chunks(s_addr, mk, full, [&](int, const float* x) {
+      for_s_halves(s_addr, mk, full, [&](int, const float* x) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mraw = fmaxf(mraw, x[e]);
+        for (int e = 0; e < 64; ++e) mraw = fmaxf(mraw, x[e]);
       });
       const float mx = mraw * sl;  // sl > 0: the maximum commutes with the scale
       const bool upd = mx > m_ref + 8.0f;
@@ -501,22 +539,21 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
       // pass 2: P = exp2(x * sl - m) as bf16 pairs over the consumed S columns
       float rs = 0.f;
-      for_s_chunks(s_addr, mk, full, [&](int c, const float* x) {
-        uint32_t pk[16];
+      for_s_halves(s_addr, mk, full, [&](int hh, const float* x) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 32; ++e) {
           const float p0 = fast_exp2(fmaf(x[2 * e], sl, -mb));
           const float p1 = fast_exp2(fmaf(x[2 * e + 1], sl, -mb));
           rs += p0 + p1;
           __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
           pk[e] = *reinterpret_cast<uint32_t*>(&bb);
         }
-        tmem_st16(s_addr + c * 16, pk);
+        tmem_st32u(s_addr + hh * 32, pk);
       });
       l += rs;
       tc_fence_before();
       mbar_arrive(&s.p_full);
-      if (t + 1 < T) row_mask<PAT>(s, a, n, r, tile_at<PAT>(s, a, n, r, t + 1), q, mk_next);
     }
     // epilogue: O / l
     if (ok && T > 0) ok = mbar_wait_warp(&s.pv_done, (T - 1) & 1, abort, lim);

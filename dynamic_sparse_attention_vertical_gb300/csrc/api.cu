@@ -139,7 +139,7 @@ EstLayout est_layout(int n_heads, int N) {
 }
 
 struct VsLayout {
-  size_t status, offbits, colbits, dbits, dlist, dcount, total;
+  size_t status, offbits, colbits, dbits, dfull, dlist, dcount, total;
   int Nw, NT, NTw;
 };
 VsLayout vs_layout(int n_heads, int N) {
@@ -152,6 +152,7 @@ VsLayout vs_layout(int n_heads, int N) {
   L.offbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.Nw);
   L.colbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.Nw);
   L.dbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.NTw);
+  L.dfull = c.take(sizeof(uint32_t) * (size_t)n_heads * L.NTw);
   L.dlist = c.take(sizeof(int) * (size_t)n_heads * L.NT);
   L.dcount = c.take(sizeof(int) * (size_t)n_heads);
   L.total = c.off;
@@ -353,6 +354,7 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
   ia.offbits = reinterpret_cast<uint32_t*>(ws + L.offbits);
   ia.colbits = reinterpret_cast<uint32_t*>(ws + L.colbits);
   ia.dbits = reinterpret_cast<uint32_t*>(ws + L.dbits);
+  ia.dfull = reinterpret_cast<uint32_t*>(ws + L.dfull);
   ia.dlist = reinterpret_cast<int*>(ws + L.dlist);
   ia.dcount = reinterpret_cast<int*>(ws + L.dcount);
   ia.status = status;
@@ -362,6 +364,7 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
   a.offbits = ia.offbits;
   a.colbits = ia.colbits;
   a.dbits = ia.dbits;
+  a.dfull = ia.dfull;
   a.dlist = ia.dlist;
   a.dcount = ia.dcount;
   a.v_idx = v_idx;

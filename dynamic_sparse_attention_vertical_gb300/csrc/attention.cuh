@@ -53,6 +53,7 @@ struct AttnArgs {
   const uint32_t* offbits;  // [n_heads, Nw]   bit o: offset o selected
   const uint32_t* colbits;  // [n_heads, Nw]   bit j: column j selected
   const uint32_t* dbits;    // [n_heads, NTw]  bit t: tile distance t touched by a diagonal
+  const uint32_t* dfull;    // [n_heads, NTw]  bit t: a tile at distance t is kept whole
   const int* dlist;         // [n_heads, NT]   the set bits of dbits, ascending
   const int* dcount;        // [n_heads]
   const int* v_idx;         // [n_heads, k_v]
@@ -72,6 +73,7 @@ struct AttnSmem {
   alignas(1024) uint8_t v[2][16384];
   int list[MI_MAX_KV];  // VS: residual columns; block: (tile << 4) | sub-block mask
   int scan[256];
+  uint32_t dfull[512];  // VS: the head's whole-tile distance bits (N <= 2^21)
   uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, mma_done;
   uint32_t tmem;
   int abort;
@@ -146,17 +148,24 @@ __device__ __forceinline__ uint32_t load_bits32(const uint32_t* bits, int pos, i
 // Raw words a row's keep-mask depends on, loaded a tile ahead of their use.
 struct MaskRaw {
   TileRef ref;
+  bool whole;        // VS: the tile is kept whole (no mask words needed)
   int base;          // VS: first offset bit of the window (q - j0 - 127)
   uint32_t off[5];   // VS: offset-bitmap words covering [base, base + 128)
   uint32_t col[4];   // VS: column-bitmap words of the tile's keys
 };
 
 template <int PAT>
-__device__ __forceinline__ MaskRaw mask_fetch(const AttnArgs& a, int n, const TileRef& ref, int q) {
+__device__ __forceinline__ MaskRaw mask_fetch(const AttnSmem& s, const AttnArgs& a, int n, int r,
+                                              const TileRef& ref, int q) {
   MaskRaw m;
   m.ref = ref;
   m.base = 0;
+  m.whole = false;
   if (PAT == kPatVS && ref.kind == 0) {
+    const int d = r - ref.t;
+    m.whole = d > 0 && ((s.dfull[d >> 5] >> (d & 31)) & 1u);
+  }
+  if (PAT == kPatVS && ref.kind == 0 && !m.whole) {
     const uint32_t* off = a.offbits + (size_t)n * a.Nw;
     const uint32_t* col = a.colbits + (size_t)n * a.Nw;
     const int j0 = ref.t * kBN;
@@ -189,15 +198,27 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
 #pragma unroll
     for (int w = 0; w < 4; ++w) out[w] = 0xFFFFFFFFu;
   } else if (PAT == kPatVS) {
+    if (m.whole) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) out[w] = 0xFFFFFFFFu;
+      return;  // never the diagonal tile (distance > 0)
+    }
     // offsets q - j0 - c for c = 0..127 are the 128 bits starting at base, reversed
     const int sh = m.base & 31;
-    const int lb = (q >> 6) << 6;  // start of the query's own 64-block
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const int k = 3 - w;
       const uint32_t win = sh ? ((m.off[k] >> sh) | (m.off[k + 1] << (32 - sh))) : m.off[k];
-      out[w] = __brev(win) | m.col[w] | range_bits(j0 + 32 * w, 0, kBlk) |
-               range_bits(j0 + 32 * w, lb, lb + kBlk);
+      out[w] = __brev(win) | m.col[w];
+    }
+    if (j0 == 0) {  // the first 64 keys
+      out[0] = 0xFFFFFFFFu;
+      out[1] = 0xFFFFFFFFu;
+    }
+    if (ref.t == r) {  // the query's own 64-block
+      const int lb = (q >> 6) << 6;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) out[w] |= range_bits(j0 + 32 * w, lb, lb + kBlk);
     }
   } else if (PAT == kPatBlock) {
     const int half = (q >> 6) & 1;
@@ -273,6 +294,7 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
       s.has_t0 = (lo == 0 || __ldg(dl + lo - 1) != r) ? 1 : 0;
       s.n_contig = lo + s.has_t0;
     }
+    for (int w = tid; w < a.NTw; w += 256) s.dfull[w] = __ldg(a.dfull + (size_t)n * a.NTw + w);
     // residual columns: selected keys in tiles 1..r-1 that no contiguous tile covers
     const int* vi = a.v_idx + (size_t)n * a.k_v;
     const uint32_t* db = a.dbits + (size_t)n * a.NTw;
@@ -464,9 +486,13 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tma_load_3d(s.q[1], &map_q, &s.q_full, 64, r * kBM, h);
     }
     int issued = 0;
+    // the next tile's reference (a global load for vertical-slash heads) is read
+    // before waiting for the buffer, so its latency overlaps that wait
+    TileRef ref_next = (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0};
     for (int t = 0; t < T; ++t) {
+      const TileRef ref = ref_next;
+      if (t + 1 < T) ref_next = tile_at<PAT>(s, a, n, r, t + 1);
       if (t >= 1 && !mbar_wait_warp(empty, (t - 1) & 1, abort, lim)) break;
-      const TileRef ref = tile_at<PAT>(s, a, n, r, t);
       if (ref.kind == 0) {
         if (lane_id() == 0) {
           mbar_arrive_expect_tx(full, 2 * 16384);
@@ -499,10 +525,10 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     // mask words are fetched one tile ahead and tile references two tiles ahead,
     // so their global loads overlap the wait for S
     TileRef ref_next2 = (T > 1) ? tile_at<PAT>(s, a, n, r, 1) : TileRef{0, 0, 0};
-    MaskRaw raw_next = mask_fetch<PAT>(a, n, (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0}, q);
+    MaskRaw raw_next = mask_fetch<PAT>(s, a, n, r, (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0}, q);
     for (int t = 0; t < T; ++t) {
       const MaskRaw raw = raw_next;
-      if (t + 1 < T) raw_next = mask_fetch<PAT>(a, n, ref_next2, q);
+      if (t + 1 < T) raw_next = mask_fetch<PAT>(s, a, n, r, ref_next2, q);
       if (t + 2 < T) ref_next2 = tile_at<PAT>(s, a, n, r, t + 2);
       ok = mbar_wait_warp(&s.s_full, t & 1, abort, lim);
       if (!ok) break;

@@ -9,6 +9,9 @@
 //            o = 128a + b touches distances a and, if b > 0, a + 1; distance 0
 //            (the local block) is always set
 //   dlist    the set distances in ascending order, dcount of them.
+//   dfull    bit delta (> 0) set when every offset a 128x128 tile at distance
+//            delta can meet, [128*delta - 127, 128*delta + 127] (within
+//            [0, N)), is selected: such a tile is kept whole for every row.
 // All are O(N/32 + k) words per head, the same for every row block.  The
 // entries are validated here: a value out of [0, N) or not strictly above its
 // predecessor raises MI_ERR_INDEX in the status word and is skipped; -1 is
@@ -26,6 +29,7 @@ struct VsIndexArgs {
   uint32_t* offbits;
   uint32_t* colbits;
   uint32_t* dbits;
+  uint32_t* dfull;
   int* dlist;
   int* dcount;
   int* status;
@@ -76,6 +80,24 @@ __global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ V
   }
   if (tid == 0) atomicOr(&db[0], 1u);
   __syncthreads();
+  // tile distances whose whole offset window is selected (read back through L2:
+  // the bitmap was just built with atomics)
+  __shared__ uint32_t dfw[512];
+  dfw[tid] = 0u;
+  __syncthreads();
+  for (int d = 1 + tid; d < a.NT; d += 512) {
+    const int lo = 128 * d - 127, hi = min(128 * d + 127, a.N - 1);  // inclusive
+    bool all = true;
+    for (int w = lo >> 5; w <= (hi >> 5) && all; ++w) {
+      uint32_t need = 0xFFFFFFFFu;
+      if (w == (lo >> 5)) need &= 0xFFFFFFFFu << (lo & 31);
+      if (w == (hi >> 5)) need &= 0xFFFFFFFFu >> (31 - (hi & 31));
+      all = (__ldcg(off + w) & need) == need;
+    }
+    if (all) atomicOr(&dfw[d >> 5], 1u << (d & 31));
+  }
+  __syncthreads();
+  if (tid < a.NTw) a.dfull[(size_t)n * a.NTw + tid] = dfw[tid];
   // dbits to global, then the ascending list of set distances
   const uint32_t word = (tid < a.NTw) ? db[tid] : 0u;
   if (tid < a.NTw) a.dbits[(size_t)n * a.NTw + tid] = word;

@@ -280,19 +280,21 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
       s.n_tiles = n_sink + (r - t_lo + 1);
     }
   } else if (PAT == kPatVS) {
-    // contiguous tiles: r - delta for the tile distances delta <= r, plus tile 0
+    // contiguous tiles: r - delta for the tile distances delta <= r, plus tile 0.
+    // All threads count the distances <= r in parallel (independent loads).
     const int* dl = a.dlist + (size_t)n * a.NT;
     const int dc = __ldg(a.dcount + n);
+    int below = 0;  // s.has_t0 was set to 1 before the barrier-init sync
+    for (int e = tid; e < dc; e += 256) {
+      const int d = __ldg(dl + e);
+      below += (d <= r) ? 1 : 0;
+      if (d == r) s.has_t0 = 0;
+    }
+    int n_below;
+    block_excl_scan_256(below, s.scan, &n_below);
     if (tid == 0) {
-      int lo = 0, hi = dc;  // first index with dl[idx] > r
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(dl + mid) <= r) lo = mid + 1;
-        else hi = mid;
-      }
-      s.d_cnt = lo;
-      s.has_t0 = (lo == 0 || __ldg(dl + lo - 1) != r) ? 1 : 0;
-      s.n_contig = lo + s.has_t0;
+      s.d_cnt = n_below;
+      s.n_contig = n_below + s.has_t0;
     }
     for (int w = tid; w < a.NTw; w += 256) s.dfull[w] = __ldg(a.dfull + (size_t)n * a.NTw + w);
     // residual columns: selected keys in tiles 1..r-1 that no contiguous tile covers
@@ -373,14 +375,16 @@ __device__ __forceinline__ void gather_tile(uint8_t (*dst)[16384], const __nv_bf
 // ---------------------------------------------------------------- kernel ----
 
 // One pass over the 128 S values of this thread's row, 64 columns per TMEM
-// wait.  Masked elements read as -inf.
+// wait.  With `apply` (which must be the same for the whole warp: the tensor
+// memory store is warp-collective), masked elements read as -inf and the masked
+// values are written back, so a later pass reads them with no mask work.
 template <class F>
-__device__ __forceinline__ void for_s_halves(uint32_t taddr, const uint32_t mk[4], bool full, F f) {
+__device__ __forceinline__ void for_s_halves(uint32_t taddr, const uint32_t mk[4], bool apply, F f) {
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     float x[64];
     tmem_ld64(taddr + hh * 64, x);
-    if (!full) {
+    if (apply) {
       const uint32_t w0 = hh ? mk[2] : mk[0];
       const uint32_t w1 = hh ? mk[3] : mk[1];
 #pragma unroll
@@ -388,6 +392,8 @@ __device__ __forceinline__ void for_s_halves(uint32_t taddr, const uint32_t mk[4
         x[e] = ((w0 >> e) & 1u) ? x[e] : -INFINITY;
         x[32 + e] = ((w1 >> e) & 1u) ? x[32 + e] : -INFINITY;
       }
+      tmem_st32(taddr + hh * 64, x);
+      tmem_st32(taddr + hh * 64 + 32, x + 32);
     }
     f(hh, x);
   }
@@ -418,6 +424,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.mma_done, 1);
     s.abort = 0;
+    s.has_t0 = 1;
     fence_mbar_init();
   }
   if (warp == 4) {
@@ -425,9 +432,14 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     tmem_relinquish();
   }
   if (tid == 160) {
-    tma_prefetch_map(&map_q);
     tma_prefetch_map(&map_k);
     tma_prefetch_map(&map_v);
+  }
+  __syncthreads();  // barriers initialised
+  if (tid == 160) {  // Q does not depend on the tile list: load it before the prologue
+    mbar_arrive_expect_tx(&s.q_full, 2 * 16384);
+    tma_load_3d(s.q[0], &map_q, &s.q_full, 0, r * kBM, h);
+    tma_load_3d(s.q[1], &map_q, &s.q_full, 64, r * kBM, h);
   }
   tc_fence_before();
   attn_prologue<PAT>(s, a, n, r);  // ends with __syncthreads
@@ -480,11 +492,6 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     uint64_t* empty = is_k ? &s.k_empty : &s.v_empty;
     uint8_t(*buf)[16384] = is_k ? s.k : s.v;
     const __nv_bfloat16* src_head = (is_k ? a.kp : a.vp) + (size_t)g * a.N * kD;
-    if (is_k && lane_id() == 0) {
-      mbar_arrive_expect_tx(&s.q_full, 2 * 16384);
-      tma_load_3d(s.q[0], &map_q, &s.q_full, 0, r * kBM, h);
-      tma_load_3d(s.q[1], &map_q, &s.q_full, 64, r * kBM, h);
-    }
     int issued = 0;
     // the next tile's reference (a global load for vertical-slash heads) is read
     // before waiting for the buffer, so its latency overlaps that wait
@@ -535,10 +542,12 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc_fence_after();
       uint32_t mk[4];
       mask_finish<PAT>(s, a, r, raw, q, mk);
-      const bool full = (mk[0] & mk[1] & mk[2] & mk[3]) == 0xFFFFFFFFu;
-      // pass 1: row maximum of the kept raw scores
+      // tcgen05.st is warp-collective: a warp masks in place if any of its rows
+      // needs it (for whole rows the mask is all ones)
+      const bool part = __any_sync(0xffffffffu, (mk[0] & mk[1] & mk[2] & mk[3]) != 0xFFFFFFFFu);
+      // pass 1: row maximum of the kept raw scores (partial tiles: masked in place)
       float mraw = -INFINITY;
-      for_s_halves(s_addr, mk, full, [&](int, const float* x) {
+      for_s_halves(s_addr, mk, part, [&](int, const float* x) {
 #pragma unroll
         for (int e = 0; e < 64; ++e) mraw = fmaxf(mraw, x[e]);
       });
@@ -565,7 +574,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
       // pass 2: P = exp2(x * sl - m) as bf16 pairs over the consumed S columns
       float rs = 0.f;
-      for_s_halves(s_addr, mk, full, [&](int hh, const float* x) {
+      for_s_halves(s_addr, mk, false, [&](int hh, const float* x) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {

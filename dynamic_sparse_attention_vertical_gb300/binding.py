@@ -45,7 +45,10 @@ SYMBOLS = (
     "mi_dense_causal_attn",
     "mi_read_status",
     "mi_strerror",
+    "mi_debug_inject",
 )
+MI_FAULT_NONE = 0
+MI_FAULT_SKIP_Q_LOAD = 1
 
 
 class MIError(RuntimeError):
@@ -84,6 +87,8 @@ def load() -> ctypes.CDLL:
     lib.mi_dense_causal_attn.restype = I
     lib.mi_read_status.argtypes = [P, P]
     lib.mi_read_status.restype = I
+    lib.mi_debug_inject.argtypes = [I, ctypes.c_uint64]
+    lib.mi_debug_inject.restype = I
     lib.mi_strerror.argtypes = [I]
     lib.mi_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -147,6 +152,11 @@ def mi_workspace_bytes(op: int, n_heads: int, Hkv: int, N: int, k_v: int = 0, k_
 
 def mi_strerror(code: int) -> str:
     return load().mi_strerror(int(code)).decode()
+
+
+def mi_debug_inject(mode: int, wait_limit_ns: int = 0) -> int:
+    """Test-only: make the attention kernels' first wait expire (see include/mi.h)."""
+    return int(load().mi_debug_inject(int(mode), int(wait_limit_ns)))
 
 
 def mi_read_status(workspace: torch.Tensor, stream=None) -> int:

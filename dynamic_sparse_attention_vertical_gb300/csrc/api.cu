@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "attention.cuh"
@@ -191,6 +192,10 @@ int launched(const char* what) {
 
 const float kScaleLog2 = 1.4426950408889634f / std::sqrt(static_cast<float>(kD));
 
+// Test-only fault injection (mi_debug_inject); normal operation: mode 0, 4 s waits.
+std::atomic<int> g_fault_mode{MI_FAULT_NONE};
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+
 int zero_status(int* status, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
   return e == cudaSuccess ? MI_OK : cuda_fail(e, "cudaMemsetAsync");
@@ -211,7 +216,8 @@ int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, 
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.status = status;
-  a.wait_limit_ns = kWaitLimitNs;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.skip_q_load = g_fault_mode.load() == MI_FAULT_SKIP_Q_LOAD ? 1 : 0;
   a.kp = reinterpret_cast<const __nv_bfloat16*>(k);
   a.vp = reinterpret_cast<const __nv_bfloat16*>(v);
   cudaError_t e = launch_attn<PAT>(mq, mk, mv, a, cdiv(N, kBM), st);
@@ -448,6 +454,19 @@ int mi_dense_causal_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
   int* status = static_cast<int*>(workspace);
   if ((rc = zero_status(status, st))) return rc;
   return run_attention<kPatDense>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
+}
+
+int mi_debug_inject(int mode, uint64_t wait_limit_ns) {
+  if (mode == MI_FAULT_NONE) {
+    g_fault_mode.store(MI_FAULT_NONE);
+    g_wait_limit_ns.store(kWaitLimitNs);
+    return MI_OK;
+  }
+  if (mode != MI_FAULT_SKIP_Q_LOAD || wait_limit_ns == 0 || wait_limit_ns > 10000000000ull)
+    return MI_ERR_ARG;
+  g_wait_limit_ns.store(wait_limit_ns);
+  g_fault_mode.store(mode);
+  return MI_OK;
 }
 
 int mi_read_status(const void* workspace, mi_stream_t stream) {

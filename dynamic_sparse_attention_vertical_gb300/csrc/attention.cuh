@@ -46,6 +46,7 @@ struct AttnArgs {
   float* lse;
   int* status;
   uint64_t wait_limit_ns;
+  int skip_q_load;  // fault injection (tests): Q is never loaded, waits expire
   // raw K/V for gathered tiles
   const __nv_bfloat16* kp;
   const __nv_bfloat16* vp;
@@ -436,7 +437,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     tma_prefetch_map(&map_v);
   }
   __syncthreads();  // barriers initialised
-  if (tid == 160) {  // Q does not depend on the tile list: load it before the prologue
+  if (tid == 160 && !a.skip_q_load) {  // Q does not depend on the tile list: load it first
     mbar_arrive_expect_tx(&s.q_full, 2 * 16384);
     tma_load_3d(s.q[0], &map_q, &s.q_full, 0, r * kBM, h);
     tma_load_3d(s.q[1], &map_q, &s.q_full, 64, r * kBM, h);

@@ -198,6 +198,21 @@ int mi_vs_estimate_noalloc(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, 
                            int32_t* v_idx, int32_t* s_idx, mi_stream_t stream);
 
 /*
+ * Test-only fault injection for the bounded-wait path.  mode 1 makes the
+ * attention kernels skip their Q load, so the first pipeline wait of every CTA
+ * expires after `wait_limit_ns`; the CTA then stops, drains what it issued,
+ * frees its tensor memory and the call reports MI_ERR_TIMEOUT through the
+ * status word.  No fault, trap or unbounded wait is involved.  mode 0 (the
+ * default) restores normal operation and the 4 s limit (wait_limit_ns is
+ * ignored).  Process-wide setting: not for concurrent use with real work.
+ * Returns MI_OK, or MI_ERR_ARG for an unknown mode or a limit of 0 or above
+ * 10 s.
+ */
+#define MI_FAULT_NONE 0
+#define MI_FAULT_SKIP_Q_LOAD 1
+int mi_debug_inject(int mode, uint64_t wait_limit_ns);
+
+/*
  * Synchronizes `stream`, then returns the status word of the last call that
  * used `workspace` (MI_OK, MI_ERR_INDEX or MI_ERR_TIMEOUT), or MI_ERR_CUDA if
  * the synchronization or the read failed.

@@ -49,3 +49,9 @@ def test_strerror_and_workspace_sizes_need_no_gpu(lib):
     vs = B.mi_workspace_bytes(B.MI_OP_VS_SPARSE_ATTN, 24, 8, 131072)
     assert vs >= 2 * 24 * 131072 // 8
     assert B.mi_workspace_bytes(99, 1, 1, 64) == 0
+
+
+def test_fault_injection_argument_checks(lib):
+    assert B.mi_debug_inject(7, 1000) == B.MI_ERR_ARG
+    assert B.mi_debug_inject(B.MI_FAULT_SKIP_Q_LOAD, 0) == B.MI_ERR_ARG
+    assert B.mi_debug_inject(B.MI_FAULT_NONE, 0) == B.MI_OK

@@ -300,3 +300,21 @@ def test_argument_and_index_errors():
     good_s = torch.tensor([[0, 7], [1, -1]], dtype=torch.int32, device=DEV)
     B.mi_vs_sparse_attn(q, k, v, good_v, good_s, workspace=ws)
     assert B.mi_read_status(ws) == B.MI_OK
+
+
+def test_bounded_wait_expiry_reports_timeout():
+    """A wait that nothing completes expires, the call reports MI_ERR_TIMEOUT, the context stays usable."""
+    N = 256
+    x = _rand_inputs(2, 1, N, seed=12)
+    q, k, v = _dev(x)
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    assert B.mi_debug_inject(B.MI_FAULT_SKIP_Q_LOAD, 2_000_000) == B.MI_OK  # 2 ms
+    try:
+        B.mi_dense_causal_attn(q, k, v, workspace=ws)
+        assert B.mi_read_status(ws) == B.MI_ERR_TIMEOUT
+    finally:
+        assert B.mi_debug_inject(B.MI_FAULT_NONE) == B.MI_OK
+    out = B.mi_dense_causal_attn(q, k, v, workspace=ws)
+    assert B.mi_read_status(ws) == B.MI_OK
+    ref, _ = O.attention_rows(x.q[0], x.k[0], x.v[0], np.arange(N), lambda r: O.causal_mask_rows(N, r))
+    assert_close(out.float().cpu().numpy()[0], ref, "after timeout")

@@ -296,6 +296,52 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------- sweep ----
+
+SWEEP_N = (16384, 65536, 131072, 262144, 524288)
+SWEEP_KV = (500, 1000, 2000)
+SWEEP_KS = (2048, 6096)
+
+
+def run_sweep(args, B):
+    """All-vertical-slash layers (32 q / 8 KV heads) over N x k_v x k_s, against the
+    dense causal kernel on identical inputs.  One JSON line with every point."""
+    from dynamic_sparse_attention_vertical_gb300 import flops as F
+    from dynamic_sparse_attention_vertical_gb300 import inputs as I
+    dev = torch.device("cuda")
+    points = []
+    Ns = [int(v) for v in args.sweep_n.split(",")] if args.sweep_n else SWEEP_N
+    for variant in [v for v in args.variants.split(",") if v]:
+        for N in Ns:
+            gen = I.local_inputs if variant == "local" else I.literal_inputs
+            x = gen(32, 8, N, n_cols=16, n_offsets=8, seed=5, device=dev)
+            out = torch.zeros_like(x.q)
+            ws_d = torch.empty(256, dtype=torch.uint8, device=dev)
+            B.mi_dense_causal_attn(x.q, x.k, x.v, out=out, workspace=ws_d)
+            dms, _ = timed(lambda e: B.mi_dense_causal_attn(x.q, x.k, x.v, out=out, workspace=ws_d), 2)
+            for k_v in SWEEP_KV:
+                for k_s in SWEEP_KS:
+                    v_idx = torch.empty((32, k_v), dtype=torch.int32, device=dev)
+                    s_idx = torch.empty((32, k_s), dtype=torch.int32, device=dev)
+                    ws_e = torch.empty(B.mi_workspace_bytes(B.MI_OP_VS_ESTIMATE, 32, 8, N), dtype=torch.uint8, device=dev)
+                    ws_v = torch.empty(B.mi_workspace_bytes(B.MI_OP_VS_SPARSE_ATTN, 32, 8, N), dtype=torch.uint8, device=dev)
+
+                    def step(_):
+                        B.mi_vs_estimate(x.q, x.k, k_v=k_v, k_s=k_s, v_idx=v_idx, s_idx=s_idx, workspace=ws_e)
+                        B.mi_vs_sparse_attn(x.q, x.k, x.v, v_idx, s_idx, out=out, workspace=ws_v)
+                    step(None)
+                    ms, _ = timed(step, args.steps)
+                    vi, si = v_idx.cpu().numpy(), s_idx.cpu().numpy()
+                    alg = sum(int(F.vs_kept_per_row(N, vi[h], si[h], device=dev).sum()) for h in range(32)) * 4 * 128
+                    exe = sum(F.vs_tiles(N, vi[h], si[h]) for h in range(32)) * F.TILE_FLOPS
+                    points.append({"variant": variant, "N": N, "k_v": k_v, "k_s": k_s, "ms_per_layer": ms,
+                                   "dense_ms": dms, "speedup": dms / ms, "alg_tflop": alg / 1e12,
+                                   "exec_tflop": exe / 1e12, "exec_tflops": exe / (ms * 1e-3) / 1e12})
+            del x, out
+            torch.cuda.empty_cache()
+    print(json.dumps({"metric": METRIC, "unit": "ms/layer", "sweep": points}), flush=True)
+
+
 # -------------------------------------------------------------------- main ----
 
 def main():
@@ -309,6 +355,8 @@ def main():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time the N x k_v x k_s sweep instead")
+    ap.add_argument("--sweep-n", default="", help="comma-separated N values for --sweep")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
     w = WORKLOADS[args.workload]
@@ -338,6 +386,9 @@ def main():
 
     from dynamic_sparse_attention_vertical_gb300 import binding as B
     B.load()
+    if args.sweep:
+        run_sweep(args, B)
+        return
     burst, sustained, hbm, peak_src = measured_peaks()
     dev = torch.device("cuda", local_rank)
     variants = [v for v in args.variants.split(",") if v]

@@ -11,16 +11,14 @@
 //     gittoolsai.com, "TL;DR" and the PIT note; talk slides, boteman.cn,
 //     "Dynamic Sparse Attention Calculation with PIT, FlashAttention").
 //
-// Warp roles (256 threads, two CTAs per SM):
+// Warp roles (192 threads, two CTAs per SM, up to 168 registers per thread):
 //   warps 0-3   softmax: thread t owns query row t (TMEM lane t)
 //   warp 4      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warp 5      Q (once) and K tiles (TMA, or cp.async gather)
-//   warp 6      V tiles (TMA, or cp.async gather)
-//   warp 7      idle after the prologue
+//   warp 5      Q (once), then K and V tiles (TMA, or cp.async gather)
 //
 // Tensor memory (256 columns): S = Q K^T (fp32, columns 0-127) and O (fp32,
 // columns 128-255).  Per tile: the MMA warp issues S = Q K_i^T; the softmax
-// warps read S in two passes (row maximum, then exp2 and pack), and write
+// warps read their S row into registers once (mask, row maximum, exp2, pack), and write
 // P_i = exp2(x - m) as bf16 pairs over the S columns they have consumed; the
 // MMA warp then issues O += P_i V_i with P read from tensor memory.  The
 // running maximum moves (and O is rescaled in tensor memory) only when a
@@ -73,7 +71,7 @@ struct AttnSmem {
   alignas(1024) uint8_t k[2][16384];
   alignas(1024) uint8_t v[2][16384];
   int list[MI_MAX_KV];  // VS: residual columns; block: (tile << 4) | sub-block mask
-  int scan[256];
+  int scan[192];
   uint32_t dfull[512];  // VS: the head's whole-tile distance bits (N <= 2^21)
   uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, mma_done;
   uint32_t tmem;
@@ -85,6 +83,7 @@ struct AttnSmem {
   int d_cnt;     // VS: number of tile distances <= r
 };
 
+constexpr int kAttnThreads = 192;
 constexpr size_t kAttnSmemBytes = sizeof(AttnSmem) + 1024;
 constexpr uint32_t kTmemCols = 256;  // S (and P over it) at 0, O at 128
 constexpr uint32_t kTmemO = 128;
@@ -243,20 +242,20 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
 
 // ------------------------------------------------------------- prologue ----
 
-// Block-wide exclusive scan of one int per thread (256 threads); returns the
+// Block-wide exclusive scan of one int per thread (192 threads); returns the
 // exclusive prefix and writes the total to *total.
-__device__ __forceinline__ int block_excl_scan_256(int x, int* scratch, int* total) {
+__device__ __forceinline__ int block_excl_scan(int x, int* scratch, int* total) {
   const int tid = threadIdx.x;
   scratch[tid] = x;
   __syncthreads();
-  for (int off = 1; off < 256; off <<= 1) {
+  for (int off = 1; off < 192; off <<= 1) {
     const int y = (tid >= off) ? scratch[tid - off] : 0;
     __syncthreads();
     scratch[tid] += y;
     __syncthreads();
   }
   const int incl = scratch[tid];
-  *total = scratch[255];
+  *total = scratch[191];
   __syncthreads();
   return incl - x;
 }
@@ -286,27 +285,27 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
     const int* dl = a.dlist + (size_t)n * a.NT;
     const int dc = __ldg(a.dcount + n);
     int below = 0;  // s.has_t0 was set to 1 before the barrier-init sync
-    for (int e = tid; e < dc; e += 256) {
+    for (int e = tid; e < dc; e += 192) {
       const int d = __ldg(dl + e);
       below += (d <= r) ? 1 : 0;
       if (d == r) s.has_t0 = 0;
     }
     int n_below;
-    block_excl_scan_256(below, s.scan, &n_below);
+    block_excl_scan(below, s.scan, &n_below);
     if (tid == 0) {
       s.d_cnt = n_below;
       s.n_contig = n_below + s.has_t0;
     }
-    for (int w = tid; w < a.NTw; w += 256) s.dfull[w] = __ldg(a.dfull + (size_t)n * a.NTw + w);
+    for (int w = tid; w < a.NTw; w += 192) s.dfull[w] = __ldg(a.dfull + (size_t)n * a.NTw + w);
     // residual columns: selected keys in tiles 1..r-1 that no contiguous tile covers
     const int* vi = a.v_idx + (size_t)n * a.k_v;
     const uint32_t* db = a.dbits + (size_t)n * a.NTw;
-    const int per = cdiv(a.k_v, 256);
+    const int per = cdiv(a.k_v, 192);
     const int beg = min(tid * per, a.k_v), end = min(beg + per, a.k_v);
     int cnt = 0;
     for (int e = beg; e < end; ++e) cnt += residual_column(__ldg(vi + e), a.N, r, db) ? 1 : 0;
     int total;
-    int pos = block_excl_scan_256(cnt, s.scan, &total);
+    int pos = block_excl_scan(cnt, s.scan, &total);
     for (int e = beg; e < end; ++e) {
       const int j = __ldg(vi + e);
       if (residual_column(j, a.N, r, db)) s.list[pos++] = j;
@@ -401,7 +400,7 @@ __device__ __forceinline__ void for_s_halves(uint32_t taddr, const uint32_t mk[4
 }
 
 template <int PAT>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(kAttnThreads, 2)
 attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -485,22 +484,16 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       mbar_wait_drain(&s.mma_done, 0, lim);
     }
     __syncwarp();
-  } else if (warp == 5 || warp == 6) {
-    // --------------------------------------------------------- loaders ----
-    const bool is_k = (warp == 5);
-    const CUtensorMap* map = is_k ? &map_k : &map_v;
-    uint64_t* full = is_k ? &s.k_full : &s.v_full;
-    uint64_t* empty = is_k ? &s.k_empty : &s.v_empty;
-    uint8_t(*buf)[16384] = is_k ? s.k : s.v;
-    const __nv_bfloat16* src_head = (is_k ? a.kp : a.vp) + (size_t)g * a.N * kD;
+  } else if (warp == 5) {
+    // -------------------------------------------------------------- loader ----
+    const __nv_bfloat16* k_head = a.kp + (size_t)g * a.N * kD;
+    const __nv_bfloat16* v_head = a.vp + (size_t)g * a.N * kD;
     int issued = 0;
     // the next tile's reference (a global load for vertical-slash heads) is read
-    // before waiting for the buffer, so its latency overlaps that wait
+    // before waiting for the buffers, so its latency overlaps those waits
     TileRef ref_next = (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0};
-    for (int t = 0; t < T; ++t) {
-      const TileRef ref = ref_next;
-      if (t + 1 < T) ref_next = tile_at<PAT>(s, a, n, r, t + 1);
-      if (t >= 1 && !mbar_wait_warp(empty, (t - 1) & 1, abort, lim)) break;
+    auto load = [&](const TileRef& ref, const CUtensorMap* map, uint64_t* full, uint8_t (*buf)[16384],
+                    const __nv_bfloat16* head) {
       if (ref.kind == 0) {
         if (lane_id() == 0) {
           mbar_arrive_expect_tx(full, 2 * 16384);
@@ -509,16 +502,29 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         }
       } else {
         const int valid = min(kBN, s.n_list - ref.t * kBN);
-        gather_tile(buf, src_head, s.list + ref.t * kBN, valid);
+        gather_tile(buf, head, s.list + ref.t * kBN, valid);
         if (lane_id() == 0) mbar_arrive(full);
       }
+    };
+    for (int t = 0; t < T; ++t) {
+      const TileRef ref = ref_next;
+      if (t + 1 < T) ref_next = tile_at<PAT>(s, a, n, r, t + 1);
+      if (t >= 1 && !mbar_wait_warp(&s.k_empty, (t - 1) & 1, abort, lim)) break;
+      load(ref, &map_k, &s.k_full, s.k, k_head);
+      if (t >= 1 && !mbar_wait_warp(&s.v_empty, (t - 1) & 1, abort, lim)) {
+        issued = -(t + 1);  // K of tile t issued, V not
+        break;
+      }
+      load(ref, &map_v, &s.v_full, s.v, v_head);
       issued = t + 1;
       __syncwarp();
     }
-    // drain: the last load must land before the CTA can exit
+    // drain: the last loads must land before the CTA can exit
     if (lane_id() == 0) {
-      if (is_k) mbar_wait_drain(&s.q_full, 0, lim);
-      if (issued > 0) mbar_wait_drain(full, (issued - 1) & 1, lim);
+      mbar_wait_drain(&s.q_full, 0, lim);
+      const int nk = issued < 0 ? -issued : issued, nv = issued < 0 ? -issued - 1 : issued;
+      if (nk > 0) mbar_wait_drain(&s.k_full, (nk - 1) & 1, lim);
+      if (nv > 0) mbar_wait_drain(&s.v_full, (nv - 1) & 1, lim);
     }
     __syncwarp();
   } else if (warp < 4) {
@@ -545,13 +551,18 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       mask_finish<PAT>(s, a, r, raw, q, mk);
       // tcgen05.st is warp-collective: a warp masks in place if any of its rows
       // needs it (for whole rows the mask is all ones)
-      const bool part = __any_sync(0xffffffffu, (mk[0] & mk[1] & mk[2] & mk[3]) != 0xFFFFFFFFu);
-      // pass 1: row maximum of the kept raw scores (partial tiles: masked in place)
-      float mraw = -INFINITY;
-      for_s_halves(s_addr, mk, part, [&](int, const float* x) {
+      const bool full = (mk[0] & mk[1] & mk[2] & mk[3]) == 0xFFFFFFFFu;
+      // the row of S in registers: one tensor-memory read per tile
+      float x[128];
+      tmem_ld64(s_addr, x);
+      tmem_ld64(s_addr + 64, x + 64);
+      if (!full) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) mraw = fmaxf(mraw, x[e]);
-      });
+        for (int e = 0; e < 128; ++e) x[e] = ((mk[e >> 5] >> (e & 31)) & 1u) ? x[e] : -INFINITY;
+      }
+      float mraw = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 128; ++e) mraw = fmaxf(mraw, x[e]);
       const float mx = mraw * sl;  // sl > 0: the maximum commutes with the scale
       const bool upd = mx > m_ref + 8.0f;
       const bool rescale_o = upd && (m_ref != -INFINITY);
@@ -561,7 +572,25 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         l *= alpha;
         m_ref = mx;
       }
-      // O holds P.V of tiles < t (that P.V completed before S of tile t was written)
+      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // P = exp2(x * sl - m) as bf16 pairs over the consumed S columns
+      float rs = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = fast_exp2(fmaf(x[hh * 64 + 2 * e], sl, -mb));
+          const float p1 = fast_exp2(fmaf(x[hh * 64 + 2 * e + 1], sl, -mb));
+          rs += p0 + p1;
+          __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
+          pk[e] = *reinterpret_cast<uint32_t*>(&bb);
+        }
+        tmem_st32u(s_addr + hh * 32, pk);
+      }
+      // O holds P.V of tiles < t (that P.V completed before S of tile t was
+      // written); it is rescaled after P is stored, when the row is dead
+      // and its registers are free
       if (__any_sync(0xffffffffu, rescale_o)) {  // tcgen05.ld/st are warp-collective
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -572,21 +601,6 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tmem_st32(o_addr + c * 32, o);
         }
       }
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // pass 2: P = exp2(x * sl - m) as bf16 pairs over the consumed S columns
-      float rs = 0.f;
-      for_s_halves(s_addr, mk, false, [&](int hh, const float* x) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = fast_exp2(fmaf(x[2 * e], sl, -mb));
-          const float p1 = fast_exp2(fmaf(x[2 * e + 1], sl, -mb));
-          rs += p0 + p1;
-          __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
-          pk[e] = *reinterpret_cast<uint32_t*>(&bb);
-        }
-        tmem_st32u(s_addr + hh * 32, pk);
-      });
       l += rs;
       tc_fence_before();
       mbar_arrive(&s.p_full);

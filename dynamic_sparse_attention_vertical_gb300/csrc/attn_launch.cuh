@@ -11,7 +11,7 @@ cudaError_t launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
   static cudaError_t attr = cudaFuncSetAttribute(
       attn_kernel<PAT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kAttnSmemBytes));
   if (attr != cudaSuccess) return attr;
-  attn_kernel<PAT><<<dim3(n_row_blocks, a.heads.n), 256, kAttnSmemBytes, st>>>(mq, mk, mv, a);
+  attn_kernel<PAT><<<dim3(n_row_blocks, a.heads.n), kAttnThreads, kAttnSmemBytes, st>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 

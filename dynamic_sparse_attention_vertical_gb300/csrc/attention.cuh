@@ -560,9 +560,16 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 #pragma unroll
         for (int e = 0; e < 128; ++e) x[e] = ((mk[e >> 5] >> (e & 31)) & 1u) ? x[e] : -INFINITY;
       }
-      float mraw = -INFINITY;
+      // row maximum as a tree: eight independent chains of three-input max
+      float m8[8];
 #pragma unroll
-      for (int e = 0; e < 128; ++e) mraw = fmaxf(mraw, x[e]);
+      for (int j = 0; j < 8; ++j) m8[j] = fmaxf(x[j], x[8 + j]);
+#pragma unroll
+      for (int e = 16; e < 128; e += 16) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m8[j] = fmax3(m8[j], x[e + j], x[e + 8 + j]);
+      }
+      const float mraw = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
       const float mx = mraw * sl;  // sl > 0: the maximum commutes with the scale
       const bool upd = mx > m_ref + 8.0f;
       const bool rescale_o = upd && (m_ref != -INFINITY);
@@ -574,7 +581,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
       // P = exp2(x * sl - m) as bf16 pairs over the consumed S columns
-      float rs = 0.f;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
@@ -582,7 +589,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         for (int e = 0; e < 32; ++e) {
           const float p0 = fast_exp2(fmaf(x[hh * 64 + 2 * e], sl, -mb));
           const float p1 = fast_exp2(fmaf(x[hh * 64 + 2 * e + 1], sl, -mb));
-          rs += p0 + p1;
+          rs8[e & 7] += p0 + p1;
           __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
           pk[e] = *reinterpret_cast<uint32_t*>(&bb);
         }
@@ -601,7 +608,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tmem_st32(o_addr + c * 32, o);
         }
       }
-      l += rs;
+      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       tc_fence_before();
       mbar_arrive(&s.p_full);
     }

@@ -101,6 +101,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 // ------------------------------------------------------------------ TMA ----
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {

@@ -108,7 +108,7 @@ __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a,
         ref.t = 0;
       } else {
         const int idx = s.d_cnt - 1 - (i - s.has_t0);
-        ref.t = r - __ldg(a.dlist + (size_t)n * a.NT + idx);
+        ref.t = r - ldg_ahead(a.dlist + (size_t)n * a.NT + idx);
       }
     } else {
       ref.kind = 1;
@@ -174,10 +174,11 @@ __device__ __forceinline__ MaskRaw mask_fetch(const AttnSmem& s, const AttnArgs&
 #pragma unroll
     for (int i = 0; i < 5; ++i) {
       const int wi = w0 + i;  // < Nw: q - j0 < NT * 128
-      m.off[i] = (wi >= 0) ? __ldg(off + wi) : 0u;
+      m.off[i] = ldg_ahead(off + max(wi, 0));
+      if (wi < 0) m.off[i] = 0u;
     }
 #pragma unroll
-    for (int w = 0; w < 4; ++w) m.col[w] = __ldg(col + (j0 >> 5) + w);
+    for (int w = 0; w < 4; ++w) m.col[w] = ldg_ahead(col + (j0 >> 5) + w);
   }
   return m;
 }

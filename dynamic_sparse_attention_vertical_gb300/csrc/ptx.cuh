@@ -101,6 +101,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Read-only global load that stays where it is written: the load is issued
+// here and only its first use waits, so a load made a tile ahead of its use
+// hides its latency (the compiler may not sink or re-issue a volatile asm).
+__device__ __forceinline__ uint32_t ldg_ahead(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int ldg_ahead(const int* p) {
+  int v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float y;

@@ -68,6 +68,29 @@ int make_map(CUtensorMap* m, const void* base, int heads, int N, int box_rows) {
   return MI_OK;
 }
 
+// [heads, N, 128] bf16 as a 2-D tensor (d, heads * N) with a 64 x 1 box and
+// 128-byte swizzle: the map for tile::gather4 loads of scattered key rows.
+int make_rows_map(CUtensorMap* m, const void* base, int heads, int N) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled is not available from the driver");
+    return MI_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
+                        static_cast<cuuint64_t>(heads) * static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MI_ERR_CUDA;
+  }
+  return MI_OK;
+}
+
 int check_device() {
   static int verdict[64];  // 0 unknown, 1 sm_103, -1 other (benign race: same value)
   int dev = 0;
@@ -205,11 +228,17 @@ int zero_status(int* status, cudaStream_t st) {
 template <int PAT>
 int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, int N,
                   mi_bf16* out, float* lse, int* status, AttnArgs& a, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mkr, mvr;
   int rc;
   if ((rc = make_map(&mq, q, Hq, N, kBM)) || (rc = make_map(&mk, k, Hkv, N, kBN)) ||
       (rc = make_map(&mv, v, Hkv, N, kBN)))
     return rc;
+  if (PAT == kPatVS) {  // gathered column tiles
+    if ((rc = make_rows_map(&mkr, k, Hkv, N)) || (rc = make_rows_map(&mvr, v, Hkv, N))) return rc;
+  } else {
+    mkr = mk;
+    mvr = mv;
+  }
   a.N = N;
   a.group = Hq / Hkv;
   a.scale_log2 = kScaleLog2;
@@ -218,9 +247,7 @@ int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, 
   a.status = status;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.skip_q_load = g_fault_mode.load() == MI_FAULT_SKIP_Q_LOAD ? 1 : 0;
-  a.kp = reinterpret_cast<const __nv_bfloat16*>(k);
-  a.vp = reinterpret_cast<const __nv_bfloat16*>(v);
-  cudaError_t e = launch_attn<PAT>(mq, mk, mv, a, cdiv(N, kBM), st);
+  cudaError_t e = launch_attn<PAT>(mq, mk, mv, mkr, mvr, a, cdiv(N, kBM), st);
   return e == cudaSuccess ? MI_OK : cuda_fail(e, "attention kernel");
 }
 

@@ -5,8 +5,8 @@
 //   - contiguous tiles, TMA-loaded from K/V ([Hkv, N, 128] bf16, 128-byte
 //     swizzle), masked element-wise by the pattern's rule;
 //   - for vertical-slash heads, "gathered" tiles of up to 128 scattered key
-//     columns that no contiguous tile covers, copied row by row into the same
-//     swizzled layout (the permutation-invariant gathering idea of PIT, which
+//     columns that no contiguous tile covers, loaded four rows at a time with
+//     TMA tile::gather4 into the same swizzled layout (the permutation-invariant gathering idea of PIT, which
 //     the MInference pages name as the basis of their kernels: README mirror,
 //     gittoolsai.com, "TL;DR" and the PIT note; talk slides, boteman.cn,
 //     "Dynamic Sparse Attention Calculation with PIT, FlashAttention").
@@ -14,7 +14,7 @@
 // Warp roles (192 threads, two CTAs per SM, up to 168 registers per thread):
 //   warps 0-3   softmax: thread t owns query row t (TMEM lane t)
 //   warp 4      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warp 5      Q (once), then K and V tiles (TMA, or cp.async gather)
+//   warp 5      Q (once), then K and V tiles (TMA tiles, or TMA gather4)
 //
 // Tensor memory (256 columns): S = Q K^T (fp32, columns 0-127) and O (fp32,
 // columns 128-255).  Per tile: the MMA warp issues S = Q K_i^T; the softmax
@@ -45,9 +45,6 @@ struct AttnArgs {
   int* status;
   uint64_t wait_limit_ns;
   int skip_q_load;  // fault injection (tests): Q is never loaded, waits expire
-  // raw K/V for gathered tiles
-  const __nv_bfloat16* kp;
-  const __nv_bfloat16* vp;
   // vertical-slash index structures (per listed head)
   const uint32_t* offbits;  // [n_heads, Nw]   bit o: offset o selected
   const uint32_t* colbits;  // [n_heads, Nw]   bit j: column j selected
@@ -354,25 +351,6 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
 
 // ------------------------------------------------------------- loaders ----
 
-// Copy up to 128 gathered key rows (256 bytes each) into a swizzled [2][128][128B]
-// tile; rows past `valid` are zero-filled.  One warp.
-__device__ __forceinline__ void gather_tile(uint8_t (*dst)[16384], const __nv_bfloat16* src_head,
-                                            const int* cols, int valid) {
-  const int lane = threadIdx.x & 31;
-  for (int e = lane; e < kBN * 16; e += 32) {
-    const int row = e >> 4, u = e & 15;
-    uint8_t* d = dst[u >> 3] + sw128_offset(row, u & 7);
-    if (row < valid) {
-      cp_async_16(d, src_head + (size_t)cols[row] * kD + u * 8);
-    } else {
-      *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-    }
-  }
-  cp_async_wait_all();
-  fence_proxy_async_smem();
-  __syncwarp();
-}
-
 // ---------------------------------------------------------------- kernel ----
 
 // One pass over the 128 S values of this thread's row, 64 columns per TMEM
@@ -403,7 +381,8 @@ __device__ __forceinline__ void for_s_halves(uint32_t taddr, const uint32_t mk[4
 template <int PAT>
 __global__ void __launch_bounds__(kAttnThreads, 2)
 attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ AttnArgs a) {
+            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_kr,
+            const __grid_constant__ CUtensorMap map_vr, const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& s = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -435,6 +414,10 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   if (tid == 160) {
     tma_prefetch_map(&map_k);
     tma_prefetch_map(&map_v);
+    if (PAT == kPatVS) {
+      tma_prefetch_map(&map_kr);
+      tma_prefetch_map(&map_vr);
+    }
   }
   __syncthreads();  // barriers initialised
   if (tid == 160 && !a.skip_q_load) {  // Q does not depend on the tile list: load it first
@@ -487,14 +470,12 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     __syncwarp();
   } else if (warp == 5) {
     // -------------------------------------------------------------- loader ----
-    const __nv_bfloat16* k_head = a.kp + (size_t)g * a.N * kD;
-    const __nv_bfloat16* v_head = a.vp + (size_t)g * a.N * kD;
     int issued = 0;
     // the next tile's reference (a global load for vertical-slash heads) is read
     // before waiting for the buffers, so its latency overlaps those waits
     TileRef ref_next = (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0};
-    auto load = [&](const TileRef& ref, const CUtensorMap* map, uint64_t* full, uint8_t (*buf)[16384],
-                    const __nv_bfloat16* head) {
+    auto load = [&](const TileRef& ref, const CUtensorMap* map, const CUtensorMap* rows_map,
+                    uint64_t* full, uint8_t (*buf)[16384]) {
       if (ref.kind == 0) {
         if (lane_id() == 0) {
           mbar_arrive_expect_tx(full, 2 * 16384);
@@ -502,21 +483,32 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tma_load_3d(buf[1], map, full, 64, ref.t * kBN, g);
         }
       } else {
-        const int valid = min(kBN, s.n_list - ref.t * kBN);
-        gather_tile(buf, head, s.list + ref.t * kBN, valid);
-        if (lane_id() == 0) mbar_arrive(full);
+        // up to 128 residual columns, four rows per tile::gather4 load: lane l
+        // loads rows 4l..4l+3 of both 64-column halves; rows past the list
+        // repeat its last column (their scores are masked)
+        const int* cols = s.list + ref.t * kBN;
+        const int last = min(kBN, s.n_list - ref.t * kBN) - 1;
+        const int base_row = g * a.N;
+        if (lane_id() == 0) mbar_arrive_expect_tx(full, 2 * 16384);
+        __syncwarp();
+        const int l = lane_id();
+        int y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) y[i] = base_row + cols[min(4 * l + i, last)];
+        tma_gather4(buf[0] + 512 * l, rows_map, full, 0, y[0], y[1], y[2], y[3]);
+        tma_gather4(buf[1] + 512 * l, rows_map, full, 64, y[0], y[1], y[2], y[3]);
       }
     };
     for (int t = 0; t < T; ++t) {
       const TileRef ref = ref_next;
       if (t + 1 < T) ref_next = tile_at<PAT>(s, a, n, r, t + 1);
       if (t >= 1 && !mbar_wait_warp(&s.k_empty, (t - 1) & 1, abort, lim)) break;
-      load(ref, &map_k, &s.k_full, s.k, k_head);
+      load(ref, &map_k, &map_kr, &s.k_full, s.k);
       if (t >= 1 && !mbar_wait_warp(&s.v_empty, (t - 1) & 1, abort, lim)) {
         issued = -(t + 1);  // K of tile t issued, V not
         break;
       }
-      load(ref, &map_v, &s.v_full, s.v, v_head);
+      load(ref, &map_v, &map_vr, &s.v_full, s.v);
       issued = t + 1;
       __syncwarp();
     }
@@ -661,6 +653,7 @@ namespace mi {
 // pattern variants compile in parallel.
 template <int PAT>
 cudaError_t launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                        const AttnArgs& a, int n_row_blocks, cudaStream_t st);
+                        const CUtensorMap& mkr, const CUtensorMap& mvr, const AttnArgs& a,
+                        int n_row_blocks, cudaStream_t st);
 
 }  // namespace mi

@@ -2,8 +2,9 @@
 #include "attn_launch.cuh"
 
 namespace mi {
-template cudaError_t launch_attn<kPatVS>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                         const AttnArgs&, int, cudaStream_t);
-template cudaError_t launch_attn<kPatBlock>(const CUtensorMap&, const CUtensorMap&,
-                                            const CUtensorMap&, const AttnArgs&, int, cudaStream_t);
+#define MI_ATTN_MAPS const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, \
+                     const CUtensorMap&
+template cudaError_t launch_attn<kPatVS>(MI_ATTN_MAPS, const AttnArgs&, int, cudaStream_t);
+template cudaError_t launch_attn<kPatBlock>(MI_ATTN_MAPS, const AttnArgs&, int, cudaStream_t);
+#undef MI_ATTN_MAPS
 }  // namespace mi

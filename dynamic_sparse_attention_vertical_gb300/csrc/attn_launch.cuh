@@ -7,11 +7,12 @@ namespace mi {
 
 template <int PAT>
 cudaError_t launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                        const AttnArgs& a, int n_row_blocks, cudaStream_t st) {
+                        const CUtensorMap& mkr, const CUtensorMap& mvr, const AttnArgs& a,
+                        int n_row_blocks, cudaStream_t st) {
   static cudaError_t attr = cudaFuncSetAttribute(
       attn_kernel<PAT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kAttnSmemBytes));
   if (attr != cudaSuccess) return attr;
-  attn_kernel<PAT><<<dim3(n_row_blocks, a.heads.n), kAttnThreads, kAttnSmemBytes, st>>>(mq, mk, mv, a);
+  attn_kernel<PAT><<<dim3(n_row_blocks, a.heads.n), kAttnThreads, kAttnSmemBytes, st>>>(mq, mk, mv, mkr, mvr, a);
   return cudaGetLastError();
 }
 

@@ -158,6 +158,7 @@ class Layer:
         self.ws_blk = ws(B.MI_OP_BLOCK_SPARSE_ATTN, nb)
         self.ws_ash = ws(B.MI_OP_ASHAPE_ATTN, 1)
         self.ws_dense = ws(B.MI_OP_DENSE_CAUSAL_ATTN, 1)
+        self.expanded = False  # vertical-slash heads in the block-expanded slash mode
         self.kernels_per_step = (KERNELS_PER_STEP["vs"] if nv else 0) + (KERNELS_PER_STEP["block"] if nb else 0) \
             + (KERNELS_PER_STEP["ashape"] if self.ash else 0)
 
@@ -171,7 +172,7 @@ class Layer:
             if ev:
                 ev[1].record()
             B.mi_vs_sparse_attn(self.q, self.k, self.v, self.v_idx, self.s_idx, heads=self.vs, out=self.out,
-                                workspace=self.ws_vs)
+                                workspace=self.ws_vs, expanded=self.expanded)
         elif ev:
             ev[1].record()
         if ev:
@@ -208,8 +209,11 @@ class Layer:
         vi = self.v_idx.cpu().numpy()
         si = self.s_idx.cpu().numpy()
         for n in range(len(self.vs)):
-            alg["vs"] += int(F.vs_kept_per_row(N, vi[n], si[n], device=dev).sum())
-            tiles["vs"] += F.vs_tiles(N, vi[n], si[n])
+            if self.expanded:
+                alg["vs"] += int(F.vs_expanded_kept_per_row(N, vi[n], si[n]).sum())
+            else:
+                alg["vs"] += int(F.vs_kept_per_row(N, vi[n], si[n], device=dev).sum())
+            tiles["vs"] += F.vs_tiles(N, vi[n], si[n], expanded=self.expanded)
         bl = self.blk_idx.cpu().numpy()
         for n in range(len(self.blk)):
             sel = [r[r >= 0] for r in bl[n]]
@@ -355,6 +359,8 @@ def main():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-expanded", action="store_true",
+                    help="skip the extra timing of the block-expanded slash mode")
     ap.add_argument("--sweep", action="store_true", help="time the N x k_v x k_s sweep instead")
     ap.add_argument("--sweep-n", default="", help="comma-separated N values for --sweep")
     args = ap.parse_args()
@@ -425,6 +431,26 @@ def main():
                "alg_tflop_per_layer": sum(alg.values()) / 1e12, "exec_tflop_per_layer": sum(exe.values()) / 1e12,
                "vs_attention_alg_tflops": alg["vs"] / (st["vs_attention_ms"] * 1e-3) / 1e12 if alg["vs"] else None,
                "vs_attention_exec_tflops": exe["vs"] / (st["vs_attention_ms"] * 1e-3) / 1e12 if exe["vs"] else None}
+        if L.vs and not args.no_expanded:
+            # the same layer with the vertical-slash heads in the block-expanded slash mode
+            L.expanded = True
+            L.step()
+            torch.cuda.synchronize()
+            L.check_status()
+            barrier()
+            xms, xevs = timed(L.step, args.steps, events_per_step=5)
+            barrier()
+            xms = max_over_ranks(xms)
+            xst = {"estimate_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in xevs),
+                   "vs_attention_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in xevs)}
+            xalg, xexe = L.work()
+            res["block_expanded"] = {
+                "ms_per_layer": xms / world, "stages": xst,
+                "alg_tflop_per_layer": sum(xalg.values()) / 1e12,
+                "exec_tflop_per_layer": sum(xexe.values()) / 1e12,
+                "vs_attention_alg_tflops": xalg["vs"] / (xst["vs_attention_ms"] * 1e-3) / 1e12,
+                "vs_attention_exec_tflops": xexe["vs"] / (xst["vs_attention_ms"] * 1e-3) / 1e12}
+            L.expanded = False
         if headline:
             if not args.no_dense:
                 for _ in range(1):
@@ -503,6 +529,8 @@ def main():
     if dense_ms:
         for r in line["variants"].values():
             r["dense_equiv_speedup"] = dense_ms / r["ms_per_layer"]
+            if "block_expanded" in r:
+                r["block_expanded"]["dense_equiv_speedup"] = dense_ms / r["block_expanded"]["ms_per_layer"]
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

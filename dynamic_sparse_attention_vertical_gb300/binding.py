@@ -33,6 +33,7 @@ MI_OP_BLOCK_SPARSE_ATTN = 3
 MI_OP_ASHAPE_ATTN = 4
 MI_OP_DENSE_CAUSAL_ATTN = 5
 MI_IDX_GIVEN = 1
+MI_VS_BLOCK_EXPANDED = 1
 
 # every entry point of include/mi.h
 SYMBOLS = (
@@ -77,7 +78,7 @@ def load() -> ctypes.CDLL:
     lib.mi_vs_estimate.restype = I
     lib.mi_vs_estimate_noalloc.argtypes = [P, P, I, I, I, I, P, I, I, I, I, P, P, P]
     lib.mi_vs_estimate_noalloc.restype = I
-    lib.mi_vs_sparse_attn.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, I, P, P, P, S, P]
+    lib.mi_vs_sparse_attn.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, I, I, P, P, P, S, P]
     lib.mi_vs_sparse_attn.restype = I
     lib.mi_block_sparse_attn.argtypes = [P, P, P, I, I, I, I, P, I, I, I, P, I, P, P, P, S, P]
     lib.mi_block_sparse_attn.restype = I
@@ -205,8 +206,11 @@ def mi_vs_estimate_noalloc(q, k, heads=None, last_q: int = 64, k_v: int = 1000, 
 
 
 def mi_vs_sparse_attn(q, k, v, v_idx, s_idx, heads=None, out=None, lse=None, workspace=None,
-                      stream=None):
-    """Vertical-slash sparse attention of the listed heads into ``out`` ([Hq, N, d])."""
+                      stream=None, expanded: bool = False):
+    """Vertical-slash sparse attention of the listed heads into ``out`` ([Hq, N, d]).
+
+    ``expanded`` selects the 64x64 block cover of the diagonals
+    (MI_VS_BLOCK_EXPANDED) instead of exact diagonals."""
     _check_qkv(q, k, v, out)
     _check_idx(v_idx, s_idx)
     Hq, N, d = q.shape
@@ -218,7 +222,8 @@ def mi_vs_sparse_attn(q, k, v, v_idx, s_idx, heads=None, out=None, lse=None, wor
     k_s = s_idx.shape[1] if s_idx is not None else 0
     ws = _workspace(MI_OP_VS_SPARSE_ATTN, n, Hkv, N, k_v, k_s, 0, workspace, q.device)
     rc = load().mi_vs_sparse_attn(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, N, d, harr, n,
-                                  _ptr(v_idx), k_v, _ptr(s_idx), k_s, _ptr(out), _ptr(lse),
+                                  _ptr(v_idx), k_v, _ptr(s_idx), k_s,
+                                  MI_VS_BLOCK_EXPANDED if expanded else 0, _ptr(out), _ptr(lse),
                                   _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "mi_vs_sparse_attn")
     return out

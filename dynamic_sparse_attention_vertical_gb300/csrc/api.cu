@@ -361,11 +361,13 @@ int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, i
 
 int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
                       int N, int d, const int32_t* heads, int n_heads, const int32_t* v_idx,
-                      int k_v, const int32_t* s_idx, int k_s, mi_bf16* out, float* lse,
+                      int k_v, const int32_t* s_idx, int k_s, int flags, mi_bf16* out, float* lse,
                       void* workspace, size_t ws_bytes, mi_stream_t stream) {
   AttnArgs a;
   int rc = attn_preamble(q, k, v, Hq, Hkv, N, d, heads, n_heads, out, &a);
   if (rc) return rc;
+  if (flags & ~MI_VS_BLOCK_EXPANDED) return MI_ERR_UNIMPLEMENTED;
+  const int expanded = (flags & MI_VS_BLOCK_EXPANDED) ? 1 : 0;
   if (k_v < 0 || k_s < 0 || k_v > MI_MAX_KV) return MI_ERR_ARG;
   if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
   const VsLayout L = vs_layout(n_heads, N);
@@ -382,6 +384,7 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
   ia.Nw = L.Nw;
   ia.NT = L.NT;
   ia.NTw = L.NTw;
+  ia.expanded = expanded;
   ia.v_idx = v_idx;
   ia.s_idx = s_idx;
   ia.offbits = reinterpret_cast<uint32_t*>(ws + L.offbits);
@@ -402,6 +405,7 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
   a.dcount = ia.dcount;
   a.v_idx = v_idx;
   a.k_v = k_v;
+  a.expand = expanded;
   a.Nw = L.Nw;
   a.NT = L.NT;
   a.NTw = L.NTw;

@@ -46,7 +46,8 @@ struct AttnArgs {
   uint64_t wait_limit_ns;
   int skip_q_load;  // fault injection (tests): Q is never loaded, waits expire
   // vertical-slash index structures (per listed head)
-  const uint32_t* offbits;  // [n_heads, Nw]   bit o: offset o selected
+  const uint32_t* offbits;  // [n_heads, Nw]   bit o: offset o selected (block-expanded
+                            //                 mode: bit e: 64-block distance e kept)
   const uint32_t* colbits;  // [n_heads, Nw]   bit j: column j selected
   const uint32_t* dbits;    // [n_heads, NTw]  bit t: tile distance t touched by a diagonal
   const uint32_t* dfull;    // [n_heads, NTw]  bit t: a tile at distance t is kept whole
@@ -54,6 +55,7 @@ struct AttnArgs {
   const int* dcount;        // [n_heads]
   const int* v_idx;         // [n_heads, k_v]
   int k_v;
+  int expand;               // block-expanded slash mode
   int Nw, NT, NTw;
   // block-sparse
   const int* blk_idx;  // [n_heads, N/64, topk]
@@ -162,7 +164,18 @@ __device__ __forceinline__ MaskRaw mask_fetch(const AttnSmem& s, const AttnArgs&
     const int d = r - ref.t;
     m.whole = d > 0 && ((s.dfull[d >> 5] >> (d & 31)) & 1u);
   }
-  if (PAT == kPatVS && ref.kind == 0 && !m.whole) {
+  if (PAT == kPatVS && ref.kind == 0 && !m.whole && a.expand) {
+    // the 64-block distances 2d-1 .. 2d+1 of the tile's four sub-blocks
+    const uint32_t* off = a.offbits + (size_t)n * a.Nw;
+    const uint32_t* col = a.colbits + (size_t)n * a.Nw;
+    const int j0 = ref.t * kBN;
+    const int e0 = max(2 * (r - ref.t) - 1, 0);
+    m.base = e0;
+    m.off[0] = ldg_ahead(off + (e0 >> 5));
+    m.off[1] = ldg_ahead(off + min((e0 >> 5) + 1, a.Nw - 1));
+#pragma unroll
+    for (int w = 0; w < 4; ++w) m.col[w] = ldg_ahead(col + (j0 >> 5) + w);
+  } else if (PAT == kPatVS && ref.kind == 0 && !m.whole) {
     const uint32_t* off = a.offbits + (size_t)n * a.Nw;
     const uint32_t* col = a.colbits + (size_t)n * a.Nw;
     const int j0 = ref.t * kBN;
@@ -200,6 +213,30 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
 #pragma unroll
       for (int w = 0; w < 4; ++w) out[w] = 0xFFFFFFFFu;
       return;  // never the diagonal tile (distance > 0)
+    }
+    if (a.expand) {
+      // sub-block (row half rh, key half kh) sits at 64-block distance 2d + rh - kh
+      const int d = r - ref.t;
+      const int rh = (q >> 6) & 1;
+      const uint64_t win = (static_cast<uint64_t>(m.off[1]) << 32) | m.off[0];
+      auto kept = [&](int e) -> bool {
+        return e >= 0 && ((win >> (e - (m.base & ~31))) & 1u);
+      };
+      const uint32_t lo = kept(2 * d + rh) ? 0xFFFFFFFFu : 0u;
+      const uint32_t hi = kept(2 * d + rh - 1) ? 0xFFFFFFFFu : 0u;
+      out[0] = lo | m.col[0];
+      out[1] = lo | m.col[1];
+      out[2] = hi | m.col[2];
+      out[3] = hi | m.col[3];
+      if (j0 == 0) {  // the first 64 keys
+        out[0] = 0xFFFFFFFFu;
+        out[1] = 0xFFFFFFFFu;
+      }
+      if (ref.t == r) {  // causal
+#pragma unroll
+        for (int w = 0; w < 4; ++w) out[w] &= range_bits(j0 + 32 * w, 0, q + 1);
+      }
+      return;
     }
     // offsets q - j0 - c for c = 0..127 are the 128 bits starting at base, reversed
     const int sh = m.base & 31;

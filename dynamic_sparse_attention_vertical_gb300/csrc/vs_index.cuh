@@ -12,6 +12,13 @@
 //   dfull    bit delta (> 0) set when every offset a 128x128 tile at distance
 //            delta can meet, [128*delta - 127, 128*delta + 127] (within
 //            [0, N)), is selected: such a tile is kept whole for every row.
+// Block-expanded mode (every 64x64 block a selected diagonal crosses is kept):
+//   offbits then holds D64, bit e set for the 64-block distances e = o/64 and
+//            (o % 64 != 0) o/64 + 1 of the selected offsets, and e = 0;
+//   dbits    bit delta set when one of the 64-block distances 2 delta - 1,
+//            2 delta, 2 delta + 1 (those of the four 64x64 sub-blocks of a
+//            128x128 tile at distance delta) is in D64;
+//   dfull    bit delta (> 0) set when all three are.
 // All are O(N/32 + k) words per head, the same for every row block.  The
 // entries are validated here: a value out of [0, N) or not strictly above its
 // predecessor raises MI_ERR_INDEX in the status word and is skipped; -1 is
@@ -24,6 +31,7 @@ namespace mi {
 
 struct VsIndexArgs {
   int N, k_v, k_s, Nw, NT, NTw;
+  int expanded;  // block-expanded mode
   const int32_t* v_idx;
   const int32_t* s_idx;
   uint32_t* offbits;
@@ -65,11 +73,18 @@ __global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ V
     if (c < 0) set_status(a.status, MI_ERR_INDEX);
     if (c != 1) continue;
     const int o = si[e];
+    if (a.expanded) {
+      const int b0 = o >> 6;  // 64-block distances the diagonal crosses
+      atomicOr(off + (b0 >> 5), 1u << (b0 & 31));
+      if ((o & 63) && 64 * (b0 + 1) < a.N) atomicOr(off + ((b0 + 1) >> 5), 1u << ((b0 + 1) & 31));
+      continue;
+    }
     atomicOr(off + (o >> 5), 1u << (o & 31));
     const int d0 = o >> 7;
     atomicOr(&db[d0 >> 5], 1u << (d0 & 31));
     if ((o & 127) && d0 + 1 < a.NT) atomicOr(&db[(d0 + 1) >> 5], 1u << ((d0 + 1) & 31));
   }
+  if (a.expanded && tid == 0) atomicOr(off, 1u);  // distance 0: the query's own 64-block
   const int32_t* vi = a.v_idx + (size_t)n * a.k_v;
   for (int e = tid; e < a.k_v; e += 512) {
     const int c = classify_entry(vi, e, a.N);
@@ -80,19 +95,37 @@ __global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ V
   }
   if (tid == 0) atomicOr(&db[0], 1u);
   __syncthreads();
+  if (a.expanded) {
+    // 128-tile distance delta: its sub-blocks sit at 64-block distances
+    // 2 delta - 1 .. 2 delta + 1 (read back through L2: built with atomics)
+    const int NB = (a.N + 63) >> 6;
+    for (int d = tid; d < a.NT; d += 512) {
+      bool any = false;
+      for (int e = 2 * d - 1; e <= 2 * d + 1; ++e)
+        if (e >= 0 && e < NB && ((__ldcg(off + (e >> 5)) >> (e & 31)) & 1u)) any = true;
+      if (any) atomicOr(&db[d >> 5], 1u << (d & 31));
+    }
+    __syncthreads();
+  }
   // tile distances whose whole offset window is selected (read back through L2:
   // the bitmap was just built with atomics)
   __shared__ uint32_t dfw[512];
   dfw[tid] = 0u;
   __syncthreads();
   for (int d = 1 + tid; d < a.NT; d += 512) {
-    const int lo = 128 * d - 127, hi = min(128 * d + 127, a.N - 1);  // inclusive
     bool all = true;
-    for (int w = lo >> 5; w <= (hi >> 5) && all; ++w) {
-      uint32_t need = 0xFFFFFFFFu;
-      if (w == (lo >> 5)) need &= 0xFFFFFFFFu << (lo & 31);
-      if (w == (hi >> 5)) need &= 0xFFFFFFFFu >> (31 - (hi & 31));
-      all = (__ldcg(off + w) & need) == need;
+    if (a.expanded) {
+      const int NB = (a.N + 63) >> 6;
+      for (int e = 2 * d - 1; e <= 2 * d + 1 && all; ++e)
+        all = e < NB && ((__ldcg(off + (e >> 5)) >> (e & 31)) & 1u);
+    } else {
+      const int lo = 128 * d - 127, hi = min(128 * d + 127, a.N - 1);  // inclusive
+      for (int w = lo >> 5; w <= (hi >> 5) && all; ++w) {
+        uint32_t need = 0xFFFFFFFFu;
+        if (w == (lo >> 5)) need &= 0xFFFFFFFFu << (lo & 31);
+        if (w == (hi >> 5)) need &= 0xFFFFFFFFu >> (31 - (hi & 31));
+        all = (__ldcg(off + w) & need) == need;
+      }
     }
     if (all) atomicOr(&dfw[d >> 5], 1u << (d & 31));
   }

@@ -62,6 +62,46 @@ def vs_kept_per_row(N: int, v_idx, s_idx, blk: int = 64, device="cpu") -> torch.
     return (ab.double() + c_out + d_out - mid).round().long()
 
 
+def _expanded_dist(N: int, s_idx, blk: int = 64) -> torch.Tensor:
+    """Block distances a block-expanded head keeps (bool over 0 .. N//blk)."""
+    nb = (N + blk - 1) // blk
+    dist = torch.zeros(nb + 2, dtype=torch.bool)
+    s = torch.as_tensor(s_idx).long()
+    s = s[(s >= 0) & (s < N)]
+    dist[s // blk] = True
+    dist[(s // blk + 1)[(s % blk) > 0]] = True
+    dist[0] = True
+    return dist[:nb]
+
+
+def vs_expanded_kept_per_row(N: int, v_idx, s_idx, blk: int = 64) -> torch.Tensor:
+    """Kept keys of every row of a block-expanded vertical-slash head (int64 [N]).
+
+    Row q in block R keeps its own block up to q, the blocks at distances in D
+    (1 <= delta <= R, blk keys each), the first block when R is not in D, and the
+    selected columns of blocks 1 .. R-1 whose distance is not in D.
+    """
+    nb = (N + blk - 1) // blk
+    dist = _expanded_dist(N, s_idx, blk)
+    d1 = dist.clone()
+    d1[0] = False
+    pd = _prefix(d1.double())                         # |D n [1, x)|
+    R = torch.arange(nb)
+    blocks = blk * pd[R + 1]                          # distances 1..R
+    first = torch.where((R >= 1) & ~dist[R], torch.full_like(R, blk), torch.zeros_like(R)).double()
+    v = torch.as_tensor(v_idx).long()
+    v = v[(v >= blk) & (v < N)]
+    cols = torch.bincount(v // blk, minlength=nb).double()
+    notd = (~dist).double()
+    notd[0] = 0.0
+    L = 1 << (2 * nb).bit_length()
+    resid = torch.fft.irfft(torch.fft.rfft(cols, L) * torch.fft.rfft(notd, L), L)[:nb].round()
+    per_block = blocks + first + resid
+    q = torch.arange(N)
+    own = q - (q // blk) * blk + 1
+    return (own.double() + per_block[q // blk]).round().long()
+
+
 def block_kept_per_row(N: int, sel_rows, blk: int = 64) -> torch.Tensor:
     """Kept keys per row of a block-sparse head; sel_rows[r] = selected blocks of query block r."""
     out = torch.zeros(N, dtype=torch.int64)
@@ -88,16 +128,24 @@ def dense_kept_per_row(N: int) -> torch.Tensor:
 
 # ------------------------------------------------------ executed tiles ----
 
-def vs_tiles(N: int, v_idx, s_idx) -> int:
+def vs_tiles(N: int, v_idx, s_idx, expanded: bool = False) -> int:
     """128x128 tiles the vertical-slash kernel issues for one head (all row blocks)."""
     NT = (N + 127) // 128
-    d = torch.zeros(NT + 1, dtype=torch.bool)
-    s = torch.as_tensor(s_idx).long()
-    s = s[(s >= 0) & (s < N)]
-    d[(s >> 7)] = True
-    d[torch.clamp((s >> 7) + 1, max=NT)[(s & 127) > 0]] = True
-    d[0] = True
-    d = d[:NT]
+    if expanded:
+        # tile distance d holds the 64-blocks at block distances 2d-1 .. 2d+1
+        e = _expanded_dist(N, s_idx, 64)
+        ep = torch.zeros(2 * NT + 2, dtype=torch.bool)
+        ep[1:1 + e.numel()] = e                       # ep[x + 1] = e[x]
+        dd = torch.arange(NT)
+        d = ep[2 * dd] | ep[2 * dd + 1] | ep[2 * dd + 2]
+    else:
+        d = torch.zeros(NT + 1, dtype=torch.bool)
+        s = torch.as_tensor(s_idx).long()
+        s = s[(s >= 0) & (s < N)]
+        d[(s >> 7)] = True
+        d[torch.clamp((s >> 7) + 1, max=NT)[(s & 127) > 0]] = True
+        d[0] = True
+        d = d[:NT]
     dcum = torch.cumsum(d.long(), 0)                      # distances <= r
     r = torch.arange(NT)
     has_t0 = ~d[r]                                        # tile 0 added unless distance r is set

@@ -115,17 +115,26 @@ int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, i
  * Slides: "Vertical-Slash" pattern and "Dynamic Sparse Attention Calculation
  * with PIT, FlashAttention"; README mirror: vertical_slash_sparse_attention.
  *
- * Row q of head h keeps key j iff j <= q and (j < 64 or j/64 == q/64 or
- * j in v_idx[n] or q - j in s_idx[n]); a key kept by several rules counts
- * once.  out[h, q] = softmax over kept keys of q.k/sqrt(d), times V.
+ * flags = 0 (exact diagonals): row q of head h keeps key j iff j <= q and
+ * (j < 64 or j/64 == q/64 or j in v_idx[n] or q - j in s_idx[n]); a key kept
+ * by several rules counts once.
+ * flags = MI_VS_BLOCK_EXPANDED (the 64x64 block cover of the diagonals used by
+ * the pages' block kernels): with D = {0} and, for each o in s_idx[n], o/64 and
+ * (if o % 64 != 0) o/64 + 1 -- the 64-block distances a diagonal o crosses --
+ * row q keeps key j iff j <= q and (j < 64 or j in v_idx[n] or
+ * q/64 - j/64 in D): every 64x64 block a selected diagonal passes through is
+ * kept whole.
+ * out[h, q] = softmax over kept keys of q.k/sqrt(d), times V.
  * v_idx: [n_heads, k_v] and s_idx: [n_heads, k_s] int32 DEVICE arrays, each row
  * strictly ascending, values in [0, N); a trailing run of -1 is allowed and
  * ignored (the layout mi_vs_estimate writes).  An entry out of range or out of
  * order sets MI_ERR_INDEX in the status word and is skipped.  k_v <= MI_MAX_KV.
+ * Unknown flag bits: MI_ERR_UNIMPLEMENTED.
  */
+#define MI_VS_BLOCK_EXPANDED 1
 int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
                       int N, int d, const int32_t* heads, int n_heads, const int32_t* v_idx,
-                      int k_v, const int32_t* s_idx, int k_s, mi_bf16* out, float* lse,
+                      int k_v, const int32_t* s_idx, int k_s, int flags, mi_bf16* out, float* lse,
                       void* workspace, size_t ws_bytes, mi_stream_t stream);
 
 /*

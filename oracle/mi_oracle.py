@@ -44,6 +44,7 @@ __all__ = [
     "topk_sorted",
     "vs_estimate",
     "vs_mask_rows",
+    "vs_expanded_mask_rows",
     "block_pool",
     "block_scores",
     "block_sparse_select",
@@ -146,6 +147,32 @@ def vs_mask_rows(N: int, rows, v_idx, s_idx, blk: int = BLK) -> np.ndarray:
     off = r - j
     slash = np.where(off >= 0, sl[np.clip(off, 0, N - 1)], False)
     keep = (j < blk) | ((j // blk) == (r // blk)) | col[None, :] | slash
+    return (j <= r) & keep
+
+
+def vs_expanded_mask_rows(N: int, rows, v_idx, s_idx, blk: int = BLK) -> np.ndarray:
+    """Block-expanded vertical-slash mask: every blk x blk block a selected diagonal crosses.
+
+    The block kernels the MInference pages build on (PIT and the block-sparse
+    FlashAttention of the talk slides, "Dynamic Sparse Attention Calculation
+    with PIT, FlashAttention") cover the diagonals with whole blocks.  A diagonal
+    o = blk*a + b crosses the blocks at block distance a and, when b > 0, a + 1;
+    distance 0 (the query's own block) is always kept.
+    M[q, j] = j <= q and (j < blk or j in V or q//blk - j//blk in D).
+    """
+    r = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.arange(N, dtype=np.int64)[None, :]
+    col = np.zeros(N, dtype=bool)
+    col[np.asarray(v_idx, dtype=np.int64)] = True
+    dist = np.zeros(N // blk + 2, dtype=bool)
+    dist[0] = True
+    for o in np.asarray(s_idx, dtype=np.int64):
+        dist[o // blk] = True
+        if o % blk:
+            dist[o // blk + 1] = True
+    bd = r // blk - j // blk
+    crossed = np.where(bd >= 0, dist[np.clip(bd, 0, dist.size - 1)], False)
+    keep = (j < blk) | col[None, :] | crossed
     return (j <= r) & keep
 
 

@@ -54,3 +54,35 @@ def test_dense_and_ashape_tiles():
     # n_init=128, window=128, 16 row blocks: block 0 one tile, block 1 two,
     # blocks 2..15 the sink tile plus two window tiles
     assert F.ashape_tiles(2048, 128, 128) == 1 + 2 + 14 * 3
+
+
+@pytest.mark.parametrize("N,kv,ks,seed", [(700, 30, 4, 0), (1024, 200, 5, 1), (2048, 64, 40, 2), (64, 3, 3, 3),
+                                          (4096, 100, 0, 4)])
+def test_vs_expanded_kept_counts_match_oracle_mask(N, kv, ks, seed):
+    rng = np.random.default_rng(seed)
+    v = np.sort(rng.choice(N, size=min(kv, N), replace=False))
+    s = np.sort(rng.choice(N, size=min(ks, N), replace=False)) if ks else np.zeros(0, dtype=np.int64)
+    ref = O.vs_expanded_mask_rows(N, np.arange(N), v, s).sum(axis=1)
+    np.testing.assert_array_equal(F.vs_expanded_kept_per_row(N, v, s).numpy(), ref)
+
+
+def _vs_expanded_tiles_brute(N, v, s):
+    """Enumerate: a 128x128 tile (r, t) is issued when one of its four 64x64 blocks is in the
+    block-expanded mask's block set, or t = 0, or it holds a residual column."""
+    NT = (N + 127) // 128
+    D = {0} | {o // 64 for o in s} | {o // 64 + 1 for o in s if o % 64}
+    total = 0
+    for r in range(NT):
+        contig = {0} | {t for t in range(r + 1)
+                        if any((2 * r + rh) - (2 * t + kh) in D for rh in (0, 1) for kh in (0, 1))}
+        resid = [j for j in v if 1 <= (j >> 7) < r and (j >> 7) not in contig]
+        total += len(contig) + math.ceil(len(resid) / 128)
+    return total
+
+
+@pytest.mark.parametrize("N,kv,ks,seed", [(4096, 300, 7, 0), (8192, 1000, 40, 1), (2112, 50, 0, 2)])
+def test_vs_expanded_tile_count_matches_enumeration(N, kv, ks, seed):
+    rng = np.random.default_rng(seed)
+    v = np.sort(rng.choice(N, size=kv, replace=False))
+    s = np.sort(rng.choice(N, size=ks, replace=False)) if ks else np.zeros(0, dtype=np.int64)
+    assert F.vs_tiles(N, v, s, expanded=True) == _vs_expanded_tiles_brute(N, v.tolist(), s.tolist())

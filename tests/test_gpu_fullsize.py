@@ -166,3 +166,24 @@ def test_sweep_points_sampled(N, k_v, k_s):
     dref, _ = O.attention_rows(x.q[h], x.k[g], x.v[g], rows, lambda r: O.causal_mask_rows(N, r), chunk=32)
     assert_close(dense[h][ridx].float().cpu().numpy(), dref, f"sweep dense N={N}")
     _free(x, v_idx, s_idx, out, dense)
+
+
+def test_vs_block_expanded_32k_sampled():
+    """Block-expanded mode on a full 32K layer (32 q / 8 KV heads, estimated indices):
+    sampled rows of three heads against the oracle's block-expanded mask."""
+    N = 32768
+    x = I.literal_inputs(32, 8, N, n_cols=16, n_offsets=8, seed=2, device=DEV)
+    v_idx, s_idx = B.mi_vs_estimate(x.q, x.k, k_v=1000, k_s=6096)
+    out = B.mi_vs_sparse_attn(x.q, x.k, x.v, v_idx, s_idx, expanded=True)
+    torch.cuda.synchronize()
+    vi_all, si_all = v_idx.cpu().numpy(), s_idx.cpu().numpy()
+    rng = np.random.default_rng(9)
+    for h in (0, 13, 31):
+        g = O.kv_head(h, 32, 8)
+        vi, si = vi_all[h][vi_all[h] >= 0], si_all[h][si_all[h] >= 0]
+        rows = sample_rows(N, rng, n_random=32, blocks=2)
+        ref, _ = O.attention_rows(x.q[h], x.k[g], x.v[g], rows,
+                                  lambda r: O.vs_expanded_mask_rows(N, r, vi, si), chunk=32)
+        assert_close(out[h][torch.as_tensor(rows, device=DEV)].float().cpu().numpy(), ref,
+                     f"expanded head {h}")
+    _free(x, v_idx, s_idx, out)

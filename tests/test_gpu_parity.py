@@ -136,6 +136,76 @@ def test_vs_attention_gathered_columns():
     _vs_check(x, range(Hq), vis, sis, out)
 
 
+def _vs_expanded_check(x, heads, v_idx, s_idx, out, rows=None):
+    Hq, N = x.q.shape[0], x.q.shape[1]
+    Hkv = x.k.shape[0]
+    o = out.float().cpu().numpy()
+    rows = np.arange(N) if rows is None else rows
+    for n, h in enumerate(heads):
+        g = O.kv_head(h, Hq, Hkv)
+        vi = np.asarray(v_idx[n])
+        vi = vi[vi >= 0]
+        si = np.asarray(s_idx[n])
+        si = si[si >= 0]
+        ref, _ = O.attention_rows(x.q[h], x.k[g], x.v[g], rows,
+                                  lambda r: O.vs_expanded_mask_rows(N, r, vi, si))
+        assert_close(o[h][rows], ref, f"vs expanded h{h}")
+
+
+@pytest.mark.parametrize("N,seed", [(1024, 21), (2112, 22), (4096, 23)])
+def test_vs_block_expanded_matches_oracle(N, seed):
+    """Block-expanded diagonals: sparse offsets (partial tiles, the 64x64 sub-block
+    mask), runs of offsets (tiles kept whole), offset 0 and the last offset,
+    columns inside and outside the covered tiles (gathered tiles)."""
+    Hq, Hkv = 3, 1
+    x = _rand_inputs(Hq, Hkv, N, seed=seed)
+    rng = np.random.default_rng(seed)
+    sis = [np.array(sorted({0, 70, 300, N // 2 + 5, N - 1})),
+           np.arange(200, 520),                                    # a run: whole tiles
+           np.sort(rng.choice(np.arange(N), size=40, replace=False))]
+    vis = [np.sort(rng.choice(np.arange(N), size=k, replace=False)) for k in (10, 200, 130)]
+    k_s = max(len(si) for si in sis)
+    k_v = max(len(vi) for vi in vis)
+    s_idx = torch.full((Hq, k_s), -1, dtype=torch.int32)
+    v_idx = torch.full((Hq, k_v), -1, dtype=torch.int32)
+    for h in range(Hq):
+        s_idx[h, : len(sis[h])] = torch.tensor(sis[h])
+        v_idx[h, : len(vis[h])] = torch.tensor(vis[h])
+    q, k, v = _dev(x)
+    out = B.mi_vs_sparse_attn(q, k, v, v_idx.to(DEV), s_idx.to(DEV), expanded=True)
+    _vs_expanded_check(x, range(Hq), vis, sis, out)
+
+
+def test_vs_block_expanded_estimated_indices_and_exact_differ():
+    """With estimated indices the expanded mode keeps a superset of the exact mask:
+    both match their own oracle mask, and on these inputs they differ."""
+    N, Hq, Hkv = 2048, 2, 1
+    x = I.literal_inputs(Hq, Hkv, N, n_cols=8, n_offsets=4, seed=31)
+    q, k, v = _dev(x)
+    v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=64, k_s=32)
+    exp = B.mi_vs_sparse_attn(q, k, v, v_idx, s_idx, expanded=True)
+    ex = B.mi_vs_sparse_attn(q, k, v, v_idx, s_idx)
+    vi, si = v_idx.cpu().numpy(), s_idx.cpu().numpy()
+    _vs_expanded_check(x, range(Hq), vi, si, exp)
+    _vs_check(x, range(Hq), vi, si, ex)
+    assert (exp.float() - ex.float()).abs().max().item() > 1e-3
+
+
+def test_vs_unknown_flag_is_refused():
+    N, Hq, Hkv = 256, 1, 1
+    x = _rand_inputs(Hq, Hkv, N, seed=4)
+    q, k, v = _dev(x)
+    v_idx = torch.tensor([[3]], dtype=torch.int32, device=DEV)
+    s_idx = torch.tensor([[5]], dtype=torch.int32, device=DEV)
+    out = torch.zeros_like(q)
+    ws = torch.empty(B.mi_workspace_bytes(B.MI_OP_VS_SPARSE_ATTN, 1, Hkv, N), dtype=torch.uint8, device=DEV)
+    lib = B.load()
+    rc = lib.mi_vs_sparse_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), Hq, Hkv, N, 128, None, 1,
+                               v_idx.data_ptr(), 1, s_idx.data_ptr(), 1, 2, out.data_ptr(), None,
+                               ws.data_ptr(), ws.numel(), None)
+    assert rc == B.MI_ERR_UNIMPLEMENTED
+
+
 def test_vs_full_budget_is_dense():
     N, Hq, Hkv = 384, 1, 1
     x = _rand_inputs(Hq, Hkv, N, seed=2)

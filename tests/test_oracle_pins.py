@@ -29,6 +29,37 @@ def test_vs_mask_hand_worked(name):
     np.testing.assert_array_equal(got, fx["mask"])
 
 
+def test_vs_expanded_mask_hand_worked():
+    fx = read_fixture("vs_expanded_mask_n8_blk2.txt")
+    N, blk = int(fx["N"][0]), int(fx["blk"][0])
+    got = O.vs_expanded_mask_rows(N, np.arange(N), _ints(fx["V"]), _ints(fx["S"]), blk=blk)
+    np.testing.assert_array_equal(got, fx["mask"])
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_vs_expanded_mask_equals_blocks_crossed_by_each_diagonal(seed):
+    """Brute force: walk every element (q, q - o) of each selected diagonal and keep
+    the whole block pair it lies in; the block-distance rule must give the same mask."""
+    rng = np.random.default_rng(seed)
+    N, blk = 96, 8
+    s = np.sort(rng.choice(N, size=7, replace=False))
+    v = np.sort(rng.choice(N, size=5, replace=False))
+    pairs = set()
+    for o in s:
+        for q in range(o, N):
+            pairs.add((q // blk, (q - o) // blk))
+    want = np.zeros((N, N), dtype=bool)
+    for q in range(N):
+        for j in range(q + 1):
+            want[q, j] = (j < blk or j in set(v.tolist()) or q // blk == j // blk
+                          or (q // blk, j // blk) in pairs)
+    got = O.vs_expanded_mask_rows(N, np.arange(N), v, s, blk=blk)
+    np.testing.assert_array_equal(got, want)
+    # the block cover contains the exact diagonals
+    exact = O.vs_mask_rows(N, np.arange(N), v, s, blk=blk)
+    assert not np.any(exact & ~got)
+
+
 def test_block_mask_hand_worked():
     fx = read_fixture("block_mask_n8_blk2.txt")
     N, blk = int(fx["N"][0]), int(fx["blk"][0])

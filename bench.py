@@ -225,6 +225,11 @@ class Layer:
         return ({k2: 4 * F.D * v2 for k2, v2 in alg.items()}, {k2: F.TILE_FLOPS * v2 for k2, v2 in tiles.items()})
 
 
+# DRAM bytes (read + write) of one vertical-slash attention launch, from a one-pass ncu capture of
+# this kernel version (profiles/attn_vs_mixed-128k_dram.md); None where no capture was taken.
+TRAFFIC_BYTES = {("mixed-128k", "literal"): 2.39e9 + 0.804e9}
+
+
 def make_inputs(w, variant, device):
     from dynamic_sparse_attention_vertical_gb300 import inputs as I
     kw = dict(n_cols=w["n_cols"], n_offsets=w["n_offsets"], seed=w["seed"], device=device)
@@ -509,7 +514,8 @@ def main():
         "stages": head["stages"],
         "roofline": {"bound": "tensor", "kernel": "vertical-slash sparse attention (tcgen05)",
                      "achieved": ach, "peak": sustained, "unit": "TFLOP/s",
-                     "frac": (ach / sustained) if ach else None, "traffic": None,
+                     "frac": (ach / sustained) if ach else None,
+                     "traffic": TRAFFIC_BYTES.get((args.workload, variants[0])),
                      "flops": "algorithmic: 4*d per kept (q, j) pair; time = the mi_vs_sparse_attn call",
                      "peak_source": f"bf16_tflops_sustained ({peak_src})",
                      "executed_tflops": head["vs_attention_exec_tflops"],

@@ -33,6 +33,12 @@ Three families of inputs:
     dimensions, so that attention to nearby keys is slightly favoured and the
     highest-scoring diagonals cluster at small offsets, the locality that real
     heads show.
+
+``pattern heads`` (for the offline pattern search)
+    Three heads, one KV head each, each shaped like one of the slides' three
+    patterns: head 0 attends to a sink (the first keys) and a local window,
+    head 1 to scattered planted columns and diagonals, head 2 to whole 64x64
+    blocks chosen by a per-block topic.
 """
 from __future__ import annotations
 
@@ -48,6 +54,7 @@ __all__ = [
     "literal_inputs",
     "margin_inputs",
     "local_inputs",
+    "pattern_head_inputs",
     "uniform_choice",
 ]
 
@@ -232,3 +239,87 @@ def local_inputs(
     q[:, :, d - 2:] = rot.to(torch.bfloat16)
     k[:, :, d - 2:] = rot.to(torch.bfloat16)
     return Inputs(q, k, base.v, base.planted_cols, base.planted_offsets, seed, "local")
+
+
+def _logit_scale(nats: float, d: int) -> float:
+    """Size a of two unit-direction entries whose product a*a is ``nats`` after the 1/sqrt(d) scale."""
+    return math.sqrt(nats * math.sqrt(d))
+
+
+def pattern_head_inputs(
+    N: int,
+    d: int = 128,
+    seed: int = 1,
+    device: str = "cpu",
+    sink: int = 128,
+    window: int = 1024,
+    n_cols: int = 24,
+    offsets=(700, 1900),
+    n_topics: int = 12,
+    nats: float = 10.0,
+) -> Inputs:
+    """Three single-KV-head heads shaped like the three patterns (see the module doc).
+
+    Every head starts from Q, K, V ~ N(0, 1/d).  Head 0: keys j < ``sink`` carry a
+    sink direction every query shares (+``nats``), and 16 rotary pairs with
+    frequencies spread over (0, pi / ``window``] add sum_f cos(f (i - j)) * nats/16:
+    ``nats`` at distance 0, positive up to about ``window`` tokens, small and not
+    recurring beyond.  Head 1: ``n_cols`` key columns drawn from [64, N) each get their
+    own basis direction (dims 0 ..), which every query carries (+``nats``), and
+    for each offset o in ``offsets`` every row i >= o and key i - o share a fresh
+    random unit direction in the upper half of the dims (+``nats``).  Head 2:
+    every 64-row block of queries and every 64-key block gets one of
+    ``n_topics`` random unit directions, and a query block attends (+``nats``)
+    to the key blocks of its own topic.  The planted columns and offsets of
+    head 1 are recorded in slot 1; the other slots record none.
+    """
+    if n_cols > d // 2:
+        raise ValueError("n_cols must fit in the lower half of the head dimension")
+    gen = _gen(device, seed)
+    sd = 1.0 / math.sqrt(d)
+    q = torch.empty((3, N, d), dtype=torch.bfloat16, device=device)
+    k = torch.empty((3, N, d), dtype=torch.bfloat16, device=device)
+    v = torch.empty((3, N, d), dtype=torch.bfloat16, device=device)
+    a = _logit_scale(nats, d)
+    # head 0: sink + local window
+    qf = _randn((N, d), gen, device, sd)
+    kf = _randn((N, d), gen, device, sd)
+    qf[:, d - 34] = a
+    kf[:sink, d - 34] += a
+    pos = torch.arange(N, device=device, dtype=torch.float64)
+    for f in range(16):
+        ang = pos * (math.pi / window) * (f + 1) / 16.0
+        rot = torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).to(torch.float32) * (a / 4.0)
+        qf[:, d - 32 + 2 * f: d - 30 + 2 * f] = rot
+        kf[:, d - 32 + 2 * f: d - 30 + 2 * f] = rot
+    q[0], k[0] = qf.to(torch.bfloat16), kf.to(torch.bfloat16)
+    v[0] = _randn((N, d), gen, device, sd).to(torch.bfloat16)
+    # head 1: vertical columns + long-range diagonals
+    qf = _randn((N, d), gen, device, sd)
+    kf = _randn((N, d), gen, device, sd)
+    cols = uniform_choice(n_cols, 64, N, gen)
+    for i, c in enumerate(cols.tolist()):
+        qf[:, i] += a
+        kf[c, i] += a
+    half = d // 2
+    offs = torch.tensor(sorted(o for o in offsets if o < N), dtype=torch.int64)
+    for o in offs.tolist():
+        f = _randn((N - o, half), gen, device, 1.0)
+        f = f / f.norm(dim=1, keepdim=True) * a
+        qf[o:, half:] += f
+        kf[: N - o, half:] += f
+    q[1], k[1] = qf.to(torch.bfloat16), kf.to(torch.bfloat16)
+    v[1] = _randn((N, d), gen, device, sd).to(torch.bfloat16)
+    # head 2: block topics
+    nb = (N + 63) // 64
+    dirs = _randn((n_topics, d), gen, device, 1.0)
+    dirs = dirs / dirs.norm(dim=1, keepdim=True)
+    tq = torch.randint(0, n_topics, (nb,), generator=gen, device=device)
+    tk = torch.randint(0, n_topics, (nb,), generator=gen, device=device)
+    rows = torch.arange(N, device=device) // 64
+    qf = _randn((N, d), gen, device, sd) + a * dirs[tq[rows]]
+    kf = _randn((N, d), gen, device, sd) + a * dirs[tk[rows]]
+    q[2], k[2] = qf.to(torch.bfloat16), kf.to(torch.bfloat16)
+    v[2] = _randn((N, d), gen, device, sd).to(torch.bfloat16)
+    empty = torch.empty(0, dtype=torch.int64)
+    return Inputs(q, k, v, [empty, cols, empty], [empty, offs, empty], seed, "pattern_heads")

@@ -191,6 +191,27 @@ class Layer:
     def dense(self):
         self.B.mi_dense_causal_attn(self.q, self.k, self.v, out=self.out, workspace=self.ws_dense)
 
+    def layer_cfg(self):
+        """The same layer as one mi_layer_attn configuration (one entry per q-head)."""
+        B, w = self.B, self.w
+        cfg = [B.HeadCfg.skip() for _ in range(w["Hq"])]
+        for h in self.vs:
+            cfg[h] = B.HeadCfg.vs(w["k_v"], w["k_s"], expanded=self.expanded)
+        for h in self.blk:
+            cfg[h] = B.HeadCfg.block(w["topk"])
+        for h in self.ash:
+            cfg[h] = B.HeadCfg.ashape(w["n_init"], w["window"])
+        return cfg
+
+    def step_layer(self, ev=None):
+        """One layer through the single layer call (estimation, selection, one attention launch)."""
+        if not hasattr(self, "_cfg"):
+            self._cfg = self.layer_cfg()
+            self._ws_layer = torch.empty(self.B.mi_layer_workspace_bytes(self.w["Hq"], self.w["Hkv"], self.w["N"],
+                                                                         self._cfg),
+                                         dtype=torch.uint8, device=self.q.device)
+        self.B.mi_layer_attn(self.q, self.k, self.v, self._cfg, out=self.out, workspace=self._ws_layer)
+
     def check_status(self):
         used = ([self.ws_est, self.ws_vs] if self.vs else []) + ([self.ws_blk] if self.blk else []) \
             + ([self.ws_ash] if self.ash else [])
@@ -364,6 +385,8 @@ def main():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-layer-call", action="store_true",
+                    help="skip the extra timing of the single layer call")
     ap.add_argument("--no-expanded", action="store_true",
                     help="skip the extra timing of the block-expanded slash mode")
     ap.add_argument("--sweep", action="store_true", help="time the N x k_v x k_s sweep instead")
@@ -436,6 +459,16 @@ def main():
                "alg_tflop_per_layer": sum(alg.values()) / 1e12, "exec_tflop_per_layer": sum(exe.values()) / 1e12,
                "vs_attention_alg_tflops": alg["vs"] / (st["vs_attention_ms"] * 1e-3) / 1e12 if alg["vs"] else None,
                "vs_attention_exec_tflops": exe["vs"] / (st["vs_attention_ms"] * 1e-3) / 1e12 if exe["vs"] else None}
+        if not args.no_layer_call:
+            # the same layer through mi_layer_attn (one attention launch for every pattern)
+            L.step_layer()
+            torch.cuda.synchronize()
+            if L.B.mi_read_status(L._ws_layer) != 0:
+                raise RuntimeError("layer call status " + L.B.mi_strerror(L.B.mi_read_status(L._ws_layer)))
+            barrier()
+            lms, _ = timed(L.step_layer, args.steps)
+            barrier()
+            res["layer_call_ms"] = max_over_ranks(lms) / world
         if L.vs and not args.no_expanded:
             # the same layer with the vertical-slash heads in the block-expanded slash mode
             L.expanded = True

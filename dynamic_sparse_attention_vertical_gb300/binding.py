@@ -44,12 +44,47 @@ SYMBOLS = (
     "mi_block_sparse_attn",
     "mi_ashape_attn",
     "mi_dense_causal_attn",
+    "mi_layer_workspace_bytes",
+    "mi_layer_attn",
     "mi_read_status",
     "mi_strerror",
     "mi_debug_inject",
 )
 MI_FAULT_NONE = 0
 MI_FAULT_SKIP_Q_LOAD = 1
+
+MI_PAT_SKIP = -1
+MI_PAT_DENSE = 0
+MI_PAT_VS = 1
+MI_PAT_BLOCK = 2
+MI_PAT_ASHAPE = 3
+
+
+class HeadCfg(ctypes.Structure):
+    """One q-head of a layer call (mi_head_cfg in include/mi.h)."""
+    _fields_ = [("pattern", ctypes.c_int32), ("k_v", ctypes.c_int32), ("k_s", ctypes.c_int32),
+                ("vs_flags", ctypes.c_int32), ("topk", ctypes.c_int32), ("n_init", ctypes.c_int32),
+                ("window", ctypes.c_int32)]
+
+    @staticmethod
+    def vs(k_v: int = 1000, k_s: int = 6096, expanded: bool = False) -> "HeadCfg":
+        return HeadCfg(MI_PAT_VS, k_v, k_s, MI_VS_BLOCK_EXPANDED if expanded else 0, 0, 0, 0)
+
+    @staticmethod
+    def block(topk: int = 100) -> "HeadCfg":
+        return HeadCfg(MI_PAT_BLOCK, 0, 0, 0, topk, 0, 0)
+
+    @staticmethod
+    def ashape(n_init: int = 128, window: int = 4096) -> "HeadCfg":
+        return HeadCfg(MI_PAT_ASHAPE, 0, 0, 0, 0, n_init, window)
+
+    @staticmethod
+    def dense() -> "HeadCfg":
+        return HeadCfg(MI_PAT_DENSE, 0, 0, 0, 0, 0, 0)
+
+    @staticmethod
+    def skip() -> "HeadCfg":
+        return HeadCfg(MI_PAT_SKIP, 0, 0, 0, 0, 0, 0)
 
 
 class MIError(RuntimeError):
@@ -86,6 +121,10 @@ def load() -> ctypes.CDLL:
     lib.mi_ashape_attn.restype = I
     lib.mi_dense_causal_attn.argtypes = [P, P, P, I, I, I, I, P, I, P, P, P, S, P]
     lib.mi_dense_causal_attn.restype = I
+    lib.mi_layer_workspace_bytes.argtypes = [I, I, I, P]
+    lib.mi_layer_workspace_bytes.restype = S
+    lib.mi_layer_attn.argtypes = [P, P, P, I, I, I, I, P, P, P, P, S, P]
+    lib.mi_layer_attn.restype = I
     lib.mi_read_status.argtypes = [P, P]
     lib.mi_read_status.restype = I
     lib.mi_debug_inject.argtypes = [I, ctypes.c_uint64]
@@ -277,4 +316,38 @@ def mi_dense_causal_attn(q, k, v, heads=None, out=None, lse=None, workspace=None
     rc = load().mi_dense_causal_attn(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, N, d, harr, n,
                                      _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "mi_dense_causal_attn")
+    return out
+
+
+def _cfg_array(cfg, Hq: int):
+    if len(cfg) != Hq:
+        raise ValueError(f"one configuration per q-head: got {len(cfg)} for {Hq} heads")
+    arr = (HeadCfg * Hq)()
+    for i, c in enumerate(cfg):
+        arr[i] = c
+    return arr
+
+
+def mi_layer_workspace_bytes(Hq: int, Hkv: int, N: int, cfg) -> int:
+    arr = _cfg_array(cfg, Hq)
+    return int(load().mi_layer_workspace_bytes(Hq, Hkv, N, ctypes.cast(arr, ctypes.c_void_p)))
+
+
+def mi_layer_attn(q, k, v, cfg, out=None, lse=None, workspace=None, stream=None):
+    """A whole layer in one call: ``cfg[h]`` (a ``HeadCfg``) gives q-head h its pattern and budgets."""
+    _check_qkv(q, k, v, out)
+    Hq, N, d = q.shape
+    Hkv = k.shape[0]
+    arr = _cfg_array(cfg, Hq)
+    if out is None:
+        out = torch.zeros_like(q)
+    need = int(load().mi_layer_workspace_bytes(Hq, Hkv, N, ctypes.cast(arr, ctypes.c_void_p)))
+    if need == 0:
+        raise MIError(MI_ERR_ARG, "mi_layer_workspace_bytes")
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    if ws.numel() < need:
+        raise ValueError(f"workspace too small: {ws.numel()} < {need} bytes")
+    rc = load().mi_layer_attn(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, N, d, ctypes.cast(arr, ctypes.c_void_p),
+                              _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "mi_layer_attn")
     return out

@@ -261,45 +261,16 @@ int attn_preamble(const void* q, const void* k, const void* v, int Hq, int Hkv, 
   return MI_OK;
 }
 
-}  // namespace
-
-// ====================================================================== ABI ==
-
-extern "C" {
-
-size_t mi_workspace_bytes(int op, int n_heads, int Hkv, int N, int k_v, int k_s, int topk) {
-  (void)k_v;
-  (void)k_s;
-  (void)topk;
-  if (n_heads <= 0 || N <= 0) return 0;
-  switch (op) {
-    case MI_OP_VS_ESTIMATE: return est_layout(n_heads, N).total;
-    case MI_OP_VS_SPARSE_ATTN: return vs_layout(n_heads, N).total;
-    case MI_OP_BLOCK_SPARSE_ATTN: return Hkv > 0 ? block_layout(n_heads, Hkv, N).total : 0;
-    case MI_OP_ASHAPE_ATTN:
-    case MI_OP_DENSE_CAUSAL_ATTN: return 256;
-    default: return 0;
-  }
-}
-
-int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
-                   const int32_t* heads, int n_heads, int last_q, int k_v, int k_s,
-                   int32_t* v_idx, int32_t* s_idx, void* workspace, size_t ws_bytes,
-                   mi_stream_t stream) {
-  int rc = check_device();
-  if (rc) return rc;
+// Estimation of the listed heads (E1, E2, T1) into rows of ld_v / ld_s entries of
+// v_idx / s_idx; ws is an est_layout(heads.n, N) workspace.
+int est_run(const void* q, const void* k, int Hq, int Hkv, int N, const HeadList& heads, int k_v,
+            int k_s, int32_t* v_idx, int ld_v, int32_t* s_idx, int ld_s, char* ws, int* status,
+            cudaStream_t st) {
   EstArgs a;
   memset(&a, 0, sizeof(a));
-  if ((rc = check_common(q, k, Hq, Hkv, N, d, heads, n_heads, &a.heads))) return rc;
-  if (last_q != kLastQ) return MI_ERR_SHAPE;
-  if (k_v < 0 || k_s < 0) return MI_ERR_ARG;
-  if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
+  a.heads = heads;
+  const int n_heads = heads.n;
   const EstLayout L = est_layout(n_heads, N);
-  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(workspace);
-  int* status = reinterpret_cast<int*>(ws + L.status);
-
   // pair up listed heads that share a KV head (two heads fill one 128-row UMMA)
   const int group = Hq / Hkv;
   int pending[kMaxHq];
@@ -342,9 +313,9 @@ int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, i
   });
   if (once_rc) return once_rc;
 
+  int rc;
   CUtensorMap mq, mk;
   if ((rc = make_map(&mq, q, Hq, N, kLastQ)) || (rc = make_map(&mk, k, Hkv, N, kBN))) return rc;
-  if ((rc = zero_status(status, st))) return rc;
   const dim3 grid(np, L.NC);
   est_kernel<1><<<grid, 256, kEstSmem1, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 1"))) return rc;
@@ -352,11 +323,166 @@ int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, i
   if ((rc = launched("estimation combine"))) return rc;
   est_kernel<2><<<grid, 256, kEstSmem2, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 2"))) return rc;
-  if (k_v > 0 || k_s > 0) {
-    vs_topk_kernel<<<dim3(n_heads, 2), 1024, 0, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx);
+  if (ld_v > 0 || ld_s > 0) {
+    vs_topk_kernel<<<dim3(n_heads, 2), 1024, 0, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx, ld_v,
+                                                      ld_s);
     if ((rc = launched("top-k"))) return rc;
   }
   return MI_OK;
+}
+
+// ------------------------------------------------------------ layer calls ----
+
+// The heads of a layer call grouped by pattern and budget.  Slots of one pattern
+// are numbered group after group, so every group's rows are contiguous.
+struct LayerPlan {
+  int n_listed = 0, n_vs = 0, n_blk = 0, n_ash = 0;
+  int KV = 0, KS = 0, TK = 0, vs_flags = 0;
+  HeadList listed;                        // launch order: dense, VS, block, A-shape
+  int n_vg = 0, vg_kv[MI_MAX_HEADS], vg_ks[MI_MAX_HEADS], vg_start[MI_MAX_HEADS + 1];
+  int n_bg = 0, bg_tk[MI_MAX_HEADS], bg_start[MI_MAX_HEADS + 1];
+  int16_t vs_head[MI_MAX_HEADS], blk_head[MI_MAX_HEADS];
+  int ash[2 * MI_MAX_HEADS];
+  int max_vg = 0;
+};
+
+int layer_plan(const mi_head_cfg* cfg, int Hq, int N, LayerPlan* P) {
+  if (!cfg) return MI_ERR_ARG;
+  int n_dense = 0;
+  int16_t dense_h[MI_MAX_HEADS];
+  bool have_vs = false;
+  for (int h = 0; h < Hq; ++h) {
+    const mi_head_cfg& c = cfg[h];
+    switch (c.pattern) {
+      case MI_PAT_SKIP: continue;
+      case MI_PAT_DENSE: break;
+      case MI_PAT_VS:
+        if (c.k_v < 0 || c.k_s < 0 || c.k_v > MI_MAX_KV) return MI_ERR_ARG;
+        if (c.vs_flags & ~MI_VS_BLOCK_EXPANDED) return MI_ERR_UNIMPLEMENTED;
+        if (have_vs && c.vs_flags != P->vs_flags) return MI_ERR_ARG;
+        have_vs = true;
+        P->vs_flags = c.vs_flags;
+        break;
+      case MI_PAT_BLOCK:
+        if (c.topk < 1 || c.topk > MI_MAX_KV / 2) return MI_ERR_ARG;
+        break;
+      case MI_PAT_ASHAPE:
+        if (c.n_init < 0 || c.window < 1) return MI_ERR_ARG;
+        break;
+      default: return MI_ERR_ARG;
+    }
+    if (P->n_listed == MI_MAX_HEADS) return MI_ERR_ARG;
+    ++P->n_listed;
+    if (c.pattern == MI_PAT_DENSE) dense_h[n_dense++] = static_cast<int16_t>(h);
+  }
+  if (P->n_listed == 0) return MI_ERR_ARG;
+  int n = 0;
+  auto list = [&](int h) { P->listed.h[n++] = static_cast<int16_t>(h); };
+  for (int i = 0; i < n_dense; ++i) list(dense_h[i]);
+  // vertical-slash heads, grouped by (k_v, k_s) in order of first appearance
+  bool done[kMaxHq] = {};
+  for (int h = 0; h < Hq; ++h) {
+    if (cfg[h].pattern != MI_PAT_VS || done[h]) continue;
+    const int kv = cfg[h].k_v, ks = cfg[h].k_s;
+    P->vg_kv[P->n_vg] = kv;
+    P->vg_ks[P->n_vg] = ks;
+    P->vg_start[P->n_vg] = P->n_vs;
+    for (int h2 = h; h2 < Hq; ++h2)
+      if (cfg[h2].pattern == MI_PAT_VS && !done[h2] && cfg[h2].k_v == kv && cfg[h2].k_s == ks) {
+        done[h2] = true;
+        P->vs_head[P->n_vs] = static_cast<int16_t>(h2);
+        list(h2);
+        ++P->n_vs;
+      }
+    P->max_vg = std::max(P->max_vg, P->n_vs - P->vg_start[P->n_vg]);
+    P->KV = std::max(P->KV, kv);
+    P->KS = std::max(P->KS, ks);
+    ++P->n_vg;
+  }
+  P->vg_start[P->n_vg] = P->n_vs;
+  for (int h = 0; h < Hq; ++h) {
+    if (cfg[h].pattern != MI_PAT_BLOCK || done[h]) continue;
+    const int tk = cfg[h].topk;
+    P->bg_tk[P->n_bg] = tk;
+    P->bg_start[P->n_bg] = P->n_blk;
+    for (int h2 = h; h2 < Hq; ++h2)
+      if (cfg[h2].pattern == MI_PAT_BLOCK && !done[h2] && cfg[h2].topk == tk) {
+        done[h2] = true;
+        P->blk_head[P->n_blk] = static_cast<int16_t>(h2);
+        list(h2);
+        ++P->n_blk;
+      }
+    P->TK = std::max(P->TK, tk);
+    ++P->n_bg;
+  }
+  P->bg_start[P->n_bg] = P->n_blk;
+  for (int h = 0; h < Hq; ++h) {
+    if (cfg[h].pattern != MI_PAT_ASHAPE) continue;
+    P->ash[2 * P->n_ash] = std::min(cfg[h].n_init, N);
+    P->ash[2 * P->n_ash + 1] = std::min(cfg[h].window, N);
+    list(h);
+    ++P->n_ash;
+  }
+  P->listed.n = n;
+  return MI_OK;
+}
+
+struct LayerLayout {
+  size_t status, est, vs, vidx, sidx, blk, blkidx, total;
+};
+LayerLayout layer_layout(const LayerPlan& P, int Hkv, int N) {
+  LayerLayout L;
+  Carve c;
+  L.status = c.take(256);
+  L.est = c.take(P.n_vs ? est_layout(P.max_vg, N).total : 0);
+  L.vs = c.take(P.n_vs ? vs_layout(P.n_vs, N).total : 0);
+  L.vidx = c.take(sizeof(int32_t) * (size_t)P.n_vs * std::max(P.KV, 1));
+  L.sidx = c.take(sizeof(int32_t) * (size_t)P.n_vs * std::max(P.KS, 1));
+  L.blk = c.take(P.n_blk ? block_layout(P.n_blk, Hkv, N).total : 0);
+  L.blkidx = c.take(sizeof(int32_t) * (size_t)P.n_blk * (N / kBlk) * std::max(P.TK, 1));
+  L.total = c.off;
+  return L;
+}
+
+}  // namespace
+
+// ====================================================================== ABI ==
+
+extern "C" {
+
+size_t mi_workspace_bytes(int op, int n_heads, int Hkv, int N, int k_v, int k_s, int topk) {
+  (void)k_v;
+  (void)k_s;
+  (void)topk;
+  if (n_heads <= 0 || N <= 0) return 0;
+  switch (op) {
+    case MI_OP_VS_ESTIMATE: return est_layout(n_heads, N).total;
+    case MI_OP_VS_SPARSE_ATTN: return vs_layout(n_heads, N).total;
+    case MI_OP_BLOCK_SPARSE_ATTN: return Hkv > 0 ? block_layout(n_heads, Hkv, N).total : 0;
+    case MI_OP_ASHAPE_ATTN:
+    case MI_OP_DENSE_CAUSAL_ATTN: return 256;
+    default: return 0;
+  }
+}
+
+int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
+                   const int32_t* heads, int n_heads, int last_q, int k_v, int k_s,
+                   int32_t* v_idx, int32_t* s_idx, void* workspace, size_t ws_bytes,
+                   mi_stream_t stream) {
+  int rc = check_device();
+  if (rc) return rc;
+  HeadList hl;
+  if ((rc = check_common(q, k, Hq, Hkv, N, d, heads, n_heads, &hl))) return rc;
+  if (last_q != kLastQ) return MI_ERR_SHAPE;
+  if (k_v < 0 || k_s < 0) return MI_ERR_ARG;
+  if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
+  const EstLayout L = est_layout(n_heads, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+  return est_run(q, k, Hq, Hkv, N, hl, k_v, k_s, v_idx, k_v, s_idx, k_s, ws, status, st);
 }
 
 int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
@@ -446,7 +572,7 @@ int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
     });
     if (once_rc) return once_rc;
     block_select_kernel<<<dim3(NB, n_heads), 256, sizeof(float) * NB, st>>>(
-        qbar, kbar, NB, Hq / Hkv, a.heads, topk, blk_idx);
+        qbar, kbar, NB, Hq / Hkv, a.heads, topk, topk, blk_idx);
     if ((rc = launched("block selection"))) return rc;
   } else {
     const int rows = n_heads * NB;
@@ -485,6 +611,145 @@ int mi_dense_causal_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
   int* status = static_cast<int*>(workspace);
   if ((rc = zero_status(status, st))) return rc;
   return run_attention<kPatDense>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
+}
+
+size_t mi_layer_workspace_bytes(int Hq, int Hkv, int N, const mi_head_cfg* cfg) {
+  if (Hq <= 0 || Hkv <= 0 || N <= 0 || Hq > kMaxHq || Hq % Hkv != 0) return 0;
+  LayerPlan P;
+  if (layer_plan(cfg, Hq, N, &P)) return 0;
+  return layer_layout(P, Hkv, N).total;
+}
+
+int mi_layer_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N,
+                  int d, const mi_head_cfg* cfg, mi_bf16* out, float* lse, void* workspace,
+                  size_t ws_bytes, mi_stream_t stream) {
+  int rc = check_device();
+  if (rc) return rc;
+  LayerPlan P;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return MI_ERR_ARG;
+  if (d != kD) return MI_ERR_SHAPE;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq > kMaxHq) return MI_ERR_SHAPE;
+  if (N < 64 || N % 64 != 0 || N > (1 << 21)) return MI_ERR_SHAPE;
+  if ((rc = layer_plan(cfg, Hq, N, &P))) return rc;
+  const LayerLayout L = layer_layout(P, Hkv, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.heads = P.listed;
+  const int group = Hq / Hkv;
+  // vertical-slash heads: estimation per budget group, one index build
+  int32_t* vidx = reinterpret_cast<int32_t*>(ws + L.vidx);
+  int32_t* sidx = reinterpret_cast<int32_t*>(ws + L.sidx);
+  if (P.n_vs) {
+    for (int gi = 0; gi < P.n_vg; ++gi) {
+      HeadList hl;
+      hl.n = P.vg_start[gi + 1] - P.vg_start[gi];
+      for (int i = 0; i < hl.n; ++i) hl.h[i] = P.vs_head[P.vg_start[gi] + i];
+      const size_t r0 = P.vg_start[gi];
+      if ((rc = est_run(q, k, Hq, Hkv, N, hl, P.vg_kv[gi], P.vg_ks[gi], vidx + r0 * P.KV, P.KV,
+                        sidx + r0 * P.KS, P.KS, ws + L.est, status, st)))
+        return rc;
+    }
+    const VsLayout V = vs_layout(P.n_vs, N);
+    char* vw = ws + L.vs;
+    VsIndexArgs ia;
+    ia.N = N;
+    ia.k_v = P.KV;
+    ia.k_s = P.KS;
+    ia.Nw = V.Nw;
+    ia.NT = V.NT;
+    ia.NTw = V.NTw;
+    ia.expanded = (P.vs_flags & MI_VS_BLOCK_EXPANDED) ? 1 : 0;
+    ia.v_idx = vidx;
+    ia.s_idx = sidx;
+    ia.offbits = reinterpret_cast<uint32_t*>(vw + V.offbits);
+    ia.colbits = reinterpret_cast<uint32_t*>(vw + V.colbits);
+    ia.dbits = reinterpret_cast<uint32_t*>(vw + V.dbits);
+    ia.dfull = reinterpret_cast<uint32_t*>(vw + V.dfull);
+    ia.dlist = reinterpret_cast<int*>(vw + V.dlist);
+    ia.dcount = reinterpret_cast<int*>(vw + V.dcount);
+    ia.status = status;
+    vs_index_kernel<<<P.n_vs, 512, 0, st>>>(ia);
+    if ((rc = launched("vertical-slash index build"))) return rc;
+    a.offbits = ia.offbits;
+    a.colbits = ia.colbits;
+    a.dbits = ia.dbits;
+    a.dfull = ia.dfull;
+    a.dlist = ia.dlist;
+    a.dcount = ia.dcount;
+    a.v_idx = vidx;
+    a.k_v = P.KV;
+    a.expand = ia.expanded;
+    a.Nw = V.Nw;
+    a.NT = V.NT;
+    a.NTw = V.NTw;
+  }
+  // block-sparse heads: pooling once, selection per top-k group
+  if (P.n_blk) {
+    const BlockLayout BL = block_layout(P.n_blk, Hkv, N);
+    char* bw = ws + L.blk;
+    float* qbar = reinterpret_cast<float*>(bw + BL.qbar);
+    float* kbar = reinterpret_cast<float*>(bw + BL.kbar);
+    int32_t* blk = reinterpret_cast<int32_t*>(ws + L.blkidx);
+    const int NB = N / kBlk;
+    HeadList hb;
+    hb.n = P.n_blk;
+    for (int i = 0; i < P.n_blk; ++i) hb.h[i] = P.blk_head[i];
+    const int wq = P.n_blk * NB, wk = Hkv * NB;
+    block_pool_kernel<<<cdiv(wq, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), N,
+                                                   P.n_blk, NB, hb, 1, qbar);
+    if ((rc = launched("block pooling (q)"))) return rc;
+    block_pool_kernel<<<cdiv(wk, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k), N,
+                                                   Hkv, NB, hb, 0, kbar);
+    if ((rc = launched("block pooling (k)"))) return rc;
+    if ((rc = set_smem(reinterpret_cast<const void*>(block_select_kernel), 160 * 1024))) return rc;
+    for (int gi = 0; gi < P.n_bg; ++gi) {
+      HeadList hl;
+      const int s0 = P.bg_start[gi];
+      hl.n = P.bg_start[gi + 1] - s0;
+      for (int i = 0; i < hl.n; ++i) hl.h[i] = P.blk_head[s0 + i];
+      block_select_kernel<<<dim3(NB, hl.n), 256, sizeof(float) * NB, st>>>(
+          qbar + (size_t)s0 * NB * kD, kbar, NB, group, hl, P.bg_tk[gi], P.TK,
+          blk + (size_t)s0 * NB * P.TK);
+      if ((rc = launched("block selection"))) return rc;
+    }
+    a.blk_idx = blk;
+    a.topk = P.TK;
+  }
+  // A-shape heads: per-head sizes, passed in the kernel arguments
+  a.ash_n = P.n_ash;
+  for (int i = 0; i < 2 * P.n_ash; ++i) a.ash_pairs[i] = P.ash[i];
+  // listed order is dense, vertical-slash, block-sparse, A-shape
+  {
+    const int n_dense = P.listed.n - P.n_vs - P.n_blk - P.n_ash;
+    a.layer_base[kPatDense] = 0;
+    a.layer_base[kPatVS] = n_dense;
+    a.layer_base[kPatBlock] = n_dense + P.n_vs;
+    a.layer_base[kPatAShape] = n_dense + P.n_vs + P.n_blk;
+    a.layer_base[4] = P.listed.n;
+  }
+  // the attention of every listed head in one launch
+  CUtensorMap mq, mk, mv, mkr, mvr;
+  if ((rc = make_map(&mq, q, Hq, N, kBM)) || (rc = make_map(&mk, k, Hkv, N, kBN)) ||
+      (rc = make_map(&mv, v, Hkv, N, kBN)) || (rc = make_rows_map(&mkr, k, Hkv, N)) ||
+      (rc = make_rows_map(&mvr, v, Hkv, N)))
+    return rc;
+  a.N = N;
+  a.group = group;
+  a.scale_log2 = kScaleLog2;
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.status = status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.skip_q_load = g_fault_mode.load() == MI_FAULT_SKIP_Q_LOAD ? 1 : 0;
+  cudaError_t e = launch_attn_layer(mq, mk, mv, mkr, mvr, a, cdiv(N, kBM), st);
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "layer attention kernel");
 }
 
 int mi_debug_inject(int mode, uint64_t wait_limit_ns) {

@@ -62,7 +62,14 @@ struct AttnArgs {
   int topk;
   // A-shape
   int n_init, window;
+  int ash_n;              // layer launches: A-shape heads with their own sizes in ash_pairs
+  int ash_pairs[2 * MI_MAX_HEADS];  // [A-shape slot][2] = n_init, window
   HeadList heads;
+  // layer launches: the listed heads are ordered dense, vertical-slash,
+  // block-sparse, A-shape; layer_base[p] is the first listed head of pattern p
+  // (layer_base[4] = heads.n), so a head's slot in its pattern's arrays is its
+  // listed index minus its pattern's base
+  int layer_base[5];
 };
 
 struct AttnSmem {
@@ -80,10 +87,13 @@ struct AttnSmem {
   int n_contig;  // leading contiguous tiles (VS)
   int has_t0;    // VS: tile 0 is prepended
   int d_cnt;     // VS: number of tile distances <= r
+  int ash_init;  // A-shape: sink tokens of this head
+  int ash_window;  // A-shape: window of this head
 };
 
 constexpr int kAttnThreads = 192;
 constexpr size_t kAttnSmemBytes = sizeof(AttnSmem) + 1024;
+static_assert(sizeof(AttnArgs) + 5 * sizeof(CUtensorMap) <= 4096, "attention kernel parameters exceed 4 KB");
 constexpr uint32_t kTmemCols = 256;  // S (and P over it) at 0, O at 128
 constexpr uint32_t kTmemO = 128;
 
@@ -118,8 +128,8 @@ __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a,
     ref.t = e >> 4;
     ref.sub = e & 0xF;
   } else {  // A-shape: sink tiles then the window tiles
-    const int t_lo = max(0, r * kBM - a.window + 1) / kBN;
-    const int n_sink = min(cdiv(a.n_init, kBN), t_lo);
+    const int t_lo = max(0, r * kBM - s.ash_window + 1) / kBN;
+    const int n_sink = min(cdiv(s.ash_init, kBN), t_lo);
     ref.t = (i < n_sink) ? i : t_lo + (i - n_sink);
   }
   return ref;
@@ -266,8 +276,8 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
   } else {  // A-shape
 #pragma unroll
     for (int w = 0; w < 4; ++w)
-      out[w] = range_bits(j0 + 32 * w, 0, a.n_init) |
-               range_bits(j0 + 32 * w, q - a.window + 1, q + 1);
+      out[w] = range_bits(j0 + 32 * w, 0, s.ash_init) |
+               range_bits(j0 + 32 * w, q - s.ash_window + 1, q + 1);
   }
   if (ref.t == r) {  // the diagonal tile: causal
 #pragma unroll
@@ -310,8 +320,8 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
     if (tid == 0) s.n_tiles = r + 1;
   } else if (PAT == kPatAShape) {
     if (tid == 0) {
-      const int t_lo = max(0, r * kBM - a.window + 1) / kBN;
-      const int n_sink = min(cdiv(a.n_init, kBN), t_lo);
+      const int t_lo = max(0, r * kBM - s.ash_window + 1) / kBN;
+      const int n_sink = min(cdiv(s.ash_init, kBN), t_lo);
       s.n_tiles = n_sink + (r - t_lo + 1);
     }
   } else if (PAT == kPatVS) {
@@ -415,19 +425,16 @@ __device__ __forceinline__ void for_s_halves(uint32_t taddr, const uint32_t mk[4
   }
 }
 
+// The engine for one CTA: row block r of head h, whose pattern arrays sit at
+// slot n.  Called by the per-pattern kernels and by the layer kernel.
 template <int PAT>
-__global__ void __launch_bounds__(kAttnThreads, 2)
-attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_kr,
-            const __grid_constant__ CUtensorMap map_vr, const __grid_constant__ AttnArgs a) {
-  extern __shared__ uint8_t smem_raw[];
+__device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& map_q,
+                                          const CUtensorMap& map_k, const CUtensorMap& map_v,
+                                          const CUtensorMap& map_kr, const CUtensorMap& map_vr,
+                                          const AttnArgs& a, int r, int n, int h) {
   AttnSmem& s = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int NRB = cdiv(a.N, kBM);
-  const int r = NRB - 1 - static_cast<int>(blockIdx.x);  // heaviest row blocks first
-  const int n = blockIdx.y;
-  const int h = a.heads.h[n];
   const int g = h / a.group;
 
   if (tid == 0) {
@@ -442,6 +449,8 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     mbar_init(&s.mma_done, 1);
     s.abort = 0;
     s.has_t0 = 1;
+    s.ash_init = a.ash_n ? a.ash_pairs[2 * n] : a.n_init;
+    s.ash_window = a.ash_n ? a.ash_pairs[2 * n + 1] : a.window;
     fence_mbar_init();
   }
   if (warp == 4) {
@@ -682,6 +691,20 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   }
 }
 
+// One pattern for all listed heads: blockIdx.y is the listed head, blockIdx.x
+// the row block counted from the last (the heaviest first).
+template <int PAT>
+__global__ void __launch_bounds__(kAttnThreads, 2)
+attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_kr,
+            const __grid_constant__ CUtensorMap map_vr, const __grid_constant__ AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const int NRB = cdiv(a.N, kBM);
+  const int n = blockIdx.y;
+  attn_body<PAT>(smem_raw, map_q, map_k, map_v, map_kr, map_vr, a,
+                 NRB - 1 - static_cast<int>(blockIdx.x), n, a.heads.h[n]);
+}
+
 }  // namespace mi
 
 namespace mi {
@@ -692,5 +715,10 @@ template <int PAT>
 cudaError_t launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const CUtensorMap& mkr, const CUtensorMap& mvr, const AttnArgs& a,
                         int n_row_blocks, cudaStream_t st);
+
+// Layer launcher (all patterns of a layer's heads in one launch).
+cudaError_t launch_attn_layer(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                              const CUtensorMap& mkr, const CUtensorMap& mvr, const AttnArgs& a,
+                              int n_row_blocks, cudaStream_t st);
 
 }  // namespace mi

@@ -39,10 +39,11 @@ __global__ void block_pool_kernel(const __nv_bfloat16* src, int N, int n_out, in
   *reinterpret_cast<float4*>(out + ((size_t)o * NB + blk) * kD + lane * 4) = res;
 }
 
-// Per (query block r, listed head): sigma over c <= r, then top-k into blk_idx.
+// Per (query block r, listed head): sigma over c <= r, then top-k into blk_idx
+// (rows of ld >= topk entries, padded with -1).
 __global__ void __launch_bounds__(256)
 block_select_kernel(const float* qbar, const float* kbar, int NB, int group, HeadList heads,
-                    int topk, int32_t* blk_idx) {
+                    int topk, int ld, int32_t* blk_idx) {
   extern __shared__ float sig[];  // [NB]
   __shared__ SelectSmem sm;
   __shared__ __align__(16) float qrow[kD];
@@ -60,11 +61,11 @@ block_select_kernel(const float* qbar, const float* kbar, int NB, int group, Hea
     if (lane == 0) sig[c] = d;
   }
   __syncthreads();
-  int32_t* out = blk_idx + ((size_t)slot * NB + r) * topk;
+  int32_t* out = blk_idx + ((size_t)slot * NB + r) * ld;
   const int kk = min(topk, r + 1);  // >= 1
   const float* sp = sig;
   topk_select_sorted<256>([sp](int i) { return float_key(sp[i]); }, r + 1, kk, out, sm);
-  for (int i = kk + tid; i < topk; i += 256) out[i] = -1;
+  for (int i = kk + tid; i < ld; i += 256) out[i] = -1;
 }
 
 // With caller-given block lists: flag any row that is not ascending, out of

@@ -128,16 +128,17 @@ __device__ void topk_select_sorted(F key_at, int n, int k, int* out, SelectSmem&
 // k > N keeps all N indices, and the row is padded with -1 up to k.
 __global__ void __launch_bounds__(1024)
 vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int32_t* v_idx,
-               int32_t* s_idx) {
+               int32_t* s_idx, int ld_v, int ld_s) {
   __shared__ SelectSmem sm;
   const int slot = blockIdx.x;
   const bool vert = blockIdx.y == 0;
   const float* x = (vert ? vsc : ssc) + (size_t)slot * N;
   const int k = vert ? k_v : k_s;
+  const int ld = vert ? ld_v : ld_s;  // row stride >= k; the rest of a row is padding
   const int kk = min(k, N);
-  int32_t* out = (vert ? v_idx : s_idx) + (size_t)slot * k;
+  int32_t* out = (vert ? v_idx : s_idx) + (size_t)slot * ld;
   if (kk > 0) topk_select_sorted<1024>([x](int i) { return float_key(__ldg(x + i)); }, N, kk, out, sm);
-  for (int i = kk + threadIdx.x; i < k; i += 1024) out[i] = -1;
+  for (int i = kk + threadIdx.x; i < ld; i += 1024) out[i] = -1;
 }
 
 }  // namespace mi

@@ -31,7 +31,7 @@ import torch
 
 from . import binding as B
 
-__all__ = ["Candidate", "Evaluation", "HeadChoice", "default_candidates", "choose", "search"]
+__all__ = ["Candidate", "Evaluation", "HeadChoice", "default_candidates", "choose", "search", "layer_config"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -158,6 +158,22 @@ def search(q, k, v, heads: Optional[Sequence[int]] = None, candidates: Optional[
         choices.append(HeadChoice(h, choose(evals, budget, recall_tol), dense_ms, budget, evals))
         del qr, kr, vr, outr
     return choices
+
+
+def layer_config(choices: Sequence[HeadChoice], Hq: int) -> List["B.HeadCfg"]:
+    """The per-head configuration of ``mi_layer_attn`` for the chosen patterns
+    (heads without a choice are computed dense)."""
+    cfg = [B.HeadCfg.dense() for _ in range(Hq)]
+    for c in choices:
+        p = c.choice.candidate.p
+        pat = c.choice.candidate.pattern
+        if pat == "vs":
+            cfg[c.head] = B.HeadCfg.vs(p["k_v"], p["k_s"])
+        elif pat == "block":
+            cfg[c.head] = B.HeadCfg.block(p["topk"])
+        else:
+            cfg[c.head] = B.HeadCfg.ashape(p["n_init"], p["window"])
+    return cfg
 
 
 def _main(argv=None) -> None:

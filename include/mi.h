@@ -178,6 +178,49 @@ int mi_dense_causal_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
                          float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream);
 
 /*
+ * A whole layer in one call: every q-head with its own pattern and budgets.
+ * Slides: "Step 1: Kernel-Aware Sparse Pattern Search" (each head's pattern is
+ * fixed offline) and "Step 2: Online Estimation of Sparsity Indices" (the indices
+ * of the dynamic patterns are found online); README mirror, "TL;DR".
+ *
+ * cfg: HOST array of Hq entries.  Head h gets the result of the per-pattern call
+ * its cfg[h].pattern names, with that entry's budgets:
+ *   MI_PAT_VS      mi_vs_estimate (k_v, k_s) + mi_vs_sparse_attn (vs_flags);
+ *   MI_PAT_BLOCK   mi_block_sparse_attn with its own selection (topk);
+ *   MI_PAT_ASHAPE  mi_ashape_attn (n_init, window);
+ *   MI_PAT_DENSE   mi_dense_causal_attn;
+ *   MI_PAT_SKIP    nothing (out rows of the head are left untouched).
+ * Budgets may differ between heads; vs_flags must be the same for every
+ * vertical-slash head.  Fields a pattern does not use are ignored.
+ * The estimation and block selection run per group of heads with equal
+ * budgets; the attention of every head of every pattern is ONE kernel launch,
+ * ordered dense, vertical-slash, block-sparse, A-shape with the heaviest row
+ * blocks first, so that lighter work fills the end of heavier work.
+ * workspace: mi_layer_workspace_bytes(Hq, Hkv, N, cfg) bytes of device memory.
+ * Errors: an invalid cfg entry returns MI_ERR_ARG (MI_ERR_SHAPE for shapes), as
+ * the per-pattern calls do; data errors land in the status word
+ * (mi_read_status on the workspace).
+ */
+#define MI_PAT_SKIP (-1)
+#define MI_PAT_DENSE 0
+#define MI_PAT_VS 1
+#define MI_PAT_BLOCK 2
+#define MI_PAT_ASHAPE 3
+typedef struct {
+  int32_t pattern;   /* MI_PAT_* */
+  int32_t k_v, k_s;  /* vertical-slash budgets (0 <= k_v <= MI_MAX_KV, k_s >= 0) */
+  int32_t vs_flags;  /* 0 or MI_VS_BLOCK_EXPANDED */
+  int32_t topk;      /* block-sparse: 1 <= topk <= MI_MAX_KV / 2 */
+  int32_t n_init, window; /* A-shape: n_init >= 0, window >= 1 */
+} mi_head_cfg;
+
+size_t mi_layer_workspace_bytes(int Hq, int Hkv, int N, const mi_head_cfg* cfg);
+
+int mi_layer_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N,
+                  int d, const mi_head_cfg* cfg, mi_bf16* out, float* lse, void* workspace,
+                  size_t ws_bytes, mi_stream_t stream);
+
+/*
  * mi_vs_estimate_noalloc: mi_vs_estimate for callers that cannot allocate device
  * memory (for instance an engine whose memory pool owns the whole device, or a
  * plugin running where cudaMalloc is not allowed).  The pages have no

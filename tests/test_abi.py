@@ -55,3 +55,21 @@ def test_fault_injection_argument_checks(lib):
     assert B.mi_debug_inject(7, 1000) == B.MI_ERR_ARG
     assert B.mi_debug_inject(B.MI_FAULT_SKIP_Q_LOAD, 0) == B.MI_ERR_ARG
     assert B.mi_debug_inject(B.MI_FAULT_NONE, 0) == B.MI_OK
+
+
+def test_layer_workspace_sizes_need_no_gpu(lib):
+    H = B.HeadCfg
+    cfg = [H.dense(), H.vs(64, 32), H.vs(128, 16), H.block(8), H.ashape(128, 512), H.skip(), H.skip(), H.skip()]
+    n = B.mi_layer_workspace_bytes(8, 2, 4096, cfg)
+    assert n > 0 and n % 256 == 0
+    # more vertical-slash budget never needs less workspace
+    cfg2 = list(cfg)
+    cfg2[2] = H.vs(1000, 2000)
+    assert B.mi_layer_workspace_bytes(8, 2, 4096, cfg2) >= n
+    bad = list(cfg)
+    bad[0] = B.HeadCfg(7, 0, 0, 0, 0, 0, 0)
+    assert B.mi_layer_workspace_bytes(8, 2, 4096, bad) == 0
+    assert B.mi_layer_workspace_bytes(8, 2, 4096, [H.skip()] * 8) == 0
+    mixed_flags = list(cfg)
+    mixed_flags[2] = H.vs(128, 16, expanded=True)
+    assert B.mi_layer_workspace_bytes(8, 2, 4096, mixed_flags) == 0

@@ -83,3 +83,12 @@ def test_search_recovers_planted_pattern_types():
     for c in choices:
         fit = [e.recall for e in c.evaluations if e.cost_ms <= c.budget_ms]
         assert c.choice.recall >= max(fit) - 0.005
+    # the chosen configuration runs as one layer call and keeps the recall it was chosen for
+    cfg = S.layer_config(choices, 3)
+    lse_d = torch.empty((3, N), dtype=torch.float32, device=DEV)
+    lse = torch.empty_like(lse_d)
+    B.mi_dense_causal_attn(x.q, x.k, x.v, lse=lse_d)
+    B.mi_layer_attn(x.q, x.k, x.v, cfg, lse=lse)
+    got = torch.exp(lse - lse_d).double().mean(dim=1).cpu().numpy()
+    for c in choices:
+        assert abs(got[c.head] - c.choice.recall) < 1e-6

@@ -310,6 +310,7 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, const HeadList
   std::call_once(once, [] {
     once_rc = set_smem(reinterpret_cast<const void*>(est_kernel<1>), kEstSmem1);
     if (once_rc == MI_OK) once_rc = set_smem(reinterpret_cast<const void*>(est_kernel<2>), kEstSmem2);
+    if (once_rc == MI_OK) once_rc = set_smem(reinterpret_cast<const void*>(vs_topk_kernel), kTopkSmemBytes);
   });
   if (once_rc) return once_rc;
 
@@ -324,7 +325,7 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, const HeadList
   est_kernel<2><<<grid, 256, kEstSmem2, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 2"))) return rc;
   if (ld_v > 0 || ld_s > 0) {
-    vs_topk_kernel<<<dim3(n_heads, 2), 1024, 0, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx, ld_v,
+    vs_topk_kernel<<<dim3(n_heads, 2), 1024, kTopkSmemBytes, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx, ld_v,
                                                       ld_s);
     if ((rc = launched("top-k"))) return rc;
   }

@@ -23,13 +23,11 @@ struct SelectSmem {
   int rem;
 };
 
-// key_at(i) -> order-preserving uint32 key of element i (see float_key).
-// Requires 1 <= k <= n.  Writes the k selected indices ascending to out[0..k).
-// All NT threads of the block must call it.  The function has no early exit:
-// every thread runs every block barrier in it.
+// The key of the k-th largest of n keys (1 <= k <= n) by a 4-pass 8-bit radix
+// select; *rem_out receives how many elements equal to that key are among the
+// top k.  All NT threads of the block must call it; no early exit.
 template <int NT, class F>
-__device__ void topk_select_sorted(F key_at, int n, int k, int* out, SelectSmem& sm) {
-  constexpr int NW = NT / 32;
+__device__ uint32_t radix_kth_key(F key_at, int n, int k, SelectSmem& sm, int* rem_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t prefix = 0, pmask = 0;
   int rem = k;
@@ -86,16 +84,24 @@ __device__ void topk_select_sorted(F key_at, int n, int k, int* out, SelectSmem&
     rem = sm.rem;
     __syncthreads();
   }
-  // prefix is now the key of the k-th largest element; take all larger keys and
-  // the first `rem` equal ones.  Warp w sweeps its own contiguous segment.
+  *rem_out = rem;
+  return prefix;
+}
+
+// Ordered take: out receives, ascending, every i with key > kth plus the first
+// `rem` i with key == kth (warp w sweeps its own contiguous segment).
+template <int NT, class F>
+__device__ void take_sorted(F key_at, int n, uint32_t kth, int rem, int* out, SelectSmem& sm) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int seg = cdiv(cdiv(n, NW), 32) * 32;
   const int beg = min(warp * seg, n), end = min(beg + seg, n);
   int gt = 0, eq = 0;
   for (int base = beg; base < end; base += 32) {
     const int i = base + lane;
     const uint32_t u = (i < end) ? key_at(i) : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, i < end && u > prefix));
-    eq += __popc(__ballot_sync(0xffffffffu, i < end && u == prefix));
+    gt += __popc(__ballot_sync(0xffffffffu, i < end && u > kth));
+    eq += __popc(__ballot_sync(0xffffffffu, i < end && u == kth));
   }
   if (lane == 0) {
     sm.wgt[warp] = gt;
@@ -111,8 +117,8 @@ __device__ void topk_select_sorted(F key_at, int n, int k, int* out, SelectSmem&
   for (int base = beg; base < end; base += 32) {
     const int i = base + lane;
     const uint32_t u = (i < end) ? key_at(i) : 0u;
-    const bool isg = i < end && u > prefix;
-    const bool ise = i < end && u == prefix;
+    const bool isg = i < end && u > kth;
+    const bool ise = i < end && u == kth;
     const unsigned bg = __ballot_sync(0xffffffffu, isg);
     const unsigned be = __ballot_sync(0xffffffffu, ise);
     const int G = gb + __popc(bg & lt), E = eb + __popc(be & lt);
@@ -124,12 +130,46 @@ __device__ void topk_select_sorted(F key_at, int n, int k, int* out, SelectSmem&
   __syncthreads();
 }
 
+// key_at(i) -> order-preserving uint32 key of element i (see float_key).
+// Requires 1 <= k <= n.  Writes the k selected indices ascending to out[0..k).
+// All NT threads of the block must call it.  The function has no early exit:
+// every thread runs every block barrier in it.
+template <int NT, class F>
+__device__ void topk_select_sorted(F key_at, int n, int k, int* out, SelectSmem& sm) {
+  int rem;
+  const uint32_t kth = radix_kth_key<NT>(key_at, n, k, sm, &rem);
+  take_sorted<NT>(key_at, n, kth, rem, out, sm);
+}
+
 // T1: top-k of the vertical (y = 0) or slash (y = 1) scores of every listed head;
-// k > N keeps all N indices, and the row is padded with -1 up to k.
-__global__ void __launch_bounds__(1024)
+// k > N keeps all N indices, and the row is padded with -1 up to the row stride.
+//
+// For k much smaller than N a threshold filter does most of the work in two
+// passes over the scores: the key at rank about 1.5 k S / N of a strided sample
+// of S = 8192 scores is a threshold that about 1.5 k scores reach; the scores at
+// or above it are compacted, in index order, into shared memory, and the exact
+// selection runs on them.  If at least k scores reach the threshold, every
+// element of the top k (ties at the k-th key included) is among them, so the
+// result is the same as selecting over all N; otherwise, or if they do not fit,
+// the selection runs over all N.
+constexpr int kTopkSample = 8192;
+constexpr int kTopkCand = 20480;
+struct TopkSmem {
+  SelectSmem sel;
+  uint32_t samp[kTopkSample];
+  uint32_t ckey[kTopkCand];
+  int cidx[kTopkCand];
+  int wcnt[32];
+};
+constexpr size_t kTopkSmemBytes = sizeof(TopkSmem);
+
+__global__ void __launch_bounds__(1024, 1)
 vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int32_t* v_idx,
                int32_t* s_idx, int ld_v, int ld_s) {
-  __shared__ SelectSmem sm;
+  extern __shared__ uint8_t topk_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(topk_raw);
+  constexpr int NT = 1024, NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = blockIdx.x;
   const bool vert = blockIdx.y == 0;
   const float* x = (vert ? vsc : ssc) + (size_t)slot * N;
@@ -137,8 +177,57 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
   const int ld = vert ? ld_v : ld_s;  // row stride >= k; the rest of a row is padding
   const int kk = min(k, N);
   int32_t* out = (vert ? v_idx : s_idx) + (size_t)slot * ld;
-  if (kk > 0) topk_select_sorted<1024>([x](int i) { return float_key(__ldg(x + i)); }, N, kk, out, sm);
-  for (int i = kk + threadIdx.x; i < ld; i += 1024) out[i] = -1;
+  auto gkey = [x](int i) { return float_key(__ldg(x + i)); };
+  bool done = kk == 0;
+  if (!done && N >= 4 * kTopkSample && 3 * kk <= 2 * kTopkCand) {
+    for (int j = tid; j < kTopkSample; j += NT)
+      sm.samp[j] = gkey(static_cast<int>((static_cast<int64_t>(j) * N) / kTopkSample));
+    __syncthreads();
+    const int rs = min(kTopkSample,
+                       static_cast<int>((3ll * kk * kTopkSample) / (2ll * N)) + 16);
+    int rem_s;
+    const uint32_t* sp = sm.samp;
+    const uint32_t tau = radix_kth_key<NT>([sp](int j) { return sp[j]; }, kTopkSample, rs, sm.sel, &rem_s);
+    // count the scores at or above the threshold, warp by warp over contiguous segments
+    const int seg = cdiv(cdiv(N, NW), 32) * 32;
+    const int beg = min(warp * seg, N), end = min(beg + seg, N);
+    int c = 0;
+    for (int base = beg; base < end; base += 32) {
+      const int i = base + lane;
+      c += __popc(__ballot_sync(0xffffffffu, i < end && gkey(i) >= tau));
+    }
+    if (lane == 0) sm.wcnt[warp] = c;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < NW; ++w) {
+      total += sm.wcnt[w];
+      if (w < warp) before += sm.wcnt[w];
+    }
+    if (total >= kk && total <= kTopkCand) {  // the same for every thread
+      const unsigned lt = (1u << lane) - 1u;
+      for (int base = beg; base < end; base += 32) {
+        const int i = base + lane;
+        const uint32_t u = (i < end) ? gkey(i) : 0u;
+        const bool in = i < end && u >= tau;
+        const unsigned b = __ballot_sync(0xffffffffu, in);
+        if (in) {
+          const int p = before + __popc(b & lt);
+          sm.ckey[p] = u;
+          sm.cidx[p] = i;
+        }
+        before += __popc(b);
+      }
+      __syncthreads();
+      const uint32_t* ck = sm.ckey;
+      topk_select_sorted<NT>([ck](int j) { return ck[j]; }, total, kk, out, sm.sel);
+      // candidate positions -> score indices (each thread its own entries)
+      for (int j = tid; j < kk; j += NT) out[j] = sm.cidx[out[j]];
+      done = true;
+    }
+    __syncthreads();
+  }
+  if (!done) topk_select_sorted<NT>(gkey, N, kk, out, sm.sel);
+  for (int i = kk + tid; i < ld; i += NT) out[i] = -1;
 }
 
 }  // namespace mi

@@ -388,3 +388,21 @@ def test_bounded_wait_expiry_reports_timeout():
     assert B.mi_read_status(ws) == B.MI_OK
     ref, _ = O.attention_rows(x.q[0], x.k[0], x.v[0], np.arange(N), lambda r: O.causal_mask_rows(N, r))
     assert_close(out.float().cpu().numpy()[0], ref, "after timeout")
+
+
+def test_estimate_all_ties_takes_lowest_indices():
+    """Zero queries: every query weighs its keys uniformly, so the column scores tie
+    (each column summed over the same rows in the same order) and the selection must
+    keep the lowest indices, also at large N where the sampled-threshold path sees
+    every score reach the threshold and the full selection runs.  The slash scores
+    also tie in exact arithmetic, but the GPU sums each diagonal in fp32 across tiles
+    in its own order, so they are compared with the tie band."""
+    N, Hq, Hkv = 32768, 2, 1
+    x = _rand_inputs(Hq, Hkv, N, seed=6)
+    q = torch.zeros_like(x.q).to(DEV)
+    k = x.k.to(DEV)
+    v_idx, s_idx = B.mi_vs_estimate(q, k, k_v=1000, k_s=2048)
+    for h in range(Hq):
+        vi_ref, si_ref, _, sc = O.vs_estimate(torch.zeros_like(x.q[h]), x.k[0], 64, 1000, 2048)
+        assert v_idx[h].cpu().tolist() == vi_ref.tolist()
+        band_agree(s_idx[h].cpu().numpy(), si_ref, sc, 2048)

@@ -166,8 +166,8 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       float x[128];
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + b * 128 + c * 32, x + c * 32);
+        tmem_ld64(tmem + lane_base + b * 128, x);
+        tmem_ld64(tmem + lane_base + b * 128 + 64, x + 64);
         tc_fence_before();
         mbar_arrive(&s.s_empty[b]);
       } else {
@@ -206,9 +206,10 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             const int sl = hh ? slot_b : slot_a;
             if (halo || sl < 0 || j0 + c >= N) continue;
             const float* col = A + hh * 64 * kEstPitch + c;
-            float acc = 0.f;
-#pragma unroll 8
-            for (int r = 0; r < 64; ++r) acc += col[r * kEstPitch];
+            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < 64; ++r) acc4[r & 3] += col[r * kEstPitch];
+            const float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
             a.vsc[(size_t)sl * N + j0 + c] = acc;
           } else {  // diagonal sums; diagonal e of the tile meets key j0 + e at row 63
             const int Jd = J - 256;
@@ -216,8 +217,21 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             const int sl = hh ? slot_b : slot_a;
             const int i_lo = max(0, 63 - e), i_hi = min(63, 190 - e);
             const float* At = A + hh * 64 * kEstPitch;
-            float acc = 0.f;
-            for (int r = i_lo; r <= i_hi; ++r) acc += At[r * kEstPitch + (e - 63 + r)];
+            // rows i_lo..i_hi in batches of 8 with independent loads (addresses
+            // clamped into the tile, out-of-range rows weighted 0), summed in a
+            // fixed order: four partial sums, then their pairwise sum
+            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r0 = 0; r0 < 64; r0 += 8) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int r = r0 + u;
+                const int c = min(max(e - 63 + r, 0), 127);
+                const float val = At[r * kEstPitch + c];
+                acc4[u & 3] += (r >= i_lo && r <= i_hi) ? val : 0.f;
+              }
+            }
+            float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
             if (e < 63) acc += cin[hh * 64 + e];
             if (e < 128) {
               const int d = j0 + e;

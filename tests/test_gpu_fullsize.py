@@ -187,3 +187,22 @@ def test_vs_block_expanded_32k_sampled():
         assert_close(out[h][torch.as_tensor(rows, device=DEV)].float().cpu().numpy(), ref,
                      f"expanded head {h}")
     _free(x, v_idx, s_idx, out)
+
+
+def test_largest_accepted_length_2m():
+    """N = 2^21, the largest length the ABI accepts: margin-planted indices bit-exact,
+    and sampled rows of the vertical-slash attention against the oracle."""
+    N = 1 << 21
+    x = I.margin_inputs(4, 1, N, 500, 2048, seed=211, device=DEV)
+    v_idx, s_idx = B.mi_vs_estimate(x.q, x.k, k_v=500, k_s=2048)
+    vi, si = v_idx.cpu().numpy(), s_idx.cpu().numpy()
+    for h in range(4):
+        assert vi[h].tolist() == x.planted_cols[0].tolist(), f"head {h}"
+        assert si[h].tolist() == x.planted_offsets[0].tolist(), f"head {h}"
+    out = B.mi_vs_sparse_attn(x.q, x.k, x.v, v_idx, s_idx, heads=[0])
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(N - 8, N),
+                                     np.random.default_rng(5).integers(0, N, 8)]))
+    ref = _check_vs_rows(x, 0, vi[0], si[0], rows, "2m")
+    assert_close(out[0][torch.as_tensor(rows, device=DEV)].float().cpu().numpy(), ref, "vs 2M head 0")
+    _free(x, v_idx, s_idx, out)

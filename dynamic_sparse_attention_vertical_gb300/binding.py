@@ -279,7 +279,7 @@ def mi_block_sparse_attn(q, k, v, topk: int = 100, heads=None, blk_idx=None, giv
     if out is None:
         out = torch.zeros_like(q)
     if blk_idx is None:
-        blk_idx = torch.empty((n, N // 64, topk), dtype=torch.int32, device=q.device)
+        blk_idx = torch.empty((n, (N + 63) // 64, topk), dtype=torch.int32, device=q.device)
     ws = _workspace(MI_OP_BLOCK_SPARSE_ATTN, n, Hkv, N, 0, 0, topk, workspace, q.device)
     rc = load().mi_block_sparse_attn(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, N, d, harr, n, block,
                                      topk, _ptr(blk_idx), MI_IDX_GIVEN if given else 0,

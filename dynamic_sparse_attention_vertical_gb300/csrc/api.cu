@@ -120,7 +120,7 @@ int check_common(const void* q, const void* k, int Hq, int Hkv, int N, int d,
   if (!q || !k || !aligned16(q) || !aligned16(k)) return MI_ERR_ARG;
   if (d != kD) return MI_ERR_SHAPE;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq > kMaxHq) return MI_ERR_SHAPE;
-  if (N < 64 || N % 64 != 0 || N > (1 << 21)) return MI_ERR_SHAPE;
+  if (N < 1 || N > (1 << 21)) return MI_ERR_SHAPE;
   if (n_heads <= 0 || n_heads > MI_MAX_HEADS || n_heads > Hq) return MI_ERR_ARG;
   if (!heads && n_heads != Hq) return MI_ERR_ARG;
   bool seen[kMaxHq] = {};
@@ -189,7 +189,7 @@ struct BlockLayout {
 BlockLayout block_layout(int n_heads, int Hkv, int N) {
   BlockLayout L;
   Carve c;
-  const int NB = N / kBlk;
+  const int NB = cdiv(N, kBlk);
   L.status = c.take(256);
   L.qbar = c.take(sizeof(float) * (size_t)n_heads * NB * kD);
   L.kbar = c.take(sizeof(float) * (size_t)Hkv * NB * kD);
@@ -440,7 +440,7 @@ LayerLayout layer_layout(const LayerPlan& P, int Hkv, int N) {
   L.vidx = c.take(sizeof(int32_t) * (size_t)P.n_vs * std::max(P.KV, 1));
   L.sidx = c.take(sizeof(int32_t) * (size_t)P.n_vs * std::max(P.KS, 1));
   L.blk = c.take(P.n_blk ? block_layout(P.n_blk, Hkv, N).total : 0);
-  L.blkidx = c.take(sizeof(int32_t) * (size_t)P.n_blk * (N / kBlk) * std::max(P.TK, 1));
+  L.blkidx = c.take(sizeof(int32_t) * (size_t)P.n_blk * cdiv(N, kBlk) * std::max(P.TK, 1));
   L.total = c.off;
   return L;
 }
@@ -474,7 +474,7 @@ int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, i
   if (rc) return rc;
   HeadList hl;
   if ((rc = check_common(q, k, Hq, Hkv, N, d, heads, n_heads, &hl))) return rc;
-  if (last_q != kLastQ) return MI_ERR_SHAPE;
+  if (last_q != kLastQ || N < kLastQ) return MI_ERR_SHAPE;
   if (k_v < 0 || k_s < 0) return MI_ERR_ARG;
   if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
   const EstLayout L = est_layout(n_heads, N);
@@ -555,7 +555,7 @@ int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.status);
   if ((rc = zero_status(status, st))) return rc;
-  const int NB = N / kBlk;
+  const int NB = cdiv(N, kBlk);
   if (!(flags & MI_IDX_GIVEN)) {
     float* qbar = reinterpret_cast<float*>(ws + L.qbar);
     float* kbar = reinterpret_cast<float*>(ws + L.kbar);
@@ -631,7 +631,7 @@ int mi_layer_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, 
     return MI_ERR_ARG;
   if (d != kD) return MI_ERR_SHAPE;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq > kMaxHq) return MI_ERR_SHAPE;
-  if (N < 64 || N % 64 != 0 || N > (1 << 21)) return MI_ERR_SHAPE;
+  if (N < 1 || N > (1 << 21)) return MI_ERR_SHAPE;
   if ((rc = layer_plan(cfg, Hq, N, &P))) return rc;
   const LayerLayout L = layer_layout(P, Hkv, N);
   if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
@@ -698,7 +698,7 @@ int mi_layer_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, 
     float* qbar = reinterpret_cast<float*>(bw + BL.qbar);
     float* kbar = reinterpret_cast<float*>(bw + BL.kbar);
     int32_t* blk = reinterpret_cast<int32_t*>(ws + L.blkidx);
-    const int NB = N / kBlk;
+    const int NB = cdiv(N, kBlk);
     HeadList hb;
     hb.n = P.n_blk;
     for (int i = 0; i < P.n_blk; ++i) hb.h[i] = P.blk_head[i];

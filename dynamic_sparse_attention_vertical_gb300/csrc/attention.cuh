@@ -58,7 +58,7 @@ struct AttnArgs {
   int expand;               // block-expanded slash mode
   int Nw, NT, NTw;
   // block-sparse
-  const int* blk_idx;  // [n_heads, N/64, topk]
+  const int* blk_idx;  // [n_heads, ceil(N/64), topk]
   int topk;
   // A-shape
   int n_init, window;
@@ -361,7 +361,7 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
     }
   } else {  // block-sparse: union of the two 64-row halves' selected blocks, as 128-key tiles
     if (tid == 0) {
-      const int NB = a.N / kBlk;
+      const int NB = cdiv(a.N, kBlk);
       const int* b0 = a.blk_idx + ((size_t)n * NB + 2 * r) * a.topk;
       const bool has1 = (2 * r + 1) < NB;
       const int* b1 = b0 + a.topk;

@@ -13,9 +13,9 @@
 
 namespace mi {
 
-// Mean of 64 consecutive rows, fp32: one warp per (head, block); lane l owns
-// dims 4l..4l+3 and adds the rows in order.  Output head o reads source head
-// heads.h[o] (use_list) or o.
+// Mean of 64 consecutive rows (of the rows left in a last, partial block), fp32:
+// one warp per (head, block); lane l owns dims 4l..4l+3 and adds the rows in
+// order.  Output head o reads source head heads.h[o] (use_list) or o.
 __global__ void block_pool_kernel(const __nv_bfloat16* src, int N, int n_out, int NB,
                                   HeadList heads, int use_list, float* out) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -25,7 +25,8 @@ __global__ void block_pool_kernel(const __nv_bfloat16* src, int N, int n_out, in
   const int h = use_list ? heads.h[o] : o;
   const __nv_bfloat16* base = src + ((size_t)h * N + (size_t)blk * kBlk) * kD + lane * 4;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int r = 0; r < kBlk; ++r) {
+  const int rows = min(kBlk, N - blk * kBlk);
+  for (int r = 0; r < rows; ++r) {
     const uint2 raw = *reinterpret_cast<const uint2*>(base + (size_t)r * kD);
     const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
     const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
@@ -34,8 +35,8 @@ __global__ void block_pool_kernel(const __nv_bfloat16* src, int N, int n_out, in
     acc[2] += __low2float(p1);
     acc[3] += __high2float(p1);
   }
-  const float4 res = make_float4(acc[0] * (1.f / kBlk), acc[1] * (1.f / kBlk),
-                                 acc[2] * (1.f / kBlk), acc[3] * (1.f / kBlk));
+  const float inv = 1.f / static_cast<float>(rows);
+  const float4 res = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
   *reinterpret_cast<float4*>(out + ((size_t)o * NB + blk) * kD + lane * 4) = res;
 }
 

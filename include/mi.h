@@ -19,7 +19,10 @@
  * --------------------------------
  *  Tensors.  q: [Hq, N, d], k and v: [Hkv, N, d], out: [Hq, N, d]; all bf16
  *    (mi_bf16 = raw bf16 bits), row-major and contiguous, DEVICE pointers owned
- *    by the caller.  d must be 128 and N a multiple of 64 in [64, 2^21].
+ *    by the caller.  d must be 128 and 1 <= N <= 2^21 (the estimation, which
+ *    scores the last 64 queries, needs N >= 64).  A last, partial 64-block of
+ *    rows or keys is a block of its own (block-sparse pooling takes the mean
+ *    of its rows).
  *    Grouped-query attention: q-head h reads KV head h / (Hq / Hkv);
  *    Hq % Hkv == 0.  q, k, v, out must be 16-byte aligned.
  *  Heads.  `heads` is a HOST array of n_heads distinct q-head indices in
@@ -58,7 +61,7 @@ typedef struct CUstream_st* mi_stream_t; /* a cudaStream_t */
 
 #define MI_OK 0
 #define MI_ERR_ARG (-1)           /* NULL/misaligned pointer, bad head list, k < 0, ... */
-#define MI_ERR_SHAPE (-2)         /* d != 128, N % 64 != 0, Hq % Hkv != 0, last_q != 64, ... */
+#define MI_ERR_SHAPE (-2)         /* d != 128, N out of range, Hq % Hkv != 0, last_q != 64, ... */
 #define MI_ERR_WORKSPACE (-3)     /* workspace NULL, misaligned or smaller than required */
 #define MI_ERR_CUDA (-4)          /* a CUDA call or kernel launch failed */
 #define MI_ERR_INDEX (-5)         /* device status: index out of range or not strictly ascending */
@@ -146,7 +149,7 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
  * blocks by sigma[r, c] = mean(q rows of block r) . mean(k rows of block c)
  * (ties: lower c), and written to blk_idx.  With MI_IDX_GIVEN, blk_idx is read
  * (a row that is not ascending, exceeds r or has a value after -1 padding
- * sets MI_ERR_INDEX).  blk_idx: [n_heads, N/64, topk] int32 DEVICE array; each
+ * sets MI_ERR_INDEX).  blk_idx: [n_heads, ceil(N/64), topk] int32 DEVICE array; each
  * row ascending, padded with -1 after the last selected block.  Row q keeps j
  * iff j <= q and j/64 is selected for q/64.  block must be 64,
  * 1 <= topk <= MI_MAX_KV / 2.

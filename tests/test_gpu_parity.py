@@ -348,10 +348,12 @@ def test_argument_and_index_errors():
     N = 256
     x = _rand_inputs(2, 1, N, seed=4)
     q, k, v = _dev(x)
-    with pytest.raises(B.MIError) as e:
-        B.mi_dense_causal_attn(q[:, :200].contiguous(), k[:, :200].contiguous(),
-                               v[:, :200].contiguous())
-    assert e.value.code == B.MI_ERR_SHAPE
+    # a length beyond 2^21 is refused before any work (the tensors are not read)
+    out = torch.empty_like(q)
+    ws0 = torch.empty(256, dtype=torch.uint8, device=DEV)
+    rc = B.load().mi_dense_causal_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), 2, 1, (1 << 21) + 64, 128,
+                                       None, 2, out.data_ptr(), None, ws0.data_ptr(), 256, None)
+    assert rc == B.MI_ERR_SHAPE
     with pytest.raises(B.MIError) as e:
         B.mi_dense_causal_attn(q, k, v, heads=[0, 0])
     assert e.value.code == B.MI_ERR_ARG

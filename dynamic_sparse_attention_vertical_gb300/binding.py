@@ -46,6 +46,8 @@ SYMBOLS = (
     "mi_dense_causal_attn",
     "mi_layer_workspace_bytes",
     "mi_layer_attn",
+    "mi_layer_workspace_bytes_varlen",
+    "mi_layer_attn_varlen",
     "mi_read_status",
     "mi_strerror",
     "mi_debug_inject",
@@ -125,6 +127,10 @@ def load() -> ctypes.CDLL:
     lib.mi_layer_workspace_bytes.restype = S
     lib.mi_layer_attn.argtypes = [P, P, P, I, I, I, I, P, P, P, P, S, P]
     lib.mi_layer_attn.restype = I
+    lib.mi_layer_workspace_bytes_varlen.argtypes = [I, I, P, I, P]
+    lib.mi_layer_workspace_bytes_varlen.restype = S
+    lib.mi_layer_attn_varlen.argtypes = [P, P, P, I, I, I, I, P, I, P, P, P, P, S, P]
+    lib.mi_layer_attn_varlen.restype = I
     lib.mi_read_status.argtypes = [P, P]
     lib.mi_read_status.restype = I
     lib.mi_debug_inject.argtypes = [I, ctypes.c_uint64]
@@ -350,4 +356,40 @@ def mi_layer_attn(q, k, v, cfg, out=None, lse=None, workspace=None, stream=None)
     rc = load().mi_layer_attn(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, N, d, ctypes.cast(arr, ctypes.c_void_p),
                               _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "mi_layer_attn")
+    return out
+
+
+def _cu_array(cu_seqlens):
+    vals = [int(c) for c in cu_seqlens]
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    return arr, len(vals) - 1
+
+
+def mi_layer_workspace_bytes_varlen(Hq: int, Hkv: int, cu_seqlens, cfg) -> int:
+    arr = _cfg_array(cfg, Hq)
+    cu, n = _cu_array(cu_seqlens)
+    return int(load().mi_layer_workspace_bytes_varlen(Hq, Hkv, ctypes.cast(cu, ctypes.c_void_p), n,
+                                                      ctypes.cast(arr, ctypes.c_void_p)))
+
+
+def mi_layer_attn_varlen(q, k, v, cu_seqlens, cfg, out=None, lse=None, workspace=None, stream=None):
+    """A packed batch: sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 of every head."""
+    _check_qkv(q, k, v, out)
+    Hq, total, d = q.shape
+    Hkv = k.shape[0]
+    arr = _cfg_array(cfg, Hq)
+    cu, n = _cu_array(cu_seqlens)
+    if out is None:
+        out = torch.zeros_like(q)
+    need = int(load().mi_layer_workspace_bytes_varlen(Hq, Hkv, ctypes.cast(cu, ctypes.c_void_p), n,
+                                                      ctypes.cast(arr, ctypes.c_void_p)))
+    if need == 0:
+        raise MIError(MI_ERR_ARG, "mi_layer_workspace_bytes_varlen")
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    if ws.numel() < need:
+        raise ValueError(f"workspace too small: {ws.numel()} < {need} bytes")
+    rc = load().mi_layer_attn_varlen(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, total, d,
+                                     ctypes.cast(cu, ctypes.c_void_p), n, ctypes.cast(arr, ctypes.c_void_p),
+                                     _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "mi_layer_attn_varlen")
     return out

@@ -45,9 +45,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [heads, N, 128] bf16 as a 3-D tensor (d, N, heads); box = 64 columns x box_rows
-// rows, 128-byte swizzle (one box row = 128 bytes).  Rows past N read as zero.
-int make_map(CUtensorMap* m, const void* base, int heads, int N, int box_rows) {
+// [heads, N, 128] bf16 as a 3-D tensor (d, N, heads), consecutive heads `ld` rows
+// apart (ld = N for a contiguous tensor; a sequence of a packed batch keeps the
+// batch's row count); box = 64 columns x box_rows rows, 128-byte swizzle (one box
+// row = 128 bytes).  Rows past N read as zero.
+int make_map(CUtensorMap* m, const void* base, int heads, int N, int box_rows, int64_t ld) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled is not available from the driver");
@@ -55,7 +57,7 @@ int make_map(CUtensorMap* m, const void* base, int heads, int N, int box_rows) {
   }
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(N) * kD * 2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(ld) * kD * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
@@ -68,16 +70,18 @@ int make_map(CUtensorMap* m, const void* base, int heads, int N, int box_rows) {
   return MI_OK;
 }
 
-// [heads, N, 128] bf16 as a 2-D tensor (d, heads * N) with a 64 x 1 box and
-// 128-byte swizzle: the map for tile::gather4 loads of scattered key rows.
-int make_rows_map(CUtensorMap* m, const void* base, int heads, int N) {
+// [heads, N, 128] bf16 (heads `ld` rows apart) as a 2-D tensor of rows
+// (d, (heads - 1) * ld + N) with a 64 x 1 box and 128-byte swizzle: the map for
+// tile::gather4 loads of scattered key rows (row g * ld + key).
+int make_rows_map(CUtensorMap* m, const void* base, int heads, int N, int64_t ld) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled is not available from the driver");
     return MI_ERR_CUDA;
   }
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
-                        static_cast<cuuint64_t>(heads) * static_cast<cuuint64_t>(N)};
+                        static_cast<cuuint64_t>(heads - 1) * static_cast<cuuint64_t>(ld) +
+                            static_cast<cuuint64_t>(N)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
   cuuint32_t box[2] = {64, 1};
   cuuint32_t es[2] = {1, 1};
@@ -230,16 +234,17 @@ int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, 
                   mi_bf16* out, float* lse, int* status, AttnArgs& a, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mkr, mvr;
   int rc;
-  if ((rc = make_map(&mq, q, Hq, N, kBM)) || (rc = make_map(&mk, k, Hkv, N, kBN)) ||
-      (rc = make_map(&mv, v, Hkv, N, kBN)))
+  if ((rc = make_map(&mq, q, Hq, N, kBM, N)) || (rc = make_map(&mk, k, Hkv, N, kBN, N)) ||
+      (rc = make_map(&mv, v, Hkv, N, kBN, N)))
     return rc;
   if (PAT == kPatVS) {  // gathered column tiles
-    if ((rc = make_rows_map(&mkr, k, Hkv, N)) || (rc = make_rows_map(&mvr, v, Hkv, N))) return rc;
+    if ((rc = make_rows_map(&mkr, k, Hkv, N, N)) || (rc = make_rows_map(&mvr, v, Hkv, N, N))) return rc;
   } else {
     mkr = mk;
     mvr = mv;
   }
   a.N = N;
+  a.ld = N;
   a.group = Hq / Hkv;
   a.scale_log2 = kScaleLog2;
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
@@ -263,9 +268,9 @@ int attn_preamble(const void* q, const void* k, const void* v, int Hq, int Hkv, 
 
 // Estimation of the listed heads (E1, E2, T1) into rows of ld_v / ld_s entries of
 // v_idx / s_idx; ws is an est_layout(heads.n, N) workspace.
-int est_run(const void* q, const void* k, int Hq, int Hkv, int N, const HeadList& heads, int k_v,
-            int k_s, int32_t* v_idx, int ld_v, int32_t* s_idx, int ld_s, char* ws, int* status,
-            cudaStream_t st) {
+int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, const HeadList& heads,
+            int k_v, int k_s, int32_t* v_idx, int ld_v, int32_t* s_idx, int ld_s, char* ws,
+            int* status, cudaStream_t st) {
   EstArgs a;
   memset(&a, 0, sizeof(a));
   a.heads = heads;
@@ -316,7 +321,7 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, const HeadList
 
   int rc;
   CUtensorMap mq, mk;
-  if ((rc = make_map(&mq, q, Hq, N, kLastQ)) || (rc = make_map(&mk, k, Hkv, N, kBN))) return rc;
+  if ((rc = make_map(&mq, q, Hq, N, kLastQ, ld)) || (rc = make_map(&mk, k, Hkv, N, kBN, ld))) return rc;
   const dim3 grid(np, L.NC);
   est_kernel<1><<<grid, 256, kEstSmem1, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 1"))) return rc;
@@ -347,7 +352,8 @@ struct LayerPlan {
   int max_vg = 0;
 };
 
-int layer_plan(const mi_head_cfg* cfg, int Hq, int N, LayerPlan* P) {
+// vs_as_dense: vertical-slash heads run dense (a sequence too short to estimate).
+int layer_plan(const mi_head_cfg* cfg, int Hq, int N, bool vs_as_dense, LayerPlan* P) {
   if (!cfg) return MI_ERR_ARG;
   int n_dense = 0;
   int16_t dense_h[MI_MAX_HEADS];
@@ -374,7 +380,8 @@ int layer_plan(const mi_head_cfg* cfg, int Hq, int N, LayerPlan* P) {
     }
     if (P->n_listed == MI_MAX_HEADS) return MI_ERR_ARG;
     ++P->n_listed;
-    if (c.pattern == MI_PAT_DENSE) dense_h[n_dense++] = static_cast<int16_t>(h);
+    if (c.pattern == MI_PAT_DENSE || (c.pattern == MI_PAT_VS && vs_as_dense))
+      dense_h[n_dense++] = static_cast<int16_t>(h);
   }
   if (P->n_listed == 0) return MI_ERR_ARG;
   int n = 0;
@@ -382,7 +389,7 @@ int layer_plan(const mi_head_cfg* cfg, int Hq, int N, LayerPlan* P) {
   for (int i = 0; i < n_dense; ++i) list(dense_h[i]);
   // vertical-slash heads, grouped by (k_v, k_s) in order of first appearance
   bool done[kMaxHq] = {};
-  for (int h = 0; h < Hq; ++h) {
+  for (int h = 0; h < Hq && !vs_as_dense; ++h) {
     if (cfg[h].pattern != MI_PAT_VS || done[h]) continue;
     const int kv = cfg[h].k_v, ks = cfg[h].k_s;
     P->vg_kv[P->n_vg] = kv;
@@ -445,6 +452,126 @@ LayerLayout layer_layout(const LayerPlan& P, int Hkv, int N) {
   return L;
 }
 
+// One layer over one sequence: q, k, v, out (and lse) point at the sequence's first
+// row, consecutive heads `ld` rows apart; ws / L / status from the caller.
+int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int N, int64_t ld,
+              const LayerPlan& P, mi_bf16* out, float* lse, char* ws, const LayerLayout& L,
+              int* status, cudaStream_t st) {
+  int rc;
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.heads = P.listed;
+  const int group = Hq / Hkv;
+  // vertical-slash heads: estimation per budget group, one index build
+  int32_t* vidx = reinterpret_cast<int32_t*>(ws + L.vidx);
+  int32_t* sidx = reinterpret_cast<int32_t*>(ws + L.sidx);
+  if (P.n_vs) {
+    for (int gi = 0; gi < P.n_vg; ++gi) {
+      HeadList hl;
+      hl.n = P.vg_start[gi + 1] - P.vg_start[gi];
+      for (int i = 0; i < hl.n; ++i) hl.h[i] = P.vs_head[P.vg_start[gi] + i];
+      const size_t r0 = P.vg_start[gi];
+      if ((rc = est_run(q, k, Hq, Hkv, N, ld, hl, P.vg_kv[gi], P.vg_ks[gi], vidx + r0 * P.KV, P.KV,
+                        sidx + r0 * P.KS, P.KS, ws + L.est, status, st)))
+        return rc;
+    }
+    const VsLayout V = vs_layout(P.n_vs, N);
+    char* vw = ws + L.vs;
+    VsIndexArgs ia;
+    ia.N = N;
+    ia.k_v = P.KV;
+    ia.k_s = P.KS;
+    ia.Nw = V.Nw;
+    ia.NT = V.NT;
+    ia.NTw = V.NTw;
+    ia.expanded = (P.vs_flags & MI_VS_BLOCK_EXPANDED) ? 1 : 0;
+    ia.v_idx = vidx;
+    ia.s_idx = sidx;
+    ia.offbits = reinterpret_cast<uint32_t*>(vw + V.offbits);
+    ia.colbits = reinterpret_cast<uint32_t*>(vw + V.colbits);
+    ia.dbits = reinterpret_cast<uint32_t*>(vw + V.dbits);
+    ia.dfull = reinterpret_cast<uint32_t*>(vw + V.dfull);
+    ia.dlist = reinterpret_cast<int*>(vw + V.dlist);
+    ia.dcount = reinterpret_cast<int*>(vw + V.dcount);
+    ia.status = status;
+    vs_index_kernel<<<P.n_vs, 512, 0, st>>>(ia);
+    if ((rc = launched("vertical-slash index build"))) return rc;
+    a.offbits = ia.offbits;
+    a.colbits = ia.colbits;
+    a.dbits = ia.dbits;
+    a.dfull = ia.dfull;
+    a.dlist = ia.dlist;
+    a.dcount = ia.dcount;
+    a.v_idx = vidx;
+    a.k_v = P.KV;
+    a.expand = ia.expanded;
+    a.Nw = V.Nw;
+    a.NT = V.NT;
+    a.NTw = V.NTw;
+  }
+  // block-sparse heads: pooling once, selection per top-k group
+  if (P.n_blk) {
+    const BlockLayout BL = block_layout(P.n_blk, Hkv, N);
+    char* bw = ws + L.blk;
+    float* qbar = reinterpret_cast<float*>(bw + BL.qbar);
+    float* kbar = reinterpret_cast<float*>(bw + BL.kbar);
+    int32_t* blk = reinterpret_cast<int32_t*>(ws + L.blkidx);
+    const int NB = cdiv(N, kBlk);
+    HeadList hb;
+    hb.n = P.n_blk;
+    for (int i = 0; i < P.n_blk; ++i) hb.h[i] = P.blk_head[i];
+    const int wq = P.n_blk * NB, wk = Hkv * NB;
+    block_pool_kernel<<<cdiv(wq, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), N, ld,
+                                                   P.n_blk, NB, hb, 1, qbar);
+    if ((rc = launched("block pooling (q)"))) return rc;
+    block_pool_kernel<<<cdiv(wk, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k), N, ld,
+                                                   Hkv, NB, hb, 0, kbar);
+    if ((rc = launched("block pooling (k)"))) return rc;
+    if ((rc = set_smem(reinterpret_cast<const void*>(block_select_kernel), 160 * 1024))) return rc;
+    for (int gi = 0; gi < P.n_bg; ++gi) {
+      HeadList hl;
+      const int s0 = P.bg_start[gi];
+      hl.n = P.bg_start[gi + 1] - s0;
+      for (int i = 0; i < hl.n; ++i) hl.h[i] = P.blk_head[s0 + i];
+      block_select_kernel<<<dim3(NB, hl.n), 256, sizeof(float) * NB, st>>>(
+          qbar + (size_t)s0 * NB * kD, kbar, NB, group, hl, P.bg_tk[gi], P.TK,
+          blk + (size_t)s0 * NB * P.TK);
+      if ((rc = launched("block selection"))) return rc;
+    }
+    a.blk_idx = blk;
+    a.topk = P.TK;
+  }
+  // A-shape heads: per-head sizes, passed in the kernel arguments
+  a.ash_n = P.n_ash;
+  for (int i = 0; i < 2 * P.n_ash; ++i) a.ash_pairs[i] = P.ash[i];
+  // listed order is dense, vertical-slash, block-sparse, A-shape
+  {
+    const int n_dense = P.listed.n - P.n_vs - P.n_blk - P.n_ash;
+    a.layer_base[kPatDense] = 0;
+    a.layer_base[kPatVS] = n_dense;
+    a.layer_base[kPatBlock] = n_dense + P.n_vs;
+    a.layer_base[kPatAShape] = n_dense + P.n_vs + P.n_blk;
+    a.layer_base[4] = P.listed.n;
+  }
+  // the attention of every listed head in one launch
+  CUtensorMap mq, mk, mv, mkr, mvr;
+  if ((rc = make_map(&mq, q, Hq, N, kBM, ld)) || (rc = make_map(&mk, k, Hkv, N, kBN, ld)) ||
+      (rc = make_map(&mv, v, Hkv, N, kBN, ld)) || (rc = make_rows_map(&mkr, k, Hkv, N, ld)) ||
+      (rc = make_rows_map(&mvr, v, Hkv, N, ld)))
+    return rc;
+  a.N = N;
+  a.ld = static_cast<int>(ld);
+  a.group = group;
+  a.scale_log2 = kScaleLog2;
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.status = status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.skip_q_load = g_fault_mode.load() == MI_FAULT_SKIP_Q_LOAD ? 1 : 0;
+  cudaError_t e = launch_attn_layer(mq, mk, mv, mkr, mvr, a, cdiv(N, kBM), st);
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, "layer attention kernel");
+}
+
 }  // namespace
 
 // ====================================================================== ABI ==
@@ -483,7 +610,7 @@ int mi_vs_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, i
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.status);
   if ((rc = zero_status(status, st))) return rc;
-  return est_run(q, k, Hq, Hkv, N, hl, k_v, k_s, v_idx, k_v, s_idx, k_s, ws, status, st);
+  return est_run(q, k, Hq, Hkv, N, N, hl, k_v, k_s, v_idx, k_v, s_idx, k_s, ws, status, st);
 }
 
 int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
@@ -560,10 +687,10 @@ int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
     float* qbar = reinterpret_cast<float*>(ws + L.qbar);
     float* kbar = reinterpret_cast<float*>(ws + L.kbar);
     const int wq = n_heads * NB, wk = Hkv * NB;
-    block_pool_kernel<<<cdiv(wq, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), N,
+    block_pool_kernel<<<cdiv(wq, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), N, N,
                                                    n_heads, NB, a.heads, 1, qbar);
     if ((rc = launched("block pooling (q)"))) return rc;
-    block_pool_kernel<<<cdiv(wk, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k), N,
+    block_pool_kernel<<<cdiv(wk, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k), N, N,
                                                    Hkv, NB, a.heads, 0, kbar);
     if ((rc = launched("block pooling (k)"))) return rc;
     static std::once_flag once;
@@ -617,7 +744,7 @@ int mi_dense_causal_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
 size_t mi_layer_workspace_bytes(int Hq, int Hkv, int N, const mi_head_cfg* cfg) {
   if (Hq <= 0 || Hkv <= 0 || N <= 0 || Hq > kMaxHq || Hq % Hkv != 0) return 0;
   LayerPlan P;
-  if (layer_plan(cfg, Hq, N, &P)) return 0;
+  if (layer_plan(cfg, Hq, N, false, &P)) return 0;
   return layer_layout(P, Hkv, N).total;
 }
 
@@ -632,125 +759,89 @@ int mi_layer_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, 
   if (d != kD) return MI_ERR_SHAPE;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq > kMaxHq) return MI_ERR_SHAPE;
   if (N < 1 || N > (1 << 21)) return MI_ERR_SHAPE;
-  if ((rc = layer_plan(cfg, Hq, N, &P))) return rc;
+  if ((rc = layer_plan(cfg, Hq, N, false, &P))) return rc;
+  if (P.n_vs && N < kLastQ) return MI_ERR_SHAPE;
   const LayerLayout L = layer_layout(P, Hkv, N);
   if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.status);
   if ((rc = zero_status(status, st))) return rc;
+  return layer_run(q, k, v, Hq, Hkv, N, N, P, out, lse, ws, L, status, st);
+}
 
-  AttnArgs a;
-  memset(&a, 0, sizeof(a));
-  a.heads = P.listed;
-  const int group = Hq / Hkv;
-  // vertical-slash heads: estimation per budget group, one index build
-  int32_t* vidx = reinterpret_cast<int32_t*>(ws + L.vidx);
-  int32_t* sidx = reinterpret_cast<int32_t*>(ws + L.sidx);
-  if (P.n_vs) {
-    for (int gi = 0; gi < P.n_vg; ++gi) {
-      HeadList hl;
-      hl.n = P.vg_start[gi + 1] - P.vg_start[gi];
-      for (int i = 0; i < hl.n; ++i) hl.h[i] = P.vs_head[P.vg_start[gi] + i];
-      const size_t r0 = P.vg_start[gi];
-      if ((rc = est_run(q, k, Hq, Hkv, N, hl, P.vg_kv[gi], P.vg_ks[gi], vidx + r0 * P.KV, P.KV,
-                        sidx + r0 * P.KS, P.KS, ws + L.est, status, st)))
-        return rc;
-    }
-    const VsLayout V = vs_layout(P.n_vs, N);
-    char* vw = ws + L.vs;
-    VsIndexArgs ia;
-    ia.N = N;
-    ia.k_v = P.KV;
-    ia.k_s = P.KS;
-    ia.Nw = V.Nw;
-    ia.NT = V.NT;
-    ia.NTw = V.NTw;
-    ia.expanded = (P.vs_flags & MI_VS_BLOCK_EXPANDED) ? 1 : 0;
-    ia.v_idx = vidx;
-    ia.s_idx = sidx;
-    ia.offbits = reinterpret_cast<uint32_t*>(vw + V.offbits);
-    ia.colbits = reinterpret_cast<uint32_t*>(vw + V.colbits);
-    ia.dbits = reinterpret_cast<uint32_t*>(vw + V.dbits);
-    ia.dfull = reinterpret_cast<uint32_t*>(vw + V.dfull);
-    ia.dlist = reinterpret_cast<int*>(vw + V.dlist);
-    ia.dcount = reinterpret_cast<int*>(vw + V.dcount);
-    ia.status = status;
-    vs_index_kernel<<<P.n_vs, 512, 0, st>>>(ia);
-    if ((rc = launched("vertical-slash index build"))) return rc;
-    a.offbits = ia.offbits;
-    a.colbits = ia.colbits;
-    a.dbits = ia.dbits;
-    a.dfull = ia.dfull;
-    a.dlist = ia.dlist;
-    a.dcount = ia.dcount;
-    a.v_idx = vidx;
-    a.k_v = P.KV;
-    a.expand = ia.expanded;
-    a.Nw = V.Nw;
-    a.NT = V.NT;
-    a.NTw = V.NTw;
+// Validates cu_seqlens and returns the longest sequence (0 on error).
+static int varlen_check(const int32_t* cu, int n_seqs, int total, int* n_max_long, int* n_max_short) {
+  if (!cu || n_seqs < 1 || cu[0] != 0 || cu[n_seqs] != total || total < 1) return 0;
+  int nmax = 0;
+  *n_max_long = 0;
+  *n_max_short = 0;
+  for (int b = 0; b < n_seqs; ++b) {
+    const int n = cu[b + 1] - cu[b];
+    if (n < 0 || n > (1 << 21)) return 0;
+    nmax = std::max(nmax, n);
+    if (n >= kLastQ) *n_max_long = std::max(*n_max_long, n);
+    else *n_max_short = std::max(*n_max_short, n);
   }
-  // block-sparse heads: pooling once, selection per top-k group
-  if (P.n_blk) {
-    const BlockLayout BL = block_layout(P.n_blk, Hkv, N);
-    char* bw = ws + L.blk;
-    float* qbar = reinterpret_cast<float*>(bw + BL.qbar);
-    float* kbar = reinterpret_cast<float*>(bw + BL.kbar);
-    int32_t* blk = reinterpret_cast<int32_t*>(ws + L.blkidx);
-    const int NB = cdiv(N, kBlk);
-    HeadList hb;
-    hb.n = P.n_blk;
-    for (int i = 0; i < P.n_blk; ++i) hb.h[i] = P.blk_head[i];
-    const int wq = P.n_blk * NB, wk = Hkv * NB;
-    block_pool_kernel<<<cdiv(wq, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(q), N,
-                                                   P.n_blk, NB, hb, 1, qbar);
-    if ((rc = launched("block pooling (q)"))) return rc;
-    block_pool_kernel<<<cdiv(wk, 8), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(k), N,
-                                                   Hkv, NB, hb, 0, kbar);
-    if ((rc = launched("block pooling (k)"))) return rc;
-    if ((rc = set_smem(reinterpret_cast<const void*>(block_select_kernel), 160 * 1024))) return rc;
-    for (int gi = 0; gi < P.n_bg; ++gi) {
-      HeadList hl;
-      const int s0 = P.bg_start[gi];
-      hl.n = P.bg_start[gi + 1] - s0;
-      for (int i = 0; i < hl.n; ++i) hl.h[i] = P.blk_head[s0 + i];
-      block_select_kernel<<<dim3(NB, hl.n), 256, sizeof(float) * NB, st>>>(
-          qbar + (size_t)s0 * NB * kD, kbar, NB, group, hl, P.bg_tk[gi], P.TK,
-          blk + (size_t)s0 * NB * P.TK);
-      if ((rc = launched("block selection"))) return rc;
-    }
-    a.blk_idx = blk;
-    a.topk = P.TK;
+  return nmax;
+}
+
+size_t mi_layer_workspace_bytes_varlen(int Hq, int Hkv, const int32_t* cu_seqlens, int n_seqs,
+                                       const mi_head_cfg* cfg) {
+  if (Hq <= 0 || Hkv <= 0 || Hq > kMaxHq || Hq % Hkv != 0 || !cu_seqlens || n_seqs < 1) return 0;
+  int nl, ns;
+  if (!varlen_check(cu_seqlens, n_seqs, cu_seqlens[n_seqs], &nl, &ns)) return 0;
+  LayerPlan Pl, Ps;
+  size_t need = 0;
+  if (nl) {
+    if (layer_plan(cfg, Hq, nl, false, &Pl)) return 0;
+    need = std::max(need, layer_layout(Pl, Hkv, nl).total);
   }
-  // A-shape heads: per-head sizes, passed in the kernel arguments
-  a.ash_n = P.n_ash;
-  for (int i = 0; i < 2 * P.n_ash; ++i) a.ash_pairs[i] = P.ash[i];
-  // listed order is dense, vertical-slash, block-sparse, A-shape
-  {
-    const int n_dense = P.listed.n - P.n_vs - P.n_blk - P.n_ash;
-    a.layer_base[kPatDense] = 0;
-    a.layer_base[kPatVS] = n_dense;
-    a.layer_base[kPatBlock] = n_dense + P.n_vs;
-    a.layer_base[kPatAShape] = n_dense + P.n_vs + P.n_blk;
-    a.layer_base[4] = P.listed.n;
+  if (ns) {
+    if (layer_plan(cfg, Hq, ns, true, &Ps)) return 0;
+    need = std::max(need, layer_layout(Ps, Hkv, ns).total);
   }
-  // the attention of every listed head in one launch
-  CUtensorMap mq, mk, mv, mkr, mvr;
-  if ((rc = make_map(&mq, q, Hq, N, kBM)) || (rc = make_map(&mk, k, Hkv, N, kBN)) ||
-      (rc = make_map(&mv, v, Hkv, N, kBN)) || (rc = make_rows_map(&mkr, k, Hkv, N)) ||
-      (rc = make_rows_map(&mvr, v, Hkv, N)))
-    return rc;
-  a.N = N;
-  a.group = group;
-  a.scale_log2 = kScaleLog2;
-  a.out = reinterpret_cast<__nv_bfloat16*>(out);
-  a.lse = lse;
-  a.status = status;
-  a.wait_limit_ns = g_wait_limit_ns.load();
-  a.skip_q_load = g_fault_mode.load() == MI_FAULT_SKIP_Q_LOAD ? 1 : 0;
-  cudaError_t e = launch_attn_layer(mq, mk, mv, mkr, mvr, a, cdiv(N, kBM), st);
-  return e == cudaSuccess ? MI_OK : cuda_fail(e, "layer attention kernel");
+  return need;
+}
+
+int mi_layer_attn_varlen(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
+                         int total, int d, const int32_t* cu_seqlens, int n_seqs,
+                         const mi_head_cfg* cfg, mi_bf16* out, float* lse, void* workspace,
+                         size_t ws_bytes, mi_stream_t stream) {
+  int rc = check_device();
+  if (rc) return rc;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return MI_ERR_ARG;
+  if (d != kD) return MI_ERR_SHAPE;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq > kMaxHq) return MI_ERR_SHAPE;
+  int nl, ns;
+  if (!cu_seqlens || n_seqs < 1 || !varlen_check(cu_seqlens, n_seqs, total, &nl, &ns)) return MI_ERR_ARG;
+  LayerPlan Pl, Ps;
+  size_t need = 0;
+  if (nl) {
+    if ((rc = layer_plan(cfg, Hq, nl, false, &Pl))) return rc;
+    need = std::max(need, layer_layout(Pl, Hkv, nl).total);
+  }
+  if (ns) {
+    if ((rc = layer_plan(cfg, Hq, ns, true, &Ps))) return rc;
+    need = std::max(need, layer_layout(Ps, Hkv, ns).total);
+  }
+  if ((rc = check_ws(workspace, ws_bytes, need))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);  // offset 0 of every layer layout
+  if ((rc = zero_status(status, st))) return rc;
+  for (int b = 0; b < n_seqs; ++b) {
+    const int n = cu_seqlens[b + 1] - cu_seqlens[b];
+    if (n == 0) continue;
+    const LayerPlan& P = (n >= kLastQ) ? Pl : Ps;
+    const LayerLayout L = layer_layout(P, Hkv, n);
+    const size_t row = static_cast<size_t>(cu_seqlens[b]);
+    if ((rc = layer_run(q + row * kD, k + row * kD, v + row * kD, Hq, Hkv, n, total, P,
+                        out + row * kD, lse ? lse + row : nullptr, ws, L, status, st)))
+      return rc;
+  }
+  return MI_OK;
 }
 
 int mi_debug_inject(int mode, uint64_t wait_limit_ns) {

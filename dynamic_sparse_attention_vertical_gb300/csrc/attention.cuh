@@ -38,6 +38,8 @@ enum Pattern : int { kPatDense = 0, kPatVS = 1, kPatBlock = 2, kPatAShape = 3 };
 
 struct AttnArgs {
   int N;
+  int ld;            // rows between consecutive heads of q, k, v, out and lse (N, or a
+                     // packed batch's token count)
   int group;         // Hq / Hkv
   float scale_log2;  // log2(e) / sqrt(d)
   __nv_bfloat16* out;
@@ -534,7 +536,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         // repeat its last column (their scores are masked)
         const int* cols = s.list + ref.t * kBN;
         const int last = min(kBN, s.n_list - ref.t * kBN) - 1;
-        const int base_row = g * a.N;
+        const int base_row = g * a.ld;
         if (lane_id() == 0) mbar_arrive_expect_tx(full, 2 * 16384);
         __syncwarp();
         const int l = lane_id();
@@ -657,7 +659,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
       tc_fence_after();
       const bool in_range = q < a.N;
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = a.out + ((size_t)h * a.N + q) * kD;
+      __nv_bfloat16* orow = a.out + ((size_t)h * a.ld + q) * kD;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float o[32];
@@ -678,7 +680,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         }
       }
       if (in_range && a.lse)
-        a.lse[(size_t)h * a.N + q] =
+        a.lse[(size_t)h * a.ld + q] =
             (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }

@@ -15,15 +15,16 @@ namespace mi {
 
 // Mean of 64 consecutive rows (of the rows left in a last, partial block), fp32:
 // one warp per (head, block); lane l owns dims 4l..4l+3 and adds the rows in
-// order.  Output head o reads source head heads.h[o] (use_list) or o.
-__global__ void block_pool_kernel(const __nv_bfloat16* src, int N, int n_out, int NB,
+// order.  Output head o reads source head heads.h[o] (use_list) or o; heads are
+// ld rows apart.
+__global__ void block_pool_kernel(const __nv_bfloat16* src, int N, int64_t ld, int n_out, int NB,
                                   HeadList heads, int use_list, float* out) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= n_out * NB) return;
   const int o = gw / NB, blk = gw - o * NB;
   const int h = use_list ? heads.h[o] : o;
-  const __nv_bfloat16* base = src + ((size_t)h * N + (size_t)blk * kBlk) * kD + lane * 4;
+  const __nv_bfloat16* base = src + ((size_t)h * ld + (size_t)blk * kBlk) * kD + lane * 4;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   const int rows = min(kBlk, N - blk * kBlk);
   for (int r = 0; r < rows; ++r) {

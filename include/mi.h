@@ -224,6 +224,28 @@ int mi_layer_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, 
                   size_t ws_bytes, mi_stream_t stream);
 
 /*
+ * A packed batch of sequences of any lengths (varlen), each through the layer
+ * call above with the same cfg.  q: [Hq, total, d], k and v: [Hkv, total, d],
+ * out: [Hq, total, d], lse (optional): [Hq, total]; sequence b holds tokens
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1 of every head and attends only to itself
+ * (its own causal prefix).  cu_seqlens: HOST array of n_seqs + 1 non-decreasing
+ * int32 with cu_seqlens[0] = 0 and cu_seqlens[n_seqs] = total; an empty
+ * sequence is skipped.  A sequence shorter than 64 tokens (too short for the
+ * estimation, which scores the last 64 queries) runs its vertical-slash heads
+ * dense.  The sequences run one after another on the stream, sharing one
+ * workspace of mi_layer_workspace_bytes_varlen(...) bytes and its status word.
+ * Errors: a malformed cu_seqlens or a sequence longer than 2^21 returns
+ * MI_ERR_ARG; otherwise as mi_layer_attn.
+ */
+size_t mi_layer_workspace_bytes_varlen(int Hq, int Hkv, const int32_t* cu_seqlens, int n_seqs,
+                                       const mi_head_cfg* cfg);
+
+int mi_layer_attn_varlen(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
+                         int total, int d, const int32_t* cu_seqlens, int n_seqs,
+                         const mi_head_cfg* cfg, mi_bf16* out, float* lse, void* workspace,
+                         size_t ws_bytes, mi_stream_t stream);
+
+/*
  * mi_vs_estimate_noalloc: mi_vs_estimate for callers that cannot allocate device
  * memory (for instance an engine whose memory pool owns the whole device, or a
  * plugin running where cudaMalloc is not allowed).  The pages have no

@@ -73,3 +73,14 @@ def test_layer_workspace_sizes_need_no_gpu(lib):
     mixed_flags = list(cfg)
     mixed_flags[2] = H.vs(128, 16, expanded=True)
     assert B.mi_layer_workspace_bytes(8, 2, 4096, mixed_flags) == 0
+
+
+def test_varlen_workspace_sizes_need_no_gpu(lib):
+    H = B.HeadCfg
+    cfg = [H.vs(64, 32), H.block(8), H.ashape(128, 512), H.dense()]
+    n = B.mi_layer_workspace_bytes_varlen(4, 2, [0, 1000, 1081, 3581], cfg)
+    assert n > 0 and n % 256 == 0
+    # the workspace is that of the longest sequence
+    assert n == B.mi_layer_workspace_bytes(4, 2, 2500, cfg)
+    for bad in ([1, 1000], [0, 500, 400], [0]):
+        assert B.mi_layer_workspace_bytes_varlen(4, 2, bad, cfg) == 0

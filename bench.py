@@ -411,12 +411,10 @@ def main():
         if dist is not None:
             dist.barrier()
 
+    from dynamic_sparse_attention_vertical_gb300.shard import reduce_max
+
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dist, device="cuda")
 
     from dynamic_sparse_attention_vertical_gb300 import binding as B
     B.load()

@@ -146,16 +146,6 @@ __device__ __forceinline__ uint32_t range_bits(int base, int lo, int hi) {
   return up & ~((1u << lo) - 1u);
 }
 
-// 32 bits of `bits` starting at bit position `pos` (may be negative: zeros).
-__device__ __forceinline__ uint32_t load_bits32(const uint32_t* bits, int pos, int nbits) {
-  if (pos >= nbits || pos + 32 <= 0) return 0u;
-  const int w = pos >> 5;  // arithmetic shift: floor
-  const int sh = pos & 31;
-  const uint32_t lo = (w >= 0 && (w << 5) < nbits) ? __ldg(bits + w) : 0u;
-  const uint32_t hi = ((w + 1) >= 0 && ((w + 1) << 5) < nbits) ? __ldg(bits + w + 1) : 0u;
-  return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
-}
-
 // Raw words a row's keep-mask depends on, loaded a tile ahead of their use.
 struct MaskRaw {
   TileRef ref;
@@ -398,34 +388,7 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
   __syncthreads();
 }
 
-// ------------------------------------------------------------- loaders ----
-
 // ---------------------------------------------------------------- kernel ----
-
-// One pass over the 128 S values of this thread's row, 64 columns per TMEM
-// wait.  With `apply` (which must be the same for the whole warp: the tensor
-// memory store is warp-collective), masked elements read as -inf and the masked
-// values are written back, so a later pass reads them with no mask work.
-template <class F>
-__device__ __forceinline__ void for_s_halves(uint32_t taddr, const uint32_t mk[4], bool apply, F f) {
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
-    float x[64];
-    tmem_ld64(taddr + hh * 64, x);
-    if (apply) {
-      const uint32_t w0 = hh ? mk[2] : mk[0];
-      const uint32_t w1 = hh ? mk[3] : mk[1];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        x[e] = ((w0 >> e) & 1u) ? x[e] : -INFINITY;
-        x[32 + e] = ((w1 >> e) & 1u) ? x[32 + e] : -INFINITY;
-      }
-      tmem_st32(taddr + hh * 64, x);
-      tmem_st32(taddr + hh * 64 + 32, x + 32);
-    }
-    f(hh, x);
-  }
-}
 
 // The engine for one CTA: row block r of head h, whose pattern arrays sit at
 // slot n.  Called by the per-pattern kernels and by the layer kernel.

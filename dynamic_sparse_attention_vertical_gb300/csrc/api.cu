@@ -237,7 +237,7 @@ int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, 
   if ((rc = make_map(&mq, q, Hq, N, kBM, N)) || (rc = make_map(&mk, k, Hkv, N, kBN, N)) ||
       (rc = make_map(&mv, v, Hkv, N, kBN, N)))
     return rc;
-  if (PAT == kPatVS) {  // gathered column tiles
+  if (is_vs(PAT)) {  // gathered column tiles
     if ((rc = make_rows_map(&mkr, k, Hkv, N, N)) || (rc = make_rows_map(&mvr, v, Hkv, N, N))) return rc;
   } else {
     mkr = mk;
@@ -663,7 +663,8 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
   a.Nw = L.Nw;
   a.NT = L.NT;
   a.NTw = L.NTw;
-  return run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
+  return expanded ? run_attention<kPatVSExp>(q, k, v, Hq, Hkv, N, out, lse, status, a, st)
+                  : run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
 }
 
 int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,

@@ -34,7 +34,10 @@
 
 namespace mi {
 
-enum Pattern : int { kPatDense = 0, kPatVS = 1, kPatBlock = 2, kPatAShape = 3 };
+enum Pattern : int { kPatDense = 0, kPatVS = 1, kPatBlock = 2, kPatAShape = 3, kPatVSExp = 4 };
+// kPatVSExp is the vertical-slash engine with block-expanded slashes: a
+// compile-time variant of kPatVS (its heads use the kPatVS slots and arrays).
+__host__ __device__ constexpr bool is_vs(int p) { return p == kPatVS || p == kPatVSExp; }
 
 struct AttnArgs {
   int N;
@@ -57,7 +60,7 @@ struct AttnArgs {
   const int* dcount;        // [n_heads]
   const int* v_idx;         // [n_heads, k_v]
   int k_v;
-  int expand;               // block-expanded slash mode
+  int expand;               // block-expanded slashes: the host launches the kPatVSExp engine
   int Nw, NT, NTw;
   // block-sparse
   const int* blk_idx;  // [n_heads, ceil(N/64), topk]
@@ -113,7 +116,7 @@ __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a,
   TileRef ref{0, 0, 0xF};
   if (PAT == kPatDense) {
     ref.t = i;
-  } else if (PAT == kPatVS) {
+  } else if (is_vs(PAT)) {
     if (i < s.n_contig) {
       if (s.has_t0 && i == 0) {
         ref.t = 0;
@@ -162,11 +165,11 @@ __device__ __forceinline__ MaskRaw mask_fetch(const AttnSmem& s, const AttnArgs&
   m.ref = ref;
   m.base = 0;
   m.whole = false;
-  if (PAT == kPatVS && ref.kind == 0) {
+  if (is_vs(PAT) && ref.kind == 0) {
     const int d = r - ref.t;
     m.whole = d > 0 && ((s.dfull[d >> 5] >> (d & 31)) & 1u);
   }
-  if (PAT == kPatVS && ref.kind == 0 && !m.whole && a.expand) {
+  if (PAT == kPatVSExp && ref.kind == 0 && !m.whole) {
     // the 64-block distances 2d-1 .. 2d+1 of the tile's four sub-blocks
     const uint32_t* off = a.offbits + (size_t)n * a.Nw;
     const uint32_t* col = a.colbits + (size_t)n * a.Nw;
@@ -200,7 +203,7 @@ template <int PAT>
 __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a, int r,
                                             const MaskRaw& m, int q, uint32_t out[4]) {
   const TileRef& ref = m.ref;
-  if (PAT == kPatVS && ref.kind == 1) {
+  if (is_vs(PAT) && ref.kind == 1) {
     const int valid = min(kBN, s.n_list - ref.t * kBN);
 #pragma unroll
     for (int w = 0; w < 4; ++w) out[w] = range_bits(32 * w, 0, valid);
@@ -210,13 +213,13 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
   if (PAT == kPatDense) {
 #pragma unroll
     for (int w = 0; w < 4; ++w) out[w] = 0xFFFFFFFFu;
-  } else if (PAT == kPatVS) {
+  } else if (is_vs(PAT)) {
     if (m.whole) {
 #pragma unroll
       for (int w = 0; w < 4; ++w) out[w] = 0xFFFFFFFFu;
       return;  // never the diagonal tile (distance > 0)
     }
-    if (a.expand) {
+    if (PAT == kPatVSExp) {
       // sub-block (row half rh, key half kh) sits at 64-block distance 2d + rh - kh
       const int d = r - ref.t;
       const int rh = (q >> 6) & 1;
@@ -316,7 +319,7 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
       const int n_sink = min(cdiv(s.ash_init, kBN), t_lo);
       s.n_tiles = n_sink + (r - t_lo + 1);
     }
-  } else if (PAT == kPatVS) {
+  } else if (is_vs(PAT)) {
     // contiguous tiles: r - delta for the tile distances delta <= r, plus tile 0.
     // All threads count the distances <= r in parallel (independent loads).
     const int* dl = a.dlist + (size_t)n * a.NT;
@@ -425,7 +428,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
   if (tid == 160) {
     tma_prefetch_map(&map_k);
     tma_prefetch_map(&map_v);
-    if (PAT == kPatVS) {
+    if (is_vs(PAT)) {
       tma_prefetch_map(&map_kr);
       tma_prefetch_map(&map_vr);
     }
@@ -553,14 +556,15 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
       tc_fence_after();
       uint32_t mk[4];
       mask_finish<PAT>(s, a, r, raw, q, mk);
-      // tcgen05.st is warp-collective: a warp masks in place if any of its rows
-      // needs it (for whole rows the mask is all ones)
-      const bool full = (mk[0] & mk[1] & mk[2] & mk[3]) == 0xFFFFFFFFu;
       // the row of S in registers: one tensor-memory read per tile
       float x[128];
       tmem_ld64(s_addr, x);
       tmem_ld64(s_addr + 64, x + 64);
-      if (!full) {
+      // masked keys read as -inf.  A row of an exact vertical-slash tile is
+      // almost never kept whole, so those tiles select without a per-row branch
+      // (measured: the branch cost more than it saved); the other patterns and
+      // the block-expanded slashes skip the rows whose mask is all ones.
+      if (PAT == kPatVS || (mk[0] & mk[1] & mk[2] & mk[3]) != 0xFFFFFFFFu) {
 #pragma unroll
         for (int e = 0; e < 128; ++e) x[e] = ((mk[e >> 5] >> (e & 31)) & 1u) ? x[e] : -INFINITY;
       }
@@ -674,7 +678,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 
 namespace mi {
 
-// Host launcher, explicitly instantiated in attn_kernels_*.cu so that the four
+// Host launcher, explicitly instantiated in attn_kernels_*.cu so that the
 // pattern variants compile in parallel.
 template <int PAT>
 cudaError_t launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,

@@ -16,7 +16,9 @@ __device__ __noinline__ void attn_body_call(uint8_t* smem_raw, const CUtensorMap
 // (dense, vertical-slash, block-sparse, A-shape in turn), blockIdx.x the row block
 // counted from the last, so the heavier patterns start first and the lighter
 // ones fill the end.  The slot is blockIdx.y minus a per-pattern constant, which
-// the compiler can recompute instead of holding a register for it.
+// the compiler can recompute instead of holding a register for it.  VSP is the
+// vertical-slash engine: exact (kPatVS) or block-expanded slashes (kPatVSExp).
+template <int VSP>
 __global__ void __launch_bounds__(kAttnThreads, 2)
 attn_layer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_kr,
@@ -28,7 +30,7 @@ attn_layer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   const int h = a.heads.h[y];
   if (y >= a.layer_base[kPatVS] && y < a.layer_base[kPatBlock]) {
     // the heaviest pattern of a layer: inlined, with the kernel's own registers
-    attn_body<kPatVS>(smem_raw, map_q, map_k, map_v, map_kr, map_vr, a, r, y - a.layer_base[kPatVS], h);
+    attn_body<VSP>(smem_raw, map_q, map_k, map_v, map_kr, map_vr, a, r, y - a.layer_base[kPatVS], h);
   } else if (y < a.layer_base[kPatVS]) {
     attn_body_call<kPatDense>(smem_raw, map_q, map_k, map_v, map_kr, map_vr, a, r, y - a.layer_base[kPatDense], h);
   } else if (y < a.layer_base[kPatAShape]) {
@@ -42,11 +44,19 @@ attn_layer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 cudaError_t launch_attn_layer(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                               const CUtensorMap& mkr, const CUtensorMap& mvr, const AttnArgs& a,
                               int n_row_blocks, cudaStream_t st) {
-  static cudaError_t attr = cudaFuncSetAttribute(attn_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static cudaError_t attr = cudaFuncSetAttribute(attn_layer_kernel<kPatVS>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(kAttnSmemBytes));
+  static cudaError_t attr_x = cudaFuncSetAttribute(attn_layer_kernel<kPatVSExp>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(kAttnSmemBytes));
   if (attr != cudaSuccess) return attr;
-  attn_layer_kernel<<<dim3(n_row_blocks, a.heads.n), kAttnThreads, kAttnSmemBytes, st>>>(mq, mk, mv, mkr, mvr,
-                                                                                        a);
+  if (attr_x != cudaSuccess) return attr_x;
+  const dim3 grid(n_row_blocks, a.heads.n);
+  if (a.expand)
+    attn_layer_kernel<kPatVSExp><<<grid, kAttnThreads, kAttnSmemBytes, st>>>(mq, mk, mv, mkr, mvr, a);
+  else
+    attn_layer_kernel<kPatVS><<<grid, kAttnThreads, kAttnSmemBytes, st>>>(mq, mk, mv, mkr, mvr, a);
   return cudaGetLastError();
 }
 

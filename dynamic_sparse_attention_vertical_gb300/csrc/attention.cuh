@@ -84,7 +84,11 @@ struct AttnSmem {
   int list[MI_MAX_KV];  // VS: residual columns; block: (tile << 4) | sub-block mask
   int scan[192];
   uint32_t dfull[512];  // VS: the head's whole-tile distance bits (N <= 2^21)
+  // VS: keep-masks of two tiles in flight (row i: bit c of word c / 32 keeps
+  // key c of the tile), built by the loader warp; tile t uses stage t & 1
+  uint32_t vmask[2][kBM][4];
   uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, mma_done;
+  uint64_t m_full[2];  // VS: mask stage written (the 32 loader lanes arrive)
   uint32_t tmem;
   int abort;
   int n_list;    // entries in list
@@ -99,6 +103,8 @@ struct AttnSmem {
 constexpr int kAttnThreads = 192;
 constexpr size_t kAttnSmemBytes = sizeof(AttnSmem) + 1024;
 static_assert(sizeof(AttnArgs) + 5 * sizeof(CUtensorMap) <= 4096, "attention kernel parameters exceed 4 KB");
+// two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(2 * (kAttnSmemBytes + 1024) <= 228 * 1024, "two attention CTAs must fit on one SM");
 constexpr uint32_t kTmemCols = 256;  // S (and P over it) at 0, O at 128
 constexpr uint32_t kTmemO = 128;
 
@@ -198,6 +204,66 @@ __device__ __forceinline__ MaskRaw mask_fetch(const AttnSmem& s, const AttnArgs&
   return m;
 }
 
+// A loader lane's raw words for the four rows q0 + 32 i (i = 0..3) of a
+// vertical-slash tile.  Exact slashes: the rows' offset windows start 32 bits
+// apart, so eight offset-bitmap words cover all four (row i uses off[i..i+4]).
+// Block-expanded slashes: the words depend on the tile alone.
+struct VsRaw4 {
+  TileRef ref;
+  bool whole;
+  int base;         // exact: first offset bit of row q0's window; expanded: first 64-block distance
+  uint32_t off[8];
+  uint32_t col[4];
+};
+
+template <int PAT>
+__device__ __forceinline__ VsRaw4 vs_fetch4(const AttnSmem& s, const AttnArgs& a, int n, int r,
+                                            const TileRef& ref, int q0) {
+  VsRaw4 m;
+  m.ref = ref;
+  m.base = 0;
+  m.whole = false;
+  if (ref.kind == 0) {
+    const int d = r - ref.t;
+    m.whole = d > 0 && ((s.dfull[d >> 5] >> (d & 31)) & 1u);
+  }
+  if (ref.kind != 0 || m.whole) return m;
+  const uint32_t* off = a.offbits + (size_t)n * a.Nw;
+  const uint32_t* col = a.colbits + (size_t)n * a.Nw;
+  const int j0 = ref.t * kBN;
+  if (PAT == kPatVSExp) {
+    const int e0 = max(2 * (r - ref.t) - 1, 0);
+    m.base = e0;
+    m.off[0] = ldg_ahead(off + (e0 >> 5));
+    m.off[1] = ldg_ahead(off + min((e0 >> 5) + 1, a.Nw - 1));
+  } else {
+    m.base = q0 - j0 - 127;
+    const int w0 = m.base >> 5;  // floor; >= -4
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int wi = w0 + i;  // the words of rows q0 .. q0 + 96, each < Nw as for one row
+      m.off[i] = ldg_ahead(off + max(wi, 0));
+      if (wi < 0) m.off[i] = 0u;
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < 4; ++w) m.col[w] = ldg_ahead(col + (j0 >> 5) + w);
+  return m;
+}
+
+// The raw words of row q0 + 32 i out of a lane's four-row fetch.
+__device__ __forceinline__ MaskRaw vs_row_raw(const VsRaw4& m, int i, bool expanded) {
+  MaskRaw r;
+  r.ref = m.ref;
+  r.whole = m.whole;
+  r.base = expanded ? m.base : m.base + 32 * i;
+#pragma unroll
+  for (int k = 0; k < 5; ++k) r.off[k] = expanded ? m.off[k] : m.off[i + k];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) r.col[w] = m.col[w];
+  return r;
+}
+
 // Keep-mask of query row q over the 128 keys of tile m.ref (bit c of out[c/32]).
 template <int PAT>
 __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a, int r,
@@ -248,7 +314,7 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const int k = 3 - w;
-      const uint32_t win = sh ? ((m.off[k] >> sh) | (m.off[k + 1] << (32 - sh))) : m.off[k];
+      const uint32_t win = __funnelshift_r(m.off[k], m.off[k + 1], sh);
       out[w] = __brev(win) | m.col[w];
     }
     if (j0 == 0) {  // the first 64 keys
@@ -415,6 +481,8 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     mbar_init(&s.p_full, 128);
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.mma_done, 1);
+    mbar_init(&s.m_full[0], 32);
+    mbar_init(&s.m_full[1], 32);
     s.abort = 0;
     s.has_t0 = 1;
     s.ash_init = a.ash_n ? a.ash_pairs[2 * n] : a.n_init;
@@ -513,11 +581,30 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         tma_gather4(buf[1] + 512 * l, rows_map, full, 64, y[0], y[1], y[2], y[3]);
       }
     };
+    // vertical-slash: this warp also builds the keep-masks, lane l for rows
+    // l + 32 i; their raw words are loaded a tile ahead of their use
+    const int q0 = r * kBM + static_cast<int>(lane_id());
+    VsRaw4 raw_next;
+    if (is_vs(PAT) && T > 0) raw_next = vs_fetch4<PAT>(s, a, n, r, ref_next, q0);
     for (int t = 0; t < T; ++t) {
       const TileRef ref = ref_next;
+      VsRaw4 raw;
+      if (is_vs(PAT)) raw = raw_next;
       if (t + 1 < T) ref_next = tile_at<PAT>(s, a, n, r, t + 1);
       if (t >= 1 && !mbar_wait_warp(&s.k_empty, (t - 1) & 1, abort, lim)) break;
       load(ref, &map_k, &map_kr, &s.k_full, s.k);
+      if (is_vs(PAT)) {
+        // stage t & 1 was last read by the softmax of tile t - 2, which ended
+        // before P.V of t - 2 and hence before S of t - 1 (waited for above)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t mk[4];
+          mask_finish<PAT>(s, a, r, vs_row_raw(raw, i, PAT == kPatVSExp), q0 + 32 * i, mk);
+          *reinterpret_cast<uint4*>(&s.vmask[t & 1][lane_id() + 32 * i][0]) = make_uint4(mk[0], mk[1], mk[2], mk[3]);
+        }
+        mbar_arrive(&s.m_full[t & 1]);
+        if (t + 1 < T) raw_next = vs_fetch4<PAT>(s, a, n, r, ref_next, q0);
+      }
       if (t >= 1 && !mbar_wait_warp(&s.v_empty, (t - 1) & 1, abort, lim)) {
         issued = -(t + 1);  // K of tile t issued, V not
         break;
@@ -543,19 +630,37 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     const float sl = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // mask words are fetched one tile ahead and tile references two tiles ahead,
-    // so their global loads overlap the wait for S
-    TileRef ref_next2 = (T > 1) ? tile_at<PAT>(s, a, n, r, 1) : TileRef{0, 0, 0};
-    MaskRaw raw_next = mask_fetch<PAT>(s, a, n, r, (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0}, q);
+    // other patterns: mask words are fetched one tile ahead and tile references
+    // two tiles ahead, so their global loads overlap the wait for S;
+    // vertical-slash masks come ready-made from the loader warp
+    TileRef ref_next2{0, 0, 0};
+    MaskRaw raw_next{};
+    if (!is_vs(PAT)) {
+      ref_next2 = (T > 1) ? tile_at<PAT>(s, a, n, r, 1) : TileRef{0, 0, 0};
+      raw_next = mask_fetch<PAT>(s, a, n, r, (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0}, q);
+    }
     for (int t = 0; t < T; ++t) {
-      const MaskRaw raw = raw_next;
-      if (t + 1 < T) raw_next = mask_fetch<PAT>(s, a, n, r, ref_next2, q);
-      if (t + 2 < T) ref_next2 = tile_at<PAT>(s, a, n, r, t + 2);
-      ok = mbar_wait_warp(&s.s_full, t & 1, abort, lim);
-      if (!ok) break;
-      tc_fence_after();
       uint32_t mk[4];
-      mask_finish<PAT>(s, a, r, raw, q, mk);
+      if (is_vs(PAT)) {
+        ok = mbar_wait_warp(&s.m_full[t & 1], (t >> 1) & 1, abort, lim);
+        if (!ok) break;
+        const uint4 m4 = *reinterpret_cast<const uint4*>(&s.vmask[t & 1][row][0]);
+        mk[0] = m4.x;
+        mk[1] = m4.y;
+        mk[2] = m4.z;
+        mk[3] = m4.w;
+        ok = mbar_wait_warp(&s.s_full, t & 1, abort, lim);
+        if (!ok) break;
+        tc_fence_after();
+      } else {
+        const MaskRaw raw = raw_next;
+        if (t + 1 < T) raw_next = mask_fetch<PAT>(s, a, n, r, ref_next2, q);
+        if (t + 2 < T) ref_next2 = tile_at<PAT>(s, a, n, r, t + 2);
+        ok = mbar_wait_warp(&s.s_full, t & 1, abort, lim);
+        if (!ok) break;
+        tc_fence_after();
+        mask_finish<PAT>(s, a, r, raw, q, mk);
+      }
       // the row of S in registers: one tensor-memory read per tile
       float x[128];
       tmem_ld64(s_addr, x);

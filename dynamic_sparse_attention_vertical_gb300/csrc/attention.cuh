@@ -346,6 +346,56 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
   }
 }
 
+// Keep-masks of a loader lane's four rows q0 + 32 i of a vertical-slash tile.
+// Off the diagonal tile the rows share their words: with exact slashes row i's
+// word w is the reversed offset window E[i + 3 - w] (windows 32 bits apart), with
+// block-expanded slashes rows 0-1 and 2-3 fall in the same 64-row half.  Whole,
+// gathered and diagonal tiles take the per-row path.
+template <int PAT>
+__device__ __forceinline__ void vs_masks4(const AttnSmem& s, const AttnArgs& a, int r, const VsRaw4& m,
+                                          int q0, uint32_t out[4][4]) {
+  const TileRef& ref = m.ref;
+  if (ref.kind == 0 && !m.whole && ref.t != r) {
+    if (PAT == kPatVSExp) {
+      const int d = r - ref.t;  // >= 1
+      const uint64_t win = (static_cast<uint64_t>(m.off[1]) << 32) | m.off[0];
+      const int b = m.base & ~31;
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        const uint32_t lo = ((win >> (2 * d + rh - b)) & 1u) ? 0xFFFFFFFFu : 0u;
+        const uint32_t hi = ((win >> (2 * d + rh - 1 - b)) & 1u) ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+        for (int i = 2 * rh; i < 2 * rh + 2; ++i) {
+          out[i][0] = lo | m.col[0];
+          out[i][1] = lo | m.col[1];
+          out[i][2] = hi | m.col[2];
+          out[i][3] = hi | m.col[3];
+        }
+      }
+    } else {
+      const int sh = m.base & 31;
+      uint32_t e[7];
+#pragma unroll
+      for (int k = 0; k < 7; ++k) e[k] = __brev(__funnelshift_r(m.off[k], m.off[k + 1], sh));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) out[i][w] = e[i + 3 - w] | m.col[w];
+      }
+    }
+    if (ref.t == 0) {  // the first 64 keys
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        out[i][0] = 0xFFFFFFFFu;
+        out[i][1] = 0xFFFFFFFFu;
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) mask_finish<PAT>(s, a, r, vs_row_raw(m, i, PAT == kPatVSExp), q0 + 32 * i, out[i]);
+}
+
 // ------------------------------------------------------------- prologue ----
 
 // Block-wide exclusive scan of one int per thread (192 threads); returns the
@@ -596,12 +646,12 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
       if (is_vs(PAT)) {
         // stage t & 1 was last read by the softmax of tile t - 2, which ended
         // before P.V of t - 2 and hence before S of t - 1 (waited for above)
+        uint32_t mk[4][4];
+        vs_masks4<PAT>(s, a, r, raw, q0, mk);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t mk[4];
-          mask_finish<PAT>(s, a, r, vs_row_raw(raw, i, PAT == kPatVSExp), q0 + 32 * i, mk);
-          *reinterpret_cast<uint4*>(&s.vmask[t & 1][lane_id() + 32 * i][0]) = make_uint4(mk[0], mk[1], mk[2], mk[3]);
-        }
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(&s.vmask[t & 1][lane_id() + 32 * i][0]) =
+              make_uint4(mk[i][0], mk[i][1], mk[i][2], mk[i][3]);
         mbar_arrive(&s.m_full[t & 1]);
         if (t + 1 < T) raw_next = vs_fetch4<PAT>(s, a, n, r, ref_next, q0);
       }

@@ -14,16 +14,19 @@
 // Warp roles (192 threads, two CTAs per SM, up to 168 registers per thread):
 //   warps 0-3   softmax: thread t owns query row t (TMEM lane t)
 //   warp 4      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warp 5      Q (once), then K and V tiles (TMA tiles, or TMA gather4)
+//   warp 5      Q (once), then K and V tiles (TMA tiles, or TMA gather4);
+//               for vertical-slash heads also the rows' keep-masks
 //
 // Tensor memory (256 columns): S = Q K^T (fp32, columns 0-127) and O (fp32,
 // columns 128-255).  Per tile: the MMA warp issues S = Q K_i^T; the softmax
 // warps read their S row into registers once (mask, row maximum, exp2, pack), and write
 // P_i = exp2(x - m) as bf16 pairs over the S columns they have consumed; the
-// MMA warp then issues O += P_i V_i with P read from tensor memory.  The
+// MMA warp then issues O += P_i V_i with P read from tensor memory, the first
+// 64 keys as soon as their half of P is stored (unless O is being rescaled in
+// this tile), the other 64 once all of P is.  The
 // running maximum moves (and O is rescaled in tensor memory) only when a
 // tile's maximum exceeds it by more than 8 (log2 units), so P stays below 2^8.
-// Shared memory holds one Q tile and one K and one V stage (about 105 KB), so
+// Shared memory holds one Q tile and one K and one V stage (about 112 KB), so
 // two CTAs share an SM and one CTA's softmax overlaps the other's MMAs.
 // Every mbarrier wait is bounded; on a timeout the CTA stops issuing work,
 // waits for what it already issued, frees TMEM and records MI_ERR_TIMEOUT.
@@ -88,6 +91,7 @@ struct AttnSmem {
   // key c of the tile), built by the loader warp; tile t uses stage t & 1
   uint32_t vmask[2][kBM][4];
   uint64_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, mma_done;
+  uint64_t p_half;     // P of the first 64 keys stored (128 softmax threads arrive)
   uint64_t m_full[2];  // VS: mask stage written (the 32 loader lanes arrive)
   uint32_t tmem;
   int abort;
@@ -529,6 +533,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     mbar_init(&s.v_empty, 1);
     mbar_init(&s.s_full, 1);
     mbar_init(&s.p_full, 128);
+    mbar_init(&s.p_half, 128);
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.mma_done, 1);
     mbar_init(&s.m_full[0], 32);
@@ -585,11 +590,19 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         }
         umma_commit(&s.s_full);
         umma_commit(&s.k_empty);
-        ok = mbar_wait(&s.p_full, t & 1, abort, lim) && mbar_wait(&s.v_full, t & 1, abort, lim);
+        ok = mbar_wait(&s.p_half, t & 1, abort, lim) && mbar_wait(&s.v_full, t & 1, abort, lim);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = sdesc_sw128(smem_u32(s.v[0]) + kk * 2048, 16384, 1024);
+          umma_bf16_ts(tmem + kTmemO, tmem + kk * 8, bd, id_pv, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        ok = mbar_wait(&s.p_full, t & 1, abort, lim);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 4; kk < 8; ++kk) {
           const uint64_t bd = sdesc_sw128(smem_u32(s.v[0]) + kk * 2048, 16384, 1024);
           umma_bf16_ts(tmem + kTmemO, tmem + kk * 8, bd, id_pv, (t > 0 || kk > 0) ? 1u : 0u);
         }
@@ -745,6 +758,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
       // P = exp2(x * sl - m) as bf16 pairs over the consumed S columns
       float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      const bool resc = __any_sync(0xffffffffu, rescale_o);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
@@ -757,11 +771,15 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
           pk[e] = *reinterpret_cast<uint32_t*>(&bb);
         }
         tmem_st32u(s_addr + hh * 32, pk);
+        if (hh == 0 && !resc) {  // P.V of these keys can start now
+          tc_fence_before();
+          mbar_arrive(&s.p_half);
+        }
       }
       // O holds P.V of tiles < t (that P.V completed before S of tile t was
       // written); it is rescaled after P is stored, when the row is dead
       // and its registers are free
-      if (__any_sync(0xffffffffu, rescale_o)) {  // tcgen05.ld/st are warp-collective
+      if (resc) {  // tcgen05.ld/st are warp-collective
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float o[32];
@@ -773,6 +791,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
       }
       l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       tc_fence_before();
+      if (resc) mbar_arrive(&s.p_half);
       mbar_arrive(&s.p_full);
     }
     // epilogue: O / l

@@ -188,6 +188,28 @@ class Layer:
         if ev:
             ev[4].record()
 
+    def step_group(self, hs):
+        """The hot path for the q-heads in ``hs`` only (a KV group or several): the same calls as
+        step() on a subset of the heads, writing their rows of the index buffers and of out."""
+        B, w = self.B, self.w
+        vs = [h for h in self.vs if h in hs]
+        blk = [h for h in self.blk if h in hs]
+        ash = [h for h in self.ash if h in hs]
+        if vs:
+            i0 = self.vs.index(vs[0])
+            vi, si = self.v_idx[i0:i0 + len(vs)], self.s_idx[i0:i0 + len(vs)]
+            B.mi_vs_estimate(self.q, self.k, heads=vs, k_v=w["k_v"], k_s=w["k_s"], v_idx=vi, s_idx=si,
+                             workspace=self.ws_est)
+            B.mi_vs_sparse_attn(self.q, self.k, self.v, vi, si, heads=vs, out=self.out, workspace=self.ws_vs,
+                                expanded=self.expanded)
+        if blk:
+            j0 = self.blk.index(blk[0])
+            B.mi_block_sparse_attn(self.q, self.k, self.v, topk=w["topk"], heads=blk,
+                                   blk_idx=self.blk_idx[j0:j0 + len(blk)], out=self.out, workspace=self.ws_blk)
+        if ash:
+            B.mi_ashape_attn(self.q, self.k, self.v, n_init=w["n_init"], window=w["window"], heads=ash,
+                             out=self.out, workspace=self.ws_ash)
+
     def dense(self):
         self.B.mi_dense_causal_attn(self.q, self.k, self.v, out=self.out, workspace=self.ws_dense)
 
@@ -251,11 +273,16 @@ class Layer:
 TRAFFIC_BYTES = {("mixed-128k", "literal"): 2.41e9 + 0.824e9}
 
 
-def e2e_pipelined(B, w, L, K, barrier):
+def e2e_pipelined(B, w, L, K, barrier, kv_per_group=2):
     """K layer steps end to end: Q/K/V from pinned host memory in, O back to pinned host memory,
-    every copy inside the CUDA-event-timed region.  Two device buffer sets let step i+1's
-    input copy and step i's output copy (each on its own copy stream) overlap step i's compute.
-    Returns (ms per step, host-to-device bytes per step, device-to-host bytes per step)."""
+    every copy inside the CUDA-event-timed region.
+
+    Two device buffer sets let step i+1's input copy and step i's output copy (each on a copy
+    stream of its own) overlap step i's compute.  The first step, whose inputs nothing can hide,
+    and the last, whose output nothing can hide, run head group by head group (``kv_per_group``
+    KV heads and their q-heads): group j computes while group j+1's inputs arrive, and its output
+    leaves while group j+1 computes.  Returns (ms per step, host-to-device bytes per step,
+    device-to-host bytes per step)."""
     qh, kh, vh = (t.cpu().pin_memory() for t in (L.q, L.k, L.v))
     ohs = [torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory() for _ in range(2)]
     L2 = Layer(B, w, torch.empty_like(L.q), torch.empty_like(L.k), torch.empty_like(L.v))
@@ -263,47 +290,71 @@ def e2e_pipelined(B, w, L, K, barrier):
     main = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event(enable_timing=False)
+    Hq, Hkv = w["Hq"], w["Hkv"]
+    gq = Hq // Hkv
+    groups = [(g0, min(Hkv, g0 + kv_per_group)) for g0 in range(0, Hkv, kv_per_group)]
 
     def run(n_steps):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(main)
-        comp = [None, None]   # compute of the last step that used each buffer
-        out_done = [None, None]  # its output copy
+        comp = [None, None]      # compute of the last step that used each buffer set
+        out_done = [[], []]      # its output copies
         s_in.wait_event(start)
         s_out.wait_event(start)
 
-        def load(Lb):
+        def load(Lb, parts):
+            """Input copies of the (KV-head range) parts, one event per part."""
+            evs = []
             with torch.cuda.stream(s_in):
-                Lb.q.copy_(qh, non_blocking=True)
-                Lb.k.copy_(kh, non_blocking=True)
-                Lb.v.copy_(vh, non_blocking=True)
-                e = ev()
-                e.record(s_in)
-            return e
+                for g0, g1 in parts:
+                    Lb.k[g0:g1].copy_(kh[g0:g1], non_blocking=True)
+                    Lb.v[g0:g1].copy_(vh[g0:g1], non_blocking=True)
+                    Lb.q[g0 * gq:g1 * gq].copy_(qh[g0 * gq:g1 * gq], non_blocking=True)
+                    e = ev()
+                    e.record(s_in)
+                    evs.append(e)
+            return evs
 
-        loaded = load(bufs[0])
+        def store(Lb, b, h0, h1, after):
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(after)
+                ohs[b][h0:h1].copy_(Lb.out[h0:h1], non_blocking=True)
+                e = ev()
+                e.record(s_out)
+                out_done[b].append(e)
+
+        loaded = load(bufs[0], groups)
         for i in range(n_steps):
             b = i % 2
             Lb = bufs[b]
-            main.wait_event(loaded)
-            if out_done[b] is not None:
-                main.wait_event(out_done[b])  # the output copy of step i-2 has read this buffer's O
-            Lb.step()
+            for e in out_done[b]:
+                main.wait_event(e)  # the output copies of step i-2 have read this buffer's O
+            out_done[b] = []
+            grouped = i == 0 or i == n_steps - 1
+            if grouped:
+                for (g0, g1), e in zip(groups, loaded):
+                    main.wait_event(e)
+                    Lb.step_group(set(range(g0 * gq, g1 * gq)))
+                    if i == n_steps - 1:
+                        c = ev()
+                        c.record(main)
+                        store(Lb, b, g0 * gq, g1 * gq, c)
+            else:
+                for e in loaded:
+                    main.wait_event(e)
+                Lb.step()
             comp[b] = ev()
             comp[b].record(main)
             if i + 1 < n_steps:
                 nb = 1 - b
                 if comp[nb] is not None:
                     s_in.wait_event(comp[nb])  # step i-1 is done with the other buffer's inputs
-                loaded = load(bufs[nb])
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(comp[b])
-                ohs[b].copy_(Lb.out, non_blocking=True)
-                out_done[b] = ev()
-                out_done[b].record(s_out)
-        main.wait_event(out_done[(n_steps - 1) % 2])
-        if n_steps > 1:
-            main.wait_event(out_done[(n_steps - 2) % 2])
+                loaded = load(bufs[nb], groups if i + 1 == n_steps - 1 else [(0, Hkv)])
+            if i != n_steps - 1:
+                store(Lb, b, 0, Hq, comp[b])
+        for b in (0, 1):
+            for e in out_done[b]:
+                main.wait_event(e)
         end.record(main)
         torch.cuda.synchronize()
         return start.elapsed_time(end) / n_steps
@@ -567,7 +618,9 @@ def main():
                 e2e = {"value": ems / world, "unit": "ms/layer", "h2d_bytes_per_step": h2d_bytes,
                        "d2h_bytes_per_step": d2h_bytes,
                        "overlap": "two device buffer sets: step i+1's host-to-device copy and step i's "
-                                  "device-to-host read run on copy streams while step i computes"}
+                                  "device-to-host read run on copy streams while step i computes; the first "
+                                  "and last steps run by groups of 2 KV heads, so that their copies overlap "
+                                  "the other groups' compute"}
             if not args.no_cpu and rank == 0 and world == 1:
                 v_ms, desc = oracle_sample(w, x, 256, np.random.default_rng(1))
                 cpu = {"value": v_ms, "unit": "ms/layer", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",

@@ -159,7 +159,9 @@ __device__ __forceinline__ uint32_t range_bits(int base, int lo, int hi) {
   return up & ~((1u << lo) - 1u);
 }
 
-// Raw words a row's keep-mask depends on, loaded a tile ahead of their use.
+// The words a row's keep-mask is built from.  Vertical-slash rows get theirs
+// from the loader warp's four-row fetch (vs_fetch4 / vs_row_raw); the other
+// patterns' masks depend on the tile reference alone.
 struct MaskRaw {
   TileRef ref;
   bool whole;        // VS: the tile is kept whole (no mask words needed)
@@ -168,43 +170,14 @@ struct MaskRaw {
   uint32_t col[4];   // VS: column-bitmap words of the tile's keys
 };
 
+// Dense, block-sparse and A-shape tiles: the reference is all a mask needs.
 template <int PAT>
-__device__ __forceinline__ MaskRaw mask_fetch(const AttnSmem& s, const AttnArgs& a, int n, int r,
-                                              const TileRef& ref, int q) {
+__device__ __forceinline__ MaskRaw mask_fetch(const TileRef& ref) {
+  static_assert(!is_vs(PAT), "vertical-slash masks are built by the loader warp");
   MaskRaw m;
   m.ref = ref;
   m.base = 0;
   m.whole = false;
-  if (is_vs(PAT) && ref.kind == 0) {
-    const int d = r - ref.t;
-    m.whole = d > 0 && ((s.dfull[d >> 5] >> (d & 31)) & 1u);
-  }
-  if (PAT == kPatVSExp && ref.kind == 0 && !m.whole) {
-    // the 64-block distances 2d-1 .. 2d+1 of the tile's four sub-blocks
-    const uint32_t* off = a.offbits + (size_t)n * a.Nw;
-    const uint32_t* col = a.colbits + (size_t)n * a.Nw;
-    const int j0 = ref.t * kBN;
-    const int e0 = max(2 * (r - ref.t) - 1, 0);
-    m.base = e0;
-    m.off[0] = ldg_ahead(off + (e0 >> 5));
-    m.off[1] = ldg_ahead(off + min((e0 >> 5) + 1, a.Nw - 1));
-#pragma unroll
-    for (int w = 0; w < 4; ++w) m.col[w] = ldg_ahead(col + (j0 >> 5) + w);
-  } else if (PAT == kPatVS && ref.kind == 0 && !m.whole) {
-    const uint32_t* off = a.offbits + (size_t)n * a.Nw;
-    const uint32_t* col = a.colbits + (size_t)n * a.Nw;
-    const int j0 = ref.t * kBN;
-    m.base = q - j0 - 127;
-    const int w0 = m.base >> 5;  // floor; >= -4
-#pragma unroll
-    for (int i = 0; i < 5; ++i) {
-      const int wi = w0 + i;  // < Nw: q - j0 < NT * 128
-      m.off[i] = ldg_ahead(off + max(wi, 0));
-      if (wi < 0) m.off[i] = 0u;
-    }
-#pragma unroll
-    for (int w = 0; w < 4; ++w) m.col[w] = ldg_ahead(col + (j0 >> 5) + w);
-  }
   return m;
 }
 
@@ -693,18 +666,17 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     const float sl = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // other patterns: mask words are fetched one tile ahead and tile references
-    // two tiles ahead, so their global loads overlap the wait for S;
+    // other patterns: tile references are read one and two tiles ahead;
     // vertical-slash masks come ready-made from the loader warp
     TileRef ref_next2{0, 0, 0};
     MaskRaw raw_next{};
-    if (!is_vs(PAT)) {
+    if constexpr (!is_vs(PAT)) {
       ref_next2 = (T > 1) ? tile_at<PAT>(s, a, n, r, 1) : TileRef{0, 0, 0};
-      raw_next = mask_fetch<PAT>(s, a, n, r, (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0}, q);
+      raw_next = mask_fetch<PAT>((T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0});
     }
     for (int t = 0; t < T; ++t) {
       uint32_t mk[4];
-      if (is_vs(PAT)) {
+      if constexpr (is_vs(PAT)) {
         ok = mbar_wait_warp(&s.m_full[t & 1], (t >> 1) & 1, abort, lim);
         if (!ok) break;
         const uint4 m4 = *reinterpret_cast<const uint4*>(&s.vmask[t & 1][row][0]);
@@ -717,7 +689,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         tc_fence_after();
       } else {
         const MaskRaw raw = raw_next;
-        if (t + 1 < T) raw_next = mask_fetch<PAT>(s, a, n, r, ref_next2, q);
+        if (t + 1 < T) raw_next = mask_fetch<PAT>(ref_next2);
         if (t + 2 < T) ref_next2 = tile_at<PAT>(s, a, n, r, t + 2);
         ok = mbar_wait_warp(&s.s_full, t & 1, abort, lim);
         if (!ok) break;

@@ -114,10 +114,11 @@ static_assert(2 * (kAttnSmemBytes + 1024) <= 228 * 1024, "two attention CTAs mus
 constexpr uint32_t kTmemCols = 256;  // S (and P over it) at 0, O at 128
 constexpr uint32_t kTmemO = 128;
 // P is stored in NQ chunks of keys and P.V of a chunk starts as soon as it is
-// stored: four for vertical-slash tiles (measured 5 % faster there), two for the
-// others (four cost dense 2.6 %)
+// stored: four for the sparse patterns (measured: vertical-slash 5 %, A-shape
+// 5 %, block-sparse 2 % faster than two; eight were slower), two for dense
+// (four cost it 2.6 %)
 template <int PAT>
-constexpr int kPChunks = is_vs(PAT) ? 4 : 2;
+constexpr int kPChunks = PAT == kPatDense ? 2 : 4;
 
 // ------------------------------------------------------------ tile list ----
 

@@ -456,38 +456,45 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
       s.n_tiles = s.n_contig + cdiv(total, kBN);
     }
   } else {  // block-sparse: union of the two 64-row halves' selected blocks, as 128-key tiles
-    if (tid == 0) {
-      const int NB = cdiv(a.N, kBlk);
-      const int* b0 = a.blk_idx + ((size_t)n * NB + 2 * r) * a.topk;
-      const bool has1 = (2 * r + 1) < NB;
-      const int* b1 = b0 + a.topk;
-      int i0 = 0, i1 = 0, cnt = 0;
-      auto valid = [&](const int* b, int i, int row) {
-        if (i >= a.topk) return false;
-        const int c = __ldg(b + i);
-        return c >= 0 && c <= row;
-      };
-      while (true) {
-        const bool v0 = valid(b0, i0, 2 * r);
-        const bool v1 = has1 && valid(b1, i1, 2 * r + 1);
-        if (!v0 && !v1) break;
-        const int c0 = v0 ? __ldg(b0 + i0) : 0x7FFFFFFF;
-        const int c1 = v1 ? __ldg(b1 + i1) : 0x7FFFFFFF;
-        const int t = min(c0, c1) >> 1;
-        int sub = 0;
-        while (valid(b0, i0, 2 * r) && (__ldg(b0 + i0) >> 1) == t) {
-          sub |= 1 << (__ldg(b0 + i0) & 1);
-          ++i0;
-        }
-        while (has1 && valid(b1, i1, 2 * r + 1) && (__ldg(b1 + i1) >> 1) == t) {
-          sub |= 4 << (__ldg(b1 + i1) & 1);
-          ++i1;
-        }
-        if (cnt < MI_MAX_KV) s.list[cnt++] = (t << 4) | sub;
+    // Each selected block sets its bit in its tile's 4-bit sub-block mask (bit =
+    // row half * 2 + key half), one byte per tile, kept in the V buffer, which
+    // the loads only fill after this prologue; the nonzero tiles are then
+    // compacted in order.  All threads take part: the lists are read once, in
+    // parallel, instead of by a serial merge of dependent loads.
+    uint32_t* subw = reinterpret_cast<uint32_t*>(&s.v[0][0]);  // tiles 0..r, <= 16 KB
+    const int nw = (r + 4) / 4;
+    for (int w = tid; w < nw; w += 192) subw[w] = 0u;
+    __syncthreads();
+    const int NB = cdiv(a.N, kBlk);
+    const int* b0 = a.blk_idx + ((size_t)n * NB + 2 * r) * a.topk;  // row half 1 follows at + topk
+    const int nsel = ((2 * r + 1) < NB) ? 2 * a.topk : a.topk;
+    for (int i = tid; i < nsel; i += 192) {
+      const int hf = (i >= a.topk) ? 1 : 0;
+      const int c = __ldg(b0 + i);
+      if (c >= 0 && c <= 2 * r + hf) {
+        const int t = c >> 1;
+        atomicOr(&subw[t >> 2], (1u << ((c & 1) + 2 * hf)) << ((t & 3) * 8));
       }
-      s.n_list = cnt;
-      s.n_tiles = cnt;
     }
+    __syncthreads();
+    const int per = cdiv(r + 1, 192);
+    const int t0 = min(tid * per, r + 1), t1 = min(t0 + per, r + 1);
+    int cnt = 0;
+    for (int t = t0; t < t1; ++t) cnt += ((subw[t >> 2] >> ((t & 3) * 8)) & 0xFu) ? 1 : 0;
+    int total;
+    int pos = block_excl_scan(cnt, s.scan, &total);
+    for (int t = t0; t < t1; ++t) {
+      const uint32_t sub = (subw[t >> 2] >> ((t & 3) * 8)) & 0xFu;
+      if (sub != 0u) {
+        if (pos < MI_MAX_KV) s.list[pos] = (t << 4) | static_cast<int>(sub);
+        ++pos;
+      }
+    }
+    if (tid == 0) {
+      s.n_list = min(total, MI_MAX_KV);
+      s.n_tiles = s.n_list;
+    }
+    fence_proxy_async_smem();  // generic writes to the V buffer before its TMA loads
   }
   __syncthreads();
 }

@@ -441,16 +441,22 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
     // residual columns: selected keys in tiles 1..r-1 that no contiguous tile covers
     const int* vi = a.v_idx + (size_t)n * a.k_v;
     const uint32_t* db = a.dbits + (size_t)n * a.NTw;
+    // each thread's columns are loaded at once (independent loads, then their
+    // bitmap words), kept in registers and written after the scan
+    constexpr int kPer = (MI_MAX_KV + 191) / 192;
     const int per = cdiv(a.k_v, 192);
     const int beg = min(tid * per, a.k_v), end = min(beg + per, a.k_v);
-    int cnt = 0;
-    for (int e = beg; e < end; ++e) cnt += residual_column(__ldg(vi + e), a.N, r, db) ? 1 : 0;
+    int jv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) jv[u] = (beg + u < end) ? __ldg(vi + beg + u) : -1;
+    uint32_t keep = 0u;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) keep |= (residual_column(jv[u], a.N, r, db) ? 1u : 0u) << u;
     int total;
-    int pos = block_excl_scan(cnt, s.scan, &total);
-    for (int e = beg; e < end; ++e) {
-      const int j = __ldg(vi + e);
-      if (residual_column(j, a.N, r, db)) s.list[pos++] = j;
-    }
+    int pos = block_excl_scan(__popc(keep), s.scan, &total);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      if ((keep >> u) & 1u) s.list[pos++] = jv[u];
     if (tid == 0) {
       s.n_list = total;
       s.n_tiles = s.n_contig + cdiv(total, kBN);

@@ -34,6 +34,7 @@ MI_OP_ASHAPE_ATTN = 4
 MI_OP_DENSE_CAUSAL_ATTN = 5
 MI_IDX_GIVEN = 1
 MI_VS_BLOCK_EXPANDED = 1
+MI_MAX_KV = 2048  # largest vertical budget; block-sparse top-k is at most half of it
 
 # every entry point of include/mi.h
 SYMBOLS = (

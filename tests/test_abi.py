@@ -84,3 +84,16 @@ def test_varlen_workspace_sizes_need_no_gpu(lib):
     assert n == B.mi_layer_workspace_bytes(4, 2, 2500, cfg)
     for bad in ([1, 1000], [0, 500, 400], [0]):
         assert B.mi_layer_workspace_bytes_varlen(4, 2, bad, cfg) == 0
+
+
+def test_binding_constants_match_the_header():
+    """Every MI_* integer constant the binding mirrors has the header's value."""
+    with open(os.path.join(ROOT, "include", "mi.h")) as f:
+        text = f.read()
+    defined = {m.group(1): int(m.group(2))
+               for m in re.finditer(r"^#define\s+(MI_\w+)\s+\(?(-?\d+)\)?", text, re.M)}
+    mirrored = {n: getattr(B, n) for n in dir(B) if n.startswith("MI_") and isinstance(getattr(B, n), int)}
+    common = sorted(set(defined) & set(mirrored))
+    assert "MI_MAX_KV" in common and "MI_VS_BLOCK_EXPANDED" in common
+    for n in common:
+        assert mirrored[n] == defined[n], n

@@ -206,3 +206,30 @@ def test_largest_accepted_length_2m():
     ref = _check_vs_rows(x, 0, vi[0], si[0], rows, "2m")
     assert_close(out[0][torch.as_tensor(rows, device=DEV)].float().cpu().numpy(), ref, "vs 2M head 0")
     _free(x, v_idx, s_idx, out)
+
+
+def test_block_sparse_largest_topk_128k_sampled():
+    """Block-sparse at the largest accepted top-k (MI_MAX_KV / 2 blocks per 64-row
+    block) on 128K tokens: a late row block's two halves select up to 2048 blocks, so
+    the CTA's list can hold every 128-key tile below the diagonal.  Sampled selections
+    (up to ties at the top-k boundary) and sampled rows against the oracle."""
+    N, Hq, Hkv, topk = 131072, 2, 1, B.MI_MAX_KV // 2
+    x = I.literal_inputs(Hq, Hkv, N, n_cols=8, n_offsets=4, seed=91)
+    q, k, v = x.q.to(DEV), x.k.to(DEV), x.v.to(DEV)
+    out, blk = B.mi_block_sparse_attn(q, k, v, topk=topk)
+    torch.cuda.synchronize()
+    bl = blk.cpu().numpy()
+    o = out.float().cpu().numpy()
+    rng = np.random.default_rng(9)
+    for h in range(Hq):
+        sig = O.block_scores(x.q[h], x.k[0])
+        for r in list(rng.integers(0, N // 64, size=24)) + [N // 64 - 1, N // 64 - 2]:
+            got = bl[h, r][bl[h, r] >= 0]
+            kk = min(topk, r + 1)
+            band_agree(got, O.topk_sorted(sig[r, : r + 1], kk), sig[r, : r + 1], kk, rel_band=1e-3)
+        sel = [row[row >= 0] for row in bl[h]]
+        rows = sample_rows(N, rng, n_random=16, blocks=1)
+        ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], rows,
+                                  lambda r: O.block_sparse_mask_rows(N, r, sel), chunk=32)
+        assert_close(o[h][rows], ref, f"block head {h} topk {topk}")
+    _free(x, q, k, v, out, blk)

@@ -233,3 +233,28 @@ def test_block_sparse_largest_topk_128k_sampled():
                                   lambda r: O.block_sparse_mask_rows(N, r, sel), chunk=32)
         assert_close(o[h][rows], ref, f"block head {h} topk {topk}")
     _free(x, q, k, v, out, blk)
+
+
+@pytest.mark.parametrize("expanded", [False, True])
+def test_vs_largest_vertical_budget_128k_sampled(expanded):
+    """The largest accepted vertical budget (MI_MAX_KV columns) with 8192 diagonals on
+    128K tokens: a late row block carries up to 16 gathered column tiles after its
+    contiguous ones.  Sampled rows against the oracle with the selected indices."""
+    N, Hq, Hkv = 131072, 2, 1
+    k_v, k_s = B.MI_MAX_KV, 8192
+    x = I.literal_inputs(Hq, Hkv, N, n_cols=24, n_offsets=8, seed=93)
+    q, k, v = x.q.to(DEV), x.k.to(DEV), x.v.to(DEV)
+    vi, si = B.mi_vs_estimate(q, k, k_v=k_v, k_s=k_s)
+    out = B.mi_vs_sparse_attn(q, k, v, vi, si, expanded=expanded)
+    torch.cuda.synchronize()
+    vi_all, si_all = vi.cpu().numpy(), si.cpu().numpy()
+    o = out.float().cpu().numpy()
+    rng = np.random.default_rng(11)
+    for h in range(Hq):
+        rows = sample_rows(N, rng, n_random=16, blocks=1)
+        vv, ss = vi_all[h][vi_all[h] >= 0], si_all[h][si_all[h] >= 0]
+        mask = (lambda r: O.vs_expanded_mask_rows(N, r, vv, ss)) if expanded else \
+            (lambda r: O.vs_mask_rows(N, r, vv, ss))
+        ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], rows, mask, chunk=32)
+        assert_close(o[h][rows], ref, f"vs head {h} k_v {k_v} expanded {expanded}")
+    _free(x, q, k, v, out, vi, si)

@@ -19,15 +19,15 @@
 //
 // Tensor memory (256 columns): S = Q K^T (fp32, columns 0-127) and O (fp32,
 // columns 128-255).  Per tile: the MMA warp issues S = Q K_i^T; the softmax
-// warps read their S row into registers once (mask, row maximum, exp2, pack), and write
-// P_i = exp2(x - m) as bf16 pairs over the S columns they have consumed; the
-// MMA warp then issues O += P_i V_i with P read from tensor memory, chunk by
-// chunk of keys as soon as each chunk of P is stored (unless O is being
-// rescaled in this tile).  The
-// running maximum moves (and O is rescaled in tensor memory) only when a
-// tile's maximum exceeds it by more than 8 (log2 units), so P stays below 2^8.
-// Shared memory holds one Q tile and one K and one V stage (about 112 KB), so
-// two CTAs share an SM and one CTA's softmax overlaps the other's MMAs.
+// warps read their S row into registers once (mask, row maximum, exp2, pack)
+// and write P_i = exp2(x - m) as bf16 pairs over the S columns they have
+// consumed; the MMA warp issues O += P_i V_i with P read from tensor memory,
+// chunk of keys by chunk as soon as each chunk of P is stored (unless O is
+// being rescaled in this tile).  The running maximum moves (and O is rescaled
+// in tensor memory) only when a tile's maximum exceeds it by more than 8 (log2
+// units), so P stays below 2^8.  Shared memory holds one Q tile and one K and
+// one V stage (about 112 KB), so two CTAs share an SM and one CTA's softmax
+// overlaps the other's MMAs.
 // Every mbarrier wait is bounded; on a timeout the CTA stops issuing work,
 // waits for what it already issued, frees TMEM and records MI_ERR_TIMEOUT.
 #pragma once

@@ -166,8 +166,7 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       float x[128];
       if (ok) {
         tc_fence_after();
-        tmem_ld64(tmem + lane_base + b * 128, x);
-        tmem_ld64(tmem + lane_base + b * 128 + 64, x + 64);
+        tmem_ld128(tmem + lane_base + b * 128, x);
         tc_fence_before();
         mbar_arrive(&s.s_empty[b]);
       } else {

@@ -270,7 +270,7 @@ class Layer:
 
 # DRAM bytes (read + write) of one vertical-slash attention launch, from a one-pass ncu capture of
 # this kernel version (profiles/attn_vs_mixed-128k_dram.md); None where no capture was taken.
-TRAFFIC_BYTES = {("mixed-128k", "literal"): 2.38e9 + 0.788e9}
+TRAFFIC_BYTES = {("mixed-128k", "literal"): 2.38e9 + 0.787e9}
 
 
 def e2e_pipelined(B, w, L, K, barrier, kv_per_group=2):

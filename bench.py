@@ -268,9 +268,27 @@ class Layer:
         return ({k2: 4 * F.D * v2 for k2, v2 in alg.items()}, {k2: F.TILE_FLOPS * v2 for k2, v2 in tiles.items()})
 
 
-# DRAM bytes (read + write) of one vertical-slash attention launch, from a one-pass ncu capture of
-# this kernel version (profiles/attn_vs_mixed-128k_dram.md); None where no capture was taken.
-TRAFFIC_BYTES = {("mixed-128k", "literal"): 2.38e9 + 0.787e9}
+# DRAM bytes (read + write) of one vertical-slash attention launch from a one-pass ncu capture,
+# with the SHA-256 of the kernel sources it was taken on.  The figure is reported only while
+# those sources are unchanged (kernel_sources_sha256() at run time); otherwise traffic is null.
+TRAFFIC = {}
+KERNEL_SOURCES = ("attention.cuh", "ptx.cuh", "common.cuh", "vs_index.cuh", "attn_launch.cuh")
+
+
+def kernel_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dynamic_sparse_attention_vertical_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_bytes(workload, variant):
+    rec = TRAFFIC.get((workload, variant))
+    if rec and rec["sources_sha256"] == kernel_sources_sha256():
+        return rec["bytes"]
+    return None
 
 
 def e2e_pipelined(B, w, L, K, barrier, kv_per_group=2):
@@ -393,6 +411,11 @@ def timed(fn, K, events_per_step=0):
 
 # -------------------------------------------------------------- CPU oracle ----
 
+# attention rows the oracle evaluates per timed sample, in both CPU legs (the product run's
+# cpu_baseline and --impl reference)
+ORACLE_SAMPLE_ROWS = 128
+
+
 def oracle_sample(w, x, rows_per_sample, rng):
     """Time the oracle on one vertical-slash head: full estimation + sampled attention rows.
 
@@ -419,6 +442,67 @@ def oracle_sample(w, x, rows_per_sample, rng):
     return ms, desc
 
 
+def _oracle_estimate_task(t):
+    """Worker: full estimation of one vertical-slash head -> (v_idx, s_idx)."""
+    import oracle as O
+    qh, kh, k_v, k_s = t
+    vi, si, _, _ = O.vs_estimate(qh, kh, 64, k_v, k_s)
+    return vi, si
+
+
+def _oracle_rows_task(t):
+    """Worker: attention of one head over a range of rows under its vertical-slash mask."""
+    import oracle as O
+    qh, kh, vh, r0, r1, vi, si = t
+    N = qh.shape[0]
+    o, _ = O.attention_rows(qh, kh, vh, np.arange(r0, r1), lambda r: O.vs_mask_rows(N, r, vi, si), chunk=128)
+    return float(np.abs(o).sum())
+
+
+def oracle_full(w, x, procs):
+    """Time the oracle on the WHOLE layer of an all-vertical-slash workload (every head's
+    estimation, then every row's attention), on ``procs`` worker processes (a spawn pool;
+    procs = 1 runs in this process).  Returns (ms per layer, description)."""
+    import multiprocessing as mp
+    Hq, Hkv, N = w["Hq"], w["Hkv"], w["N"]
+    gq = Hq // Hkv
+    q = x.q.float().cpu().numpy()
+    k = x.k.float().cpu().numpy()
+    v = x.v.float().cpu().numpy()
+    est = [(q[h], k[h // gq], w["k_v"], w["k_s"]) for h in range(Hq)]
+    rows_per_task = 1024
+
+    def tasks(idx):
+        return [(q[h], k[h // gq], v[h // gq], r0, min(N, r0 + rows_per_task), idx[h][0], idx[h][1])
+                for h in range(Hq) for r0 in range(0, N, rows_per_task)]
+    if procs == 1:
+        t0 = time.perf_counter()
+        idx = [_oracle_estimate_task(e) for e in est]
+        for t in tasks(idx):
+            _oracle_rows_task(t)
+        dt = time.perf_counter() - t0
+    else:
+        env = {k2: os.environ.get(k2) for k2 in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k2 in env:
+            os.environ[k2] = "1"  # one BLAS thread per worker process
+        try:
+            with mp.get_context("spawn").Pool(procs) as pool:
+                pool.map(abs, range(procs))  # workers started before the clock
+                t0 = time.perf_counter()
+                idx = pool.map(_oracle_estimate_task, est)
+                pool.map(_oracle_rows_task, tasks(idx), chunksize=1)
+                dt = time.perf_counter() - t0
+        finally:
+            for k2, val in env.items():
+                if val is None:
+                    os.environ.pop(k2, None)
+                else:
+                    os.environ[k2] = val
+    desc = (f"oracle on the whole layer: estimation of all {Hq} heads + attention of all {Hq} x {N} rows "
+            f"(nothing extrapolated), {procs} worker process(es) with one BLAS thread each")
+    return dt * 1e3, desc
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
@@ -427,10 +511,10 @@ def run_reference(args, w, rank, world):
                          seed=w["seed"], device="cuda" if torch.cuda.is_available() else "cpu")
     rng = np.random.default_rng(0)
     for _ in range(args.warmup):
-        oracle_sample(w, x, 32, rng)
+        oracle_sample(w, x, ORACLE_SAMPLE_ROWS, rng)
     vals, desc = [], ""
     for _ in range(args.steps):
-        v, desc = oracle_sample(w, x, 64, rng)
+        v, desc = oracle_sample(w, x, ORACLE_SAMPLE_ROWS, rng)
         vals.append(v)
     value = statistics.mean(vals)
     cores = len(os.sched_getaffinity(0))
@@ -439,7 +523,8 @@ def run_reference(args, w, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {describe(w)}", "input": "literal", "seq_len": w["N"]},
-        "cpu_baseline": {"value": value, "unit": "ms/layer", "cores": cores, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "ms/layer", "cores": cores, "kind": "oracle", "sample": desc,
+                         "extrapolated": True},
         "e2e": {"value": value, "unit": "ms/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -509,6 +594,9 @@ def main():
     ap.add_argument("--no-expanded", action="store_true",
                     help="skip the extra timing of the block-expanded slash mode")
     ap.add_argument("--sweep", action="store_true", help="time the N x k_v x k_s sweep instead")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="also time the oracle on the whole layer (all-vertical-slash workloads up to 32K tokens; "
+                         "single-core and all-core)")
     ap.add_argument("--sweep-n", default="", help="comma-separated N values for --sweep")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
@@ -547,6 +635,7 @@ def main():
     dense_ms = None
     e2e = None
     cpu = None
+    cpu_full = None
     clocks = None
     for vi_, variant in enumerate(variants):
         x = make_inputs(w, variant, dev)
@@ -622,9 +711,18 @@ def main():
                                   "and last steps run by groups of 2 KV heads, so that their copies overlap "
                                   "the other groups' compute"}
             if not args.no_cpu and rank == 0 and world == 1:
-                v_ms, desc = oracle_sample(w, x, 256, np.random.default_rng(1))
+                v_ms, desc = oracle_sample(w, x, ORACLE_SAMPLE_ROWS, np.random.default_rng(1))
                 cpu = {"value": v_ms, "unit": "ms/layer", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-                       "sample": desc}
+                       "sample": desc, "extrapolated": True}
+            if args.cpu_full and rank == 0 and world == 1:
+                assert w["n_vs"] == w["Hq"] and w["N"] <= 32768, "--cpu-full is for the 4K and 32K workloads"
+                cores = len(os.sched_getaffinity(0))
+                full_ms, full_desc = oracle_full(w, x, cores)
+                cpu_full = {"value": full_ms, "unit": "ms/layer", "cores": cores, "kind": "oracle",
+                            "sample": full_desc, "extrapolated": False}
+                if w["N"] <= 4096:
+                    one_ms, one_desc = oracle_full(w, x, 1)
+                    cpu_full["single_core"] = {"value": one_ms, "unit": "ms/layer", "cores": 1, "sample": one_desc}
             kernels = L.kernels_per_step * args.steps
         results[variant] = res
         del L, x
@@ -655,7 +753,7 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "vertical-slash sparse attention (tcgen05)",
                      "achieved": ach, "peak": sustained, "unit": "TFLOP/s",
                      "frac": (ach / sustained) if ach else None,
-                     "traffic": TRAFFIC_BYTES.get((args.workload, variants[0])),
+                     "traffic": traffic_bytes(args.workload, variants[0]),
                      "flops": "algorithmic: 4*d per kept (q, j) pair; time = the mi_vs_sparse_attn call",
                      "peak_source": f"bf16_tflops_sustained ({peak_src})",
                      "executed_tflops": head["vs_attention_exec_tflops"],
@@ -672,6 +770,8 @@ def main():
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    if cpu_full:
+        line["cpu_full_layer"] = cpu_full
     if dense_ms:
         for r in line["variants"].values():
             r["dense_equiv_speedup"] = dense_ms / r["ms_per_layer"]

@@ -21,7 +21,10 @@ namespace {
 static __device__ __align__(256) unsigned char g_est_scratch[MI_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_setup_mu;
-void* g_scratch_addr[64];  // device address of g_est_scratch, per device ordinal
+// Device address of g_est_scratch, per device ordinal, looked up once with that
+// device current.  It belongs to the context that existed at the lookup: after a
+// cudaDeviceReset the library must not be used again in the process.
+void* g_scratch_addr[64];
 
 // Once per device, with that device current: look up the scratch's device address.
 int scratch_for_current_device(void** out) {
@@ -44,13 +47,16 @@ extern "C" int mi_vs_estimate_noalloc(const mi_bf16* q, const mi_bf16* k, int Hq
                                       int d, const int32_t* heads, int n_heads, int last_q,
                                       int k_v, int k_s, int32_t* v_idx, int32_t* s_idx,
                                       mi_stream_t stream) {
-  if (n_heads > 0 && N > 0) {
-    const size_t need = mi_workspace_bytes(MI_OP_VS_ESTIMATE, n_heads, Hkv, N, k_v, k_s, 0);
-    if (need > MI_NOALLOC_SCRATCH_BYTES) return MI_ERR_WORKSPACE;  // job too large for the array
-  }
+  // Argument and shape checks in mi_vs_estimate's own order: without a workspace
+  // that call queues nothing and returns the first argument, shape or device
+  // error, or MI_ERR_WORKSPACE when everything else is valid.
+  int rc = mi_vs_estimate(q, k, Hq, Hkv, N, d, heads, n_heads, last_q, k_v, k_s, v_idx, s_idx,
+                          nullptr, 0, stream);
+  if (rc != MI_ERR_WORKSPACE) return rc;
+  const size_t need = mi_workspace_bytes(MI_OP_VS_ESTIMATE, n_heads, Hkv, N, k_v, k_s, 0);
+  if (need > MI_NOALLOC_SCRATCH_BYTES) return MI_ERR_WORKSPACE;  // job too large for the array
   void* scratch = nullptr;
-  const int rc = scratch_for_current_device(&scratch);
-  if (rc != MI_OK) return rc;
+  if ((rc = scratch_for_current_device(&scratch)) != MI_OK) return rc;
   // The status word at the start of the scratch is cleared by the call itself;
   // every other scratch element is written before it is read.
   return mi_vs_estimate(q, k, Hq, Hkv, N, d, heads, n_heads, last_q, k_v, k_s, v_idx, s_idx,

@@ -252,16 +252,22 @@ int mi_layer_attn_varlen(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
  * counterpart; this is a packaging variant of the call above.
  *
  * Same arguments, results and errors as mi_vs_estimate, minus the workspace: the
- * scratch is a fixed array of MI_NOALLOC_SCRATCH_BYTES in device memory owned by
- * libmi.so, present on every GPU that loads the library until the process
- * exits.  The call allocates nothing.
+ * scratch is a fixed array of MI_NOALLOC_SCRATCH_BYTES (36 MiB) in device memory
+ * owned by libmi.so, present on every GPU that loads the library until the
+ * process exits.  The call allocates nothing.
  *  - Size limit: the job must fit the array, i.e.
  *    mi_workspace_bytes(MI_OP_VS_ESTIMATE, n_heads, Hkv, N, 0, 0, 0)
- *    <= MI_NOALLOC_SCRATCH_BYTES (about 8 * n_heads * N bytes: 32 heads at 128K
- *    tokens fit); a larger job returns MI_ERR_WORKSPACE before any work is queued.
+ *    <= MI_NOALLOC_SCRATCH_BYTES.  That size is 256 + 512 * n_heads * ceil(N / 1024)
+ *    + 512 * n_heads + 8 * n_heads * N bytes, each of the five terms rounded up to
+ *    a multiple of 256.  A whole 32-head layer fits up to N = 138686 tokens (so at
+ *    128K tokens); 32 heads at N = 138687 do not.  A job that does not fit
+ *    returns MI_ERR_WORKSPACE before any work is queued, after the argument and
+ *    shape checks of mi_vs_estimate (which come first, as in that call).
  *  - Set-up: the first call on a device, with that device current, looks up the
  *    array's device address (once per device).  Make that first call before any
- *    stream capture begins.
+ *    stream capture begins.  The address belongs to the context of that first
+ *    call: after a cudaDeviceReset the library must not be used again in the
+ *    process.
  *  - Sharing: every call uses the same array and leaves its contents behind; the
  *    call clears what has to start at zero.  Calls that overlap on the GPU (on
  *    different streams or from different threads) race on the array and must be
@@ -269,7 +275,7 @@ int mi_layer_attn_varlen(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
  *  - The device status word lives in the shared array and cannot be read back
  *    with mi_read_status; use mi_vs_estimate with a workspace when it matters.
  */
-#define MI_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define MI_NOALLOC_SCRATCH_BYTES (36u << 20)
 int mi_vs_estimate_noalloc(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
                            const int32_t* heads, int n_heads, int last_q, int k_v, int k_s,
                            int32_t* v_idx, int32_t* s_idx, mi_stream_t stream);

@@ -748,8 +748,10 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         m_ref = mx;
       }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P = exp2(x * sl - m) as bf16 pairs over the consumed S columns
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      // P = exp2(x * sl - m) as bf16 pairs over the consumed S columns; the
+      // scale-and-shift and the row sum take two keys per instruction (f32x2)
+      float2 rs4[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // independent partial sums
+      const float2 sl2 = make_float2(sl, sl), nmb2 = make_float2(-mb, -mb);
       const bool resc = __any_sync(0xffffffffu, rescale_o);
 #pragma unroll
       constexpr int NQ = kPChunks<PAT>, CP = 64 / NQ;  // chunks, bf16 pairs per chunk
@@ -758,10 +760,10 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         uint32_t pk[CP];
 #pragma unroll
         for (int e = 0; e < CP; ++e) {
-          const float p0 = fast_exp2(fmaf(x[qq * 2 * CP + 2 * e], sl, -mb));
-          const float p1 = fast_exp2(fmaf(x[qq * 2 * CP + 2 * e + 1], sl, -mb));
-          rs8[e & 7] += p0 + p1;
-          __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
+          const float2 y = fma2(make_float2(x[qq * 2 * CP + 2 * e], x[qq * 2 * CP + 2 * e + 1]), sl2, nmb2);
+          const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+          rs4[e & 3] = add2(rs4[e & 3], p);
+          __nv_bfloat162 bb = __floats2bfloat162_rn(p.x, p.y);
           pk[e] = *reinterpret_cast<uint32_t*>(&bb);
         }
         if constexpr (CP == 32) {
@@ -787,7 +789,8 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
           tmem_st32(o_addr + c * 32, o);
         }
       }
-      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      const float2 rs = add2(add2(rs4[0], rs4[1]), add2(rs4[2], rs4[3]));
+      l += rs.x + rs.y;
       tc_fence_before();
       if (resc) {
 #pragma unroll

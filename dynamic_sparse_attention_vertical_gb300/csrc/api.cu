@@ -323,11 +323,11 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
   CUtensorMap mq, mk;
   if ((rc = make_map(&mq, q, Hq, N, kLastQ, ld)) || (rc = make_map(&mk, k, Hkv, N, kBN, ld))) return rc;
   const dim3 grid(np, L.NC);
-  est_kernel<1><<<grid, 256, kEstSmem1, st>>>(mq, mk, a);
+  est_kernel<1><<<grid, kEstThreads, kEstSmem1, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 1"))) return rc;
   est_combine<<<n_heads, kLastQ, 0, st>>>(a.part, a.stats, L.NC);
   if ((rc = launched("estimation combine"))) return rc;
-  est_kernel<2><<<grid, 256, kEstSmem2, st>>>(mq, mk, a);
+  est_kernel<2><<<grid, kEstThreads, kEstSmem2, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 2"))) return rc;
   if (ld_v > 0 || ld_s > 0) {
     vs_topk_kernel<<<dim3(n_heads, 2), 1024, kTopkSmemBytes, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx, ld_v,

@@ -9,11 +9,13 @@
 // Layout of the work: one CTA takes a pair of q-heads that share a KV head
 // (128 query rows = 2 x 64, one UMMA M) and a chunk of 1024 keys, and runs
 // S = Q K^T per 128-key tile on the tensor cores (TMEM accumulator), so each
-// K tile is read once for both heads.
+// K tile is read once for both heads.  Eight warps do the arithmetic, two
+// threads per row (64 keys of each tile each).
 //   pass 1  per row: running max m and sum z = sum exp2(x - m) over the chunk
 //   combine per row: merge the chunk partials in chunk order -> (m, 1/z)
-//   pass 2  per tile: a = exp2(x - m) / z into shared memory; column sums give
-//           v[j] for the tile's keys; sums along each diagonal give s[o].
+//   pass 2  per tile: a = exp2(x - m) / z into shared memory, skewed so that
+//           every diagonal is a column; column sums give v[j] for the tile's
+//           keys, sums down the skewed columns give s[o].
 // A diagonal d (the key its row 63 meets) spans keys d-63..d, so it may start
 // in the previous tile: partial diagonal sums are carried from tile to tile,
 // and each pass-2 CTA also scores the 128 keys before its chunk (a halo tile
@@ -47,25 +49,30 @@ struct EstSmem {
   uint64_t q_full, k_full[2], k_empty[2], s_full[2], s_empty[2], mma_done;
   uint32_t tmem;
   int abort;
-  float carry[2][2][64];  // [buffer][head of pair][diagonal]
+  float carry[2][2][64];  // pass 2: [buffer][head of pair][diagonal]
+  float mz[2][128][2];    // pass 1: the two column halves' (m, z) of each row
 };
-constexpr int kEstPitch = 129;  // fp32 row pitch of the probability tile
+// Pass 2 keeps each tile's probabilities in a skewed layout, per head of the
+// pair 64 rows x 192 fp32: row i's key c sits at column c + 63 - i, so that
+// diagonal e of the tile (the diagonal that meets key j0 + e at row 63) is
+// column e, and key column c runs along i -> c + 63 - i.  Positions outside a
+// row's 128 keys stay zero (written once).
+constexpr int kSkPitch = 192;
+constexpr int kSkHead = 64 * kSkPitch;
+constexpr int kEstThreads = 384;  // warp 0 MMA, warp 1 TMA, warps 4-11 the rows' arithmetic
+constexpr int kEstMath = 256;     // threads of warps 4-11
 constexpr size_t kEstSmem1 = sizeof(EstSmem) + 1024;
-constexpr size_t kEstSmem2 = sizeof(EstSmem) + 1024 + sizeof(float) * 128 * kEstPitch;
-
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
+constexpr size_t kEstSmem2 = sizeof(EstSmem) + 1024 + sizeof(float) * 2 * kSkHead;
 
 template <int PASS>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kEstThreads, 1)
 est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ EstArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   EstSmem& s = *reinterpret_cast<EstSmem*>(base);
-  float* A = reinterpret_cast<float*>(base + sizeof(EstSmem));  // pass 2 only: [128][kEstPitch]
+  float* Sk = reinterpret_cast<float*>(base + sizeof(EstSmem));  // pass 2 only: [2][64][kSkPitch]
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int pr = blockIdx.x, chunk = blockIdx.y;
@@ -85,13 +92,16 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_init(&s.k_full[b], 1);
       mbar_init(&s.k_empty[b], 1);
       mbar_init(&s.s_full[b], 1);
-      mbar_init(&s.s_empty[b], 128);
+      mbar_init(&s.s_empty[b], kEstMath);
     }
     mbar_init(&s.mma_done, 1);
     s.abort = 0;
     fence_mbar_init();
   }
   if (tid < 128) (&s.carry[0][0][0])[tid + 128] = 0.f;  // buffer 1 = carry into tile 0
+  if (PASS == 2) {
+    for (int e = tid; e < 2 * kSkHead; e += kEstThreads) Sk[e] = 0.f;
+  }
   if (warp == 0) {
     tmem_alloc(&s.tmem, 256);
     tmem_relinquish();
@@ -148,38 +158,46 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     }
     __syncwarp();
   } else if (warp >= 4) {
-    const int row = tid - 128;  // TMEM lane; rows 0-63 head a, 64-127 head b
+    // two threads per row: warp w reads TMEM lanes 32 (w % 4) .. + 31 (the rows)
+    // and the columns 64 ch .. 64 ch + 63 of each tile, ch = (w - 4) / 4
+    const int mt = tid - 128;                 // 0..255
+    const int row = ((warp & 3) << 5) | static_cast<int>(lane_id());  // rows 0-63 head a, 64-127 head b
+    const int ch = (warp - 4) >> 2;
     const int hs = row >> 6, i = row & 63;
     const int slot = hs ? slot_b : slot_a;
     const int p_i = N - kLastQ + i;  // position of this query row
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64 * ch;
     float m = -INFINITY, z = 0.f, invz = 0.f;
     if (PASS == 2 && slot >= 0) {
       m = a.stats[((size_t)slot * kLastQ + i) * 2 + 0];
       invz = a.stats[((size_t)slot * kLastQ + i) * 2 + 1];
     }
+    // pass 2: this thread's place in the skewed tile, and its reductions: threads
+    // 0-95 take four adjacent diagonals (of head mt / 48), threads 96-255 one or
+    // two key columns (of the 256 columns of both heads)
+    float* sk_row = Sk + hs * kSkHead + i * (kSkPitch - 1) + 63 + 64 * ch;  // + c: key 64 ch + c
     for (int t = 0; t < T; ++t) {
       const int b = t & 1;
       // On a failed (timed-out) wait the loop still runs to the end with zeros, so
-      // that the four row warps keep meeting at the named barriers below.
+      // that the math warps keep meeting at the named barriers below.
       const bool ok = mbar_wait_warp(&s.s_full[b], (t >> 1) & 1, abort, lim);
-      float x[128];
+      float x[64];
       if (ok) {
         tc_fence_after();
-        tmem_ld128(tmem + lane_base + b * 128, x);
+        tmem_ld64(taddr + b * 128, x);
         tc_fence_before();
         mbar_arrive(&s.s_empty[b]);
       } else {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = 0.f;
+        for (int c = 0; c < 64; ++c) x[c] = 0.f;
       }
       const int j0 = k_lo + t * kBN;
-      // keys j0 + c with c <= lim_c are causal; rows of an absent second head are dropped
-      const int lim_c = (slot >= 0) ? p_i - j0 : -1;
+      // keys j0 + 64 ch + c with c <= lim_c are causal; rows of an absent second head are dropped
+      const int lim_c = (slot >= 0) ? p_i - j0 - 64 * ch : -1;
       if (PASS == 1) {
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < 64; ++c) {
           x[c] = (c <= lim_c) ? x[c] * a.scale_log2 : -INFINITY;
           mx = fmaxf(mx, x[c]);
         }
@@ -187,66 +205,80 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const float mb = (mn == -INFINITY) ? 0.f : mn;
         float acc = 0.f;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) acc += fast_exp2(x[c] - mb);
+        for (int c = 0; c < 64; ++c) acc += fast_exp2(x[c] - mb);
         z = z * fast_exp2(m - mb) + acc;
         m = mn;
       } else {
-        float* Ar = A + row * kEstPitch;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          Ar[c] = (c <= lim_c) ? fast_exp2(x[c] * a.scale_log2 - m) * invz : 0.f;
-        named_bar_sync(1, 128);
+        for (int c = 0; c < 64; ++c)
+          sk_row[c] = (c <= lim_c) ? fast_exp2(x[c] * a.scale_log2 - m) * invz : 0.f;
+        named_bar_sync(1, kEstMath);
         const bool halo = has_halo && t == 0;
         const float* cin = &s.carry[(t + 1) & 1][0][0];
         float* cout = &s.carry[t & 1][0][0];
-        for (int J = row; J < 2 * 128 + 2 * 191; J += 128) {
-          if (J < 256) {  // column sums
-            const int hh = J >> 7, c = J & 127;
-            const int sl = hh ? slot_b : slot_a;
-            if (halo || sl < 0 || j0 + c >= N) continue;
-            const float* col = A + hh * 64 * kEstPitch + c;
-            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (mt < 96) {
+          // diagonals e0 .. e0 + 3 of head hh: column sums of the skewed tile,
+          // 16-byte loads, rows in a fixed order (four partial sums per diagonal)
+          const int hh = mt / 48, e0 = 4 * (mt - 48 * hh);
+          const int sl = hh ? slot_b : slot_a;
+          const float* col = Sk + hh * kSkHead + e0;
+          float4 acc[4] = {};
 #pragma unroll
-            for (int r = 0; r < 64; ++r) acc4[r & 3] += col[r * kEstPitch];
-            const float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-            a.vsc[(size_t)sl * N + j0 + c] = acc;
-          } else {  // diagonal sums; diagonal e of the tile meets key j0 + e at row 63
-            const int Jd = J - 256;
-            const int hh = Jd / 191, e = Jd - hh * 191;
-            const int sl = hh ? slot_b : slot_a;
-            const int i_lo = max(0, 63 - e), i_hi = min(63, 190 - e);
-            const float* At = A + hh * 64 * kEstPitch;
-            // rows i_lo..i_hi in batches of 8 with independent loads (addresses
-            // clamped into the tile, out-of-range rows weighted 0), summed in a
-            // fixed order: four partial sums, then their pairwise sum
-            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int r = 0; r < 64; ++r) {
+            const float4 v = *reinterpret_cast<const float4*>(col + r * kSkPitch);
+            float4& A = acc[r & 3];
+            A.x += v.x;
+            A.y += v.y;
+            A.z += v.z;
+            A.w += v.w;
+          }
+          const float d4[4] = {(acc[0].x + acc[1].x) + (acc[2].x + acc[3].x),
+                               (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y),
+                               (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z),
+                               (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w)};
 #pragma unroll
-            for (int r0 = 0; r0 < 64; r0 += 8) {
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int r = r0 + u;
-                const int c = min(max(e - 63 + r, 0), 127);
-                const float val = At[r * kEstPitch + c];
-                acc4[u & 3] += (r >= i_lo && r <= i_hi) ? val : 0.f;
-              }
-            }
-            float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-            if (e < 63) acc += cin[hh * 64 + e];
+          for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u;
+            float v = d4[u];
+            if (e < 63) v += cin[hh * 64 + e];
             if (e < 128) {
               const int d = j0 + e;
-              if (!halo && sl >= 0 && d < N) a.ssc[(size_t)sl * N + (N - 1 - d)] = acc;
-            } else {
-              cout[hh * 64 + (e - 128)] = acc;
+              if (!halo && sl >= 0 && d < N) a.ssc[(size_t)sl * N + (N - 1 - d)] = v;
+            } else if (e < 191) {
+              cout[hh * 64 + (e - 128)] = v;
             }
           }
+        } else {
+          // key columns J and J + 160 (J < 96) of both heads: column c of head hh
+          // runs along the skewed rows, i -> c + 63 - i
+          for (int J = mt - 96; J < 256; J += 160) {
+            const int hh = J >> 7, c = J & 127;
+            const int sl = hh ? slot_b : slot_a;
+            const float* col = Sk + hh * kSkHead + 63 + c;
+            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < 64; ++r) acc4[r & 3] += col[r * (kSkPitch - 1)];
+            const float v = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+            if (!halo && sl >= 0 && j0 + c < N) a.vsc[(size_t)sl * N + j0 + c] = v;
+          }
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEstMath);
       }
     }
-    if (PASS == 1 && slot >= 0) {
-      float* pp = a.part + (((size_t)slot * kLastQ + i) * a.NC + chunk) * 2;
-      pp[0] = m;
-      pp[1] = z;
+    if (PASS == 1) {
+      // merge the two column halves of each row, in a fixed order
+      s.mz[ch][row][0] = m;
+      s.mz[ch][row][1] = z;
+      named_bar_sync(1, kEstMath);
+      if (ch == 0 && slot >= 0) {
+        const float m1 = s.mz[1][row][0], z1 = s.mz[1][row][1];
+        const float mn = fmaxf(m, m1);
+        const float mb = (mn == -INFINITY) ? 0.f : mn;
+        const float zz = z * fast_exp2(m - mb) + z1 * fast_exp2(m1 - mb);
+        float* pp = a.part + (((size_t)slot * kLastQ + i) * a.NC + chunk) * 2;
+        pp[0] = mn;
+        pp[1] = zz;
+      }
     }
   }
   tc_fence_before();

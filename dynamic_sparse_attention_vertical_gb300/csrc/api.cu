@@ -234,8 +234,8 @@ int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, 
                   mi_bf16* out, float* lse, int* status, AttnArgs& a, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mkr, mvr;
   int rc;
-  if ((rc = make_map(&mq, q, Hq, N, kBM, N)) || (rc = make_map(&mk, k, Hkv, N, kBN, N)) ||
-      (rc = make_map(&mv, v, Hkv, N, kBN, N)))
+  if ((rc = make_map(&mq, q, Hq, N, kBM, N)) || (rc = make_map(&mk, k, Hkv, N, kBlk, N)) ||
+      (rc = make_map(&mv, v, Hkv, N, kBlk, N)))
     return rc;
   if (is_vs(PAT)) {  // gathered column tiles
     if ((rc = make_rows_map(&mkr, k, Hkv, N, N)) || (rc = make_rows_map(&mvr, v, Hkv, N, N))) return rc;
@@ -555,8 +555,8 @@ int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int 
   }
   // the attention of every listed head in one launch
   CUtensorMap mq, mk, mv, mkr, mvr;
-  if ((rc = make_map(&mq, q, Hq, N, kBM, ld)) || (rc = make_map(&mk, k, Hkv, N, kBN, ld)) ||
-      (rc = make_map(&mv, v, Hkv, N, kBN, ld)) || (rc = make_rows_map(&mkr, k, Hkv, N, ld)) ||
+  if ((rc = make_map(&mq, q, Hq, N, kBM, ld)) || (rc = make_map(&mk, k, Hkv, N, kBlk, ld)) ||
+      (rc = make_map(&mv, v, Hkv, N, kBlk, ld)) || (rc = make_rows_map(&mkr, k, Hkv, N, ld)) ||
       (rc = make_rows_map(&mvr, v, Hkv, N, ld)))
     return rc;
   a.N = N;

@@ -3,7 +3,10 @@
 // One CTA computes 128 query rows (one row block r) of one head.  Its key
 // range is a list of 128-key tiles chosen by the head's pattern:
 //   - contiguous tiles, TMA-loaded from K/V ([Hkv, N, 128] bf16, 128-byte
-//     swizzle), masked element-wise by the pattern's rule;
+//     swizzle, 64-key boxes), masked element-wise by the pattern's rule;
+//   - for block-sparse heads, tiles made of two 64-key blocks from anywhere
+//     below the diagonal (two boxes each), paired from the two 64-row halves'
+//     selections;
 //   - for vertical-slash heads, "gathered" tiles of up to 128 scattered key
 //     columns that no contiguous tile covers, loaded four rows at a time with
 //     TMA tile::gather4 into the same swizzled layout (the permutation-invariant gathering idea of PIT, which
@@ -84,7 +87,7 @@ struct AttnSmem {
   alignas(1024) uint8_t q[2][16384];
   alignas(1024) uint8_t k[2][16384];
   alignas(1024) uint8_t v[2][16384];
-  int list[MI_MAX_KV];  // VS: residual columns; block: (tile << 4) | sub-block mask
+  int list[MI_MAX_KV];  // VS: residual columns; block: per tile (block A << 4) | sub-block mask, block B
   int scan[192];
   uint32_t dfull[512];  // VS: the head's whole-tile distance bits (N <= 2^21)
   // VS: keep-masks of two tiles in flight (row i: bit c of word c / 32 keeps
@@ -124,14 +127,16 @@ constexpr int kPChunks = PAT == kPatDense ? 2 : 4;
 
 struct TileRef {
   int kind;  // 0 contiguous, 1 gathered
-  int t;     // contiguous: key tile index; gathered: chunk of the residual list
-  int sub;   // block pattern: 4-bit mask (bit = rowhalf*2 + colhalf)
+  int t;     // contiguous: key tile index; gathered: chunk of the residual list;
+             // block pattern: the 64-key block in keys 0-63 of the tile
+  int sub;   // block pattern: 4-bit mask (bit = rowhalf*2 + keyhalf)
+  int t2;    // block pattern: the 64-key block in keys 64-127 of the tile
 };
 
 template <int PAT>
 __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a, int n, int r,
                                            int i) {
-  TileRef ref{0, 0, 0xF};
+  TileRef ref{0, 0, 0xF, 0};
   if (PAT == kPatDense) {
     ref.t = i;
   } else if (is_vs(PAT)) {
@@ -147,9 +152,10 @@ __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a,
       ref.t = i - s.n_contig;
     }
   } else if (PAT == kPatBlock) {
-    const int e = s.list[i];
+    const int e = s.list[2 * i];
     ref.t = e >> 4;
     ref.sub = e & 0xF;
+    ref.t2 = s.list[2 * i + 1];
   } else {  // A-shape: sink tiles then the window tiles
     const int t_lo = max(0, r * kBM - s.ash_window + 1) / kBN;
     const int n_sink = min(cdiv(s.ash_init, kBN), t_lo);
@@ -312,13 +318,24 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
       for (int w = 0; w < 4; ++w) out[w] |= range_bits(j0 + 32 * w, lb, lb + kBlk);
     }
   } else if (PAT == kPatBlock) {
-    const int half = (q >> 6) & 1;
+    // keys 0-63 are block ref.t, keys 64-127 block ref.t2; a row keeps a block
+    // its half selected, causally inside its own block
+    const int half = (q >> 6) & 1, own = q >> 6;
     const uint32_t lo = ((ref.sub >> (half * 2)) & 1) ? 0xFFFFFFFFu : 0u;
     const uint32_t hi = ((ref.sub >> (half * 2 + 1)) & 1) ? 0xFFFFFFFFu : 0u;
     out[0] = lo;
     out[1] = lo;
     out[2] = hi;
     out[3] = hi;
+    if (ref.t == own) {
+      out[0] &= range_bits(ref.t * kBlk, 0, q + 1);
+      out[1] &= range_bits(ref.t * kBlk + 32, 0, q + 1);
+    }
+    if (ref.t2 == own) {
+      out[2] &= range_bits(ref.t2 * kBlk, 0, q + 1);
+      out[3] &= range_bits(ref.t2 * kBlk + 32, 0, q + 1);
+    }
+    return;
   } else {  // A-shape
 #pragma unroll
     for (int w = 0; w < 4; ++w)
@@ -461,45 +478,75 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
       s.n_list = total;
       s.n_tiles = s.n_contig + cdiv(total, kBN);
     }
-  } else {  // block-sparse: union of the two 64-row halves' selected blocks, as 128-key tiles
-    // Each selected block sets its bit in its tile's 4-bit sub-block mask (bit =
-    // row half * 2 + key half), one byte per tile, kept in the V buffer, which
-    // the loads only fill after this prologue; the nonzero tiles are then
-    // compacted in order.  All threads take part: the lists are read once, in
-    // parallel, instead of by a serial merge of dependent loads.
-    uint32_t* subw = reinterpret_cast<uint32_t*>(&s.v[0][0]);  // tiles 0..r, <= 16 KB
-    const int nw = (r + 4) / 4;
-    for (int w = tid; w < nw; w += 192) subw[w] = 0u;
-    __syncthreads();
+  } else {  // block-sparse: the two 64-row halves' selected 64-key blocks, paired into 128-key tiles
+    // A tile holds any two blocks A (keys 0-63) and B (keys 64-127).  Blocks
+    // selected by both halves pair with each other (tiles kept whole); the
+    // blocks only one half selected pair with the other half's (each half keeps
+    // its own block of the tile).  The bitmaps and lists live in the V buffer,
+    // which the loads only fill after this prologue.
     const int NB = cdiv(a.N, kBlk);
+    const int nblk = min(2 * r + 2, NB);  // blocks this CTA's rows can select
+    const int nwb = cdiv(nblk, 32);
+    uint32_t* bm0 = reinterpret_cast<uint32_t*>(&s.v[0][0]);  // <= 1024 words each (N <= 2^21)
+    uint32_t* bm1 = bm0 + nwb;
+    int* lc = reinterpret_cast<int*>(bm1 + nwb);  // selected by both halves
+    int* l0 = lc + a.topk;                        // by the first half only
+    int* l1 = l0 + a.topk;                        // by the second half only (3 x topk <= 3 K ints)
+    for (int w = tid; w < 2 * nwb; w += kAttnThreads) bm0[w] = 0u;
+    __syncthreads();
     const int* b0 = a.blk_idx + ((size_t)n * NB + 2 * r) * a.topk;  // row half 1 follows at + topk
     const int nsel = ((2 * r + 1) < NB) ? 2 * a.topk : a.topk;
-    for (int i = tid; i < nsel; i += 192) {
+    for (int i = tid; i < nsel; i += kAttnThreads) {
       const int hf = (i >= a.topk) ? 1 : 0;
       const int c = __ldg(b0 + i);
-      if (c >= 0 && c <= 2 * r + hf) {
-        const int t = c >> 1;
-        atomicOr(&subw[t >> 2], (1u << ((c & 1) + 2 * hf)) << ((t & 3) * 8));
-      }
+      if (c >= 0 && c <= 2 * r + hf) atomicOr(&(hf ? bm1 : bm0)[c >> 5], 1u << (c & 31));
     }
     __syncthreads();
-    const int per = cdiv(r + 1, 192);
-    const int t0 = min(tid * per, r + 1), t1 = min(t0 + per, r + 1);
-    int cnt = 0;
-    for (int t = t0; t < t1; ++t) cnt += ((subw[t >> 2] >> ((t & 3) * 8)) & 0xFu) ? 1 : 0;
-    int total;
-    int pos = block_excl_scan(cnt, s.scan, &total);
-    for (int t = t0; t < t1; ++t) {
-      const uint32_t sub = (subw[t >> 2] >> ((t & 3) * 8)) & 0xFu;
-      if (sub != 0u) {
-        if (pos < MI_MAX_KV) s.list[pos] = (t << 4) | static_cast<int>(sub);
-        ++pos;
+    const int per = cdiv(nwb, kAttnThreads);
+    const int w0 = min(tid * per, nwb), w1 = min(w0 + per, nwb);
+    int nc = 0, n0 = 0, n1 = 0;
+    for (int w = w0; w < w1; ++w) {
+      const uint32_t x0 = bm0[w], x1 = bm1[w];
+      nc += __popc(x0 & x1);
+      n0 += __popc(x0 & ~x1);
+      n1 += __popc(x1 & ~x0);
+    }
+    int tc, t0, t1;
+    int pc = block_excl_scan(nc, s.scan, &tc);
+    int p0 = block_excl_scan(n0, s.scan, &t0);
+    int p1 = block_excl_scan(n1, s.scan, &t1);
+    for (int w = w0; w < w1; ++w) {
+      const uint32_t x0 = bm0[w], x1 = bm1[w];
+      for (uint32_t m = x0 & x1; m; m &= m - 1) lc[pc++] = 32 * w + __ffs(m) - 1;
+      for (uint32_t m = x0 & ~x1; m; m &= m - 1) l0[p0++] = 32 * w + __ffs(m) - 1;
+      for (uint32_t m = x1 & ~x0; m; m &= m - 1) l1[p1++] = 32 * w + __ffs(m) - 1;
+    }
+    __syncthreads();
+    const int ncp = (tc + 1) / 2;
+    const int ntile = ncp + max(t0, t1);  // <= topk <= MI_MAX_KV / 2
+    for (int t = tid; t < ntile; t += kAttnThreads) {
+      int A, Bb, sub;
+      if (t < ncp) {
+        A = lc[2 * t];
+        Bb = (2 * t + 1 < tc) ? lc[2 * t + 1] : -1;
+        sub = (Bb >= 0) ? 0xF : 0x5;
+      } else {
+        const int j = t - ncp;
+        A = (j < t0) ? l0[j] : -1;
+        Bb = (j < t1) ? l1[j] : -1;
+        sub = (A >= 0 ? 0x1 : 0) | (Bb >= 0 ? 0x8 : 0);
       }
+      // an empty half of a tile loads the other block again (finite data, masked)
+      if (A < 0) A = Bb;
+      if (Bb < 0) Bb = A;
+      s.list[2 * t] = (A << 4) | sub;
+      s.list[2 * t + 1] = Bb;
     }
     if (tid == 0) {
-      s.n_list = min(total, MI_MAX_KV);
-      s.n_tiles = s.n_list;
+      s.n_list = ntile;
+      s.n_tiles = ntile;
     }
+    __syncthreads();  // the lists in the V buffer are read before any V load is issued
     fence_proxy_async_smem();  // generic writes to the V buffer before its TMA loads
   }
   __syncthreads();
@@ -612,14 +659,20 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     int issued = 0;
     // the next tile's reference (a global load for vertical-slash heads) is read
     // before waiting for the buffers, so its latency overlaps those waits
-    TileRef ref_next = (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0};
+    TileRef ref_next = (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0, 0};
     auto load = [&](const TileRef& ref, const CUtensorMap* map, const CUtensorMap* rows_map,
                     uint64_t* full, uint8_t (*buf)[16384]) {
       if (ref.kind == 0) {
+        // two 64-key boxes per 64-column half: keys 0-63 and 64-127 of the
+        // tile (for block-sparse tiles, blocks ref.t and ref.t2)
         if (lane_id() == 0) {
+          const int ka = (PAT == kPatBlock) ? ref.t * kBlk : ref.t * kBN;
+          const int kb = (PAT == kPatBlock) ? ref.t2 * kBlk : ref.t * kBN + kBlk;
           mbar_arrive_expect_tx(full, 2 * 16384);
-          tma_load_3d(buf[0], map, full, 0, ref.t * kBN, g);
-          tma_load_3d(buf[1], map, full, 64, ref.t * kBN, g);
+          tma_load_3d(buf[0], map, full, 0, ka, g);
+          tma_load_3d(buf[0] + 8192, map, full, 0, kb, g);
+          tma_load_3d(buf[1], map, full, 64, ka, g);
+          tma_load_3d(buf[1] + 8192, map, full, 64, kb, g);
         }
       } else {
         // up to 128 residual columns, four rows per tile::gather4 load: lane l
@@ -692,8 +745,8 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     TileRef ref_next2{0, 0, 0};
     MaskRaw raw_next{};
     if constexpr (!is_vs(PAT)) {
-      ref_next2 = (T > 1) ? tile_at<PAT>(s, a, n, r, 1) : TileRef{0, 0, 0};
-      raw_next = mask_fetch<PAT>((T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0});
+      ref_next2 = (T > 1) ? tile_at<PAT>(s, a, n, r, 1) : TileRef{0, 0, 0, 0};
+      raw_next = mask_fetch<PAT>((T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0, 0});
     }
     for (int t = 0; t < T; ++t) {
       uint32_t mk[4];

@@ -177,12 +177,13 @@ def ashape_tiles(N: int, n_init: int, window: int) -> int:
 
 
 def block_tiles(sel_rows) -> int:
-    """Tiles of the block-sparse kernel: per 128-row block, the union of both halves' 128-key tiles."""
+    """Tiles of the block-sparse kernel: per 128-row block, the blocks both 64-row halves
+    selected pair with each other, and the blocks only one half selected pair with the
+    other half's, two 64-key blocks per 128-key tile."""
     total = 0
     for r in range(0, len(sel_rows), 2):
-        tiles = set()
-        for rr in (r, r + 1):
-            if rr < len(sel_rows):
-                tiles |= {int(c) >> 1 for c in sel_rows[rr] if int(c) >= 0}
-        total += len(tiles)
+        s0 = {int(c) for c in sel_rows[r] if int(c) >= 0}
+        s1 = {int(c) for c in sel_rows[r + 1] if int(c) >= 0} if r + 1 < len(sel_rows) else set()
+        both = s0 & s1
+        total += (len(both) + 1) // 2 + max(len(s0 - both), len(s1 - both))
     return total

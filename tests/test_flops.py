@@ -86,3 +86,39 @@ def test_vs_expanded_tile_count_matches_enumeration(N, kv, ks, seed):
     v = np.sort(rng.choice(N, size=kv, replace=False))
     s = np.sort(rng.choice(N, size=ks, replace=False)) if ks else np.zeros(0, dtype=np.int64)
     assert F.vs_tiles(N, v, s, expanded=True) == _vs_expanded_tiles_brute(N, v.tolist(), s.tolist())
+
+
+def test_block_tiles_pairing_covers_each_selection_once():
+    """The block-sparse schedule: per 128-row block, blocks both 64-row halves selected
+    pair with each other, blocks one half selected pair with the other half's.  Every
+    (half, selected block) must be kept in exactly one tile, no tile keeps a block for a
+    half that did not select it, and the tile count is the one the bench reports."""
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        nb = int(rng.integers(2, 80))
+        topk = int(rng.integers(1, 40))
+        sel = [np.sort(rng.choice(r + 1, size=min(topk, r + 1), replace=False)) for r in range(nb)]
+        total = 0
+        for r in range(0, nb, 2):
+            s0 = set(int(c) for c in sel[r])
+            s1 = set(int(c) for c in sel[r + 1]) if r + 1 < nb else set()
+            both = sorted(s0 & s1)
+            only0, only1 = sorted(s0 - s1), sorted(s1 - s0)
+            tiles = [(both[i], both[i + 1] if i + 1 < len(both) else None, True, True)
+                     for i in range(0, len(both), 2)]
+            for j in range(max(len(only0), len(only1))):
+                tiles.append((only0[j] if j < len(only0) else None, only1[j] if j < len(only1) else None,
+                              False, False))
+            kept = {0: [], 1: []}
+            for a, b, common_a, common_b in tiles:
+                if common_a:  # a common pair: both halves keep both blocks
+                    for h in (0, 1):
+                        kept[h] += [a] + ([b] if b is not None else [])
+                else:
+                    if a is not None:
+                        kept[0].append(a)
+                    if b is not None:
+                        kept[1].append(b)
+            assert sorted(kept[0]) == sorted(s0) and sorted(kept[1]) == sorted(s1)
+            total += len(tiles)
+        assert total == F.block_tiles(sel)

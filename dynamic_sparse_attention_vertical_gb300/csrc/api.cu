@@ -70,31 +70,6 @@ int make_map(CUtensorMap* m, const void* base, int heads, int N, int box_rows, i
   return MI_OK;
 }
 
-// [heads, N, 128] bf16 (heads `ld` rows apart) as a 2-D tensor of rows
-// (d, (heads - 1) * ld + N) with a 64 x 1 box and 128-byte swizzle: the map for
-// tile::gather4 loads of scattered key rows (row g * ld + key).
-int make_rows_map(CUtensorMap* m, const void* base, int heads, int N, int64_t ld) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) {
-    snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled is not available from the driver");
-    return MI_ERR_CUDA;
-  }
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
-                        static_cast<cuuint64_t>(heads - 1) * static_cast<cuuint64_t>(ld) +
-                            static_cast<cuuint64_t>(N)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
-    return MI_ERR_CUDA;
-  }
-  return MI_OK;
-}
-
 int check_device() {
   static int verdict[64];  // 0 unknown, 1 sm_103, -1 other (benign race: same value)
   int dev = 0;
@@ -167,7 +142,7 @@ EstLayout est_layout(int n_heads, int N) {
 }
 
 struct VsLayout {
-  size_t status, offbits, colbits, dbits, dfull, dlist, dcount, total;
+  size_t status, offbits, colbits, dbits, dfull, dlist, dcount, clist, ccount, kc, vc, total;
   int Nw, NT, NTw;
 };
 VsLayout vs_layout(int n_heads, int N) {
@@ -183,6 +158,10 @@ VsLayout vs_layout(int n_heads, int N) {
   L.dfull = c.take(sizeof(uint32_t) * (size_t)n_heads * L.NTw);
   L.dlist = c.take(sizeof(int) * (size_t)n_heads * L.NT);
   L.dcount = c.take(sizeof(int) * (size_t)n_heads);
+  L.clist = c.take(sizeof(int) * (size_t)n_heads * MI_MAX_KV);
+  L.ccount = c.take(sizeof(int) * (size_t)n_heads);
+  L.kc = c.take(sizeof(uint16_t) * kD * (size_t)n_heads * MI_MAX_KV);
+  L.vc = c.take(sizeof(uint16_t) * kD * (size_t)n_heads * MI_MAX_KV);
   L.total = c.off;
   return L;
 }
@@ -229,16 +208,21 @@ int zero_status(int* status, cudaStream_t st) {
 }
 
 // Shared by the four attention entry points: pattern-specific fields of `a` are set.
+// Vertical-slash launches pass the listed heads' compacted column rows (kc, vc:
+// [n_heads, MI_MAX_KV, 128] bf16) for the column tiles.
 template <int PAT>
 int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, int N,
-                  mi_bf16* out, float* lse, int* status, AttnArgs& a, cudaStream_t st) {
+                  mi_bf16* out, float* lse, int* status, AttnArgs& a, cudaStream_t st,
+                  const void* kc = nullptr, const void* vc = nullptr) {
   CUtensorMap mq, mk, mv, mkr, mvr;
   int rc;
   if ((rc = make_map(&mq, q, Hq, N, kBM, N)) || (rc = make_map(&mk, k, Hkv, N, kBlk, N)) ||
       (rc = make_map(&mv, v, Hkv, N, kBlk, N)))
     return rc;
-  if (is_vs(PAT)) {  // gathered column tiles
-    if ((rc = make_rows_map(&mkr, k, Hkv, N, N)) || (rc = make_rows_map(&mvr, v, Hkv, N, N))) return rc;
+  if (is_vs(PAT)) {  // column tiles
+    if ((rc = make_map(&mkr, kc, a.heads.n, MI_MAX_KV, kBlk, MI_MAX_KV)) ||
+        (rc = make_map(&mvr, vc, a.heads.n, MI_MAX_KV, kBlk, MI_MAX_KV)))
+      return rc;
   } else {
     mkr = mk;
     mvr = mv;
@@ -463,6 +447,7 @@ int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int 
   a.heads = P.listed;
   const int group = Hq / Hkv;
   // vertical-slash heads: estimation per budget group, one index build
+  __nv_bfloat16 *kc = nullptr, *vc = nullptr;  // their compacted column rows
   int32_t* vidx = reinterpret_cast<int32_t*>(ws + L.vidx);
   int32_t* sidx = reinterpret_cast<int32_t*>(ws + L.sidx);
   if (P.n_vs) {
@@ -493,17 +478,28 @@ int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int 
     ia.dfull = reinterpret_cast<uint32_t*>(vw + V.dfull);
     ia.dlist = reinterpret_cast<int*>(vw + V.dlist);
     ia.dcount = reinterpret_cast<int*>(vw + V.dcount);
+    ia.clist = reinterpret_cast<int*>(vw + V.clist);
+    ia.ccount = reinterpret_cast<int*>(vw + V.ccount);
     ia.status = status;
     vs_index_kernel<<<P.n_vs, 512, 0, st>>>(ia);
     if ((rc = launched("vertical-slash index build"))) return rc;
+    HeadList hv;
+    hv.n = P.n_vs;
+    for (int i = 0; i < P.n_vs; ++i) hv.h[i] = P.vs_head[i];
+    kc = reinterpret_cast<__nv_bfloat16*>(vw + V.kc);
+    vc = reinterpret_cast<__nv_bfloat16*>(vw + V.vc);
+    vs_colgather_kernel<<<dim3(cdiv(std::min(P.KV + kBN, MI_MAX_KV), 8), P.n_vs), 256, 0, st>>>(
+        reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), ld, group, hv,
+        ia.clist, ia.ccount, kc, vc);
+    if ((rc = launched("vertical-slash column copy"))) return rc;
     a.offbits = ia.offbits;
     a.colbits = ia.colbits;
     a.dbits = ia.dbits;
     a.dfull = ia.dfull;
     a.dlist = ia.dlist;
     a.dcount = ia.dcount;
-    a.v_idx = vidx;
-    a.k_v = P.KV;
+    a.clist = ia.clist;
+    a.ccount = ia.ccount;
     a.expand = ia.expanded;
     a.Nw = V.Nw;
     a.NT = V.NT;
@@ -556,9 +552,16 @@ int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int 
   // the attention of every listed head in one launch
   CUtensorMap mq, mk, mv, mkr, mvr;
   if ((rc = make_map(&mq, q, Hq, N, kBM, ld)) || (rc = make_map(&mk, k, Hkv, N, kBlk, ld)) ||
-      (rc = make_map(&mv, v, Hkv, N, kBlk, ld)) || (rc = make_rows_map(&mkr, k, Hkv, N, ld)) ||
-      (rc = make_rows_map(&mvr, v, Hkv, N, ld)))
+      (rc = make_map(&mv, v, Hkv, N, kBlk, ld)))
     return rc;
+  if (P.n_vs) {  // the vertical-slash heads' column tiles
+    if ((rc = make_map(&mkr, kc, P.n_vs, MI_MAX_KV, kBlk, MI_MAX_KV)) ||
+        (rc = make_map(&mvr, vc, P.n_vs, MI_MAX_KV, kBlk, MI_MAX_KV)))
+      return rc;
+  } else {
+    mkr = mk;
+    mvr = mv;
+  }
   a.N = N;
   a.ld = static_cast<int>(ld);
   a.group = group;
@@ -647,9 +650,17 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
   ia.dfull = reinterpret_cast<uint32_t*>(ws + L.dfull);
   ia.dlist = reinterpret_cast<int*>(ws + L.dlist);
   ia.dcount = reinterpret_cast<int*>(ws + L.dcount);
+  ia.clist = reinterpret_cast<int*>(ws + L.clist);
+  ia.ccount = reinterpret_cast<int*>(ws + L.ccount);
   ia.status = status;
   vs_index_kernel<<<n_heads, 512, 0, st>>>(ia);
   if ((rc = launched("vertical-slash index build"))) return rc;
+  __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(ws + L.kc);
+  __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(ws + L.vc);
+  vs_colgather_kernel<<<dim3(cdiv(std::min(k_v + kBN, MI_MAX_KV), 8), n_heads), 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), N, Hq / Hkv,
+      a.heads, ia.clist, ia.ccount, kc, vc);
+  if ((rc = launched("vertical-slash column copy"))) return rc;
 
   a.offbits = ia.offbits;
   a.colbits = ia.colbits;
@@ -657,14 +668,14 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
   a.dfull = ia.dfull;
   a.dlist = ia.dlist;
   a.dcount = ia.dcount;
-  a.v_idx = v_idx;
-  a.k_v = k_v;
+  a.clist = ia.clist;
+  a.ccount = ia.ccount;
   a.expand = expanded;
   a.Nw = L.Nw;
   a.NT = L.NT;
   a.NTw = L.NTw;
-  return expanded ? run_attention<kPatVSExp>(q, k, v, Hq, Hkv, N, out, lse, status, a, st)
-                  : run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st);
+  return expanded ? run_attention<kPatVSExp>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc)
+                  : run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc);
 }
 
 int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,

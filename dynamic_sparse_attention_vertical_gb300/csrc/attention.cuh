@@ -7,17 +7,20 @@
 //   - for block-sparse heads, tiles made of two 64-key blocks from anywhere
 //     below the diagonal (two boxes each), paired from the two 64-row halves'
 //     selections;
-//   - for vertical-slash heads, "gathered" tiles of up to 128 scattered key
-//     columns that no contiguous tile covers, loaded four rows at a time with
-//     TMA tile::gather4 into the same swizzled layout (the permutation-invariant gathering idea of PIT, which
-//     the MInference pages name as the basis of their kernels: README mirror,
-//     gittoolsai.com, "TL;DR" and the PIT note; talk slides, boteman.cn,
-//     "Dynamic Sparse Attention Calculation with PIT, FlashAttention").
+//   - for vertical-slash heads, "gathered" column tiles: the head's selected
+//     key columns are copied side by side once per call (their K and V rows,
+//     vs_colgather_kernel), and a tile is 128 consecutive entries of that
+//     compacted list, TMA-loaded like a contiguous tile and masked to the
+//     columns no contiguous tile of the row block covers (the
+//     permutation-invariant gathering idea of PIT, which the MInference pages
+//     name as the basis of their kernels: README mirror, gittoolsai.com,
+//     "TL;DR" and the PIT note; talk slides, boteman.cn, "Dynamic Sparse
+//     Attention Calculation with PIT, FlashAttention").
 //
 // Warp roles (192 threads, two CTAs per SM, up to 168 registers per thread):
 //   warps 0-3   softmax: thread t owns query row t (TMEM lane t)
 //   warp 4      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warp 5      Q (once), then K and V tiles (TMA tiles, or TMA gather4);
+//   warp 5      Q (once), then K and V tiles (TMA boxes of 64 keys);
 //               for vertical-slash heads also the rows' keep-masks
 //
 // Tensor memory (256 columns): S = Q K^T (fp32, columns 0-127) and O (fp32,
@@ -64,8 +67,8 @@ struct AttnArgs {
   const uint32_t* dfull;    // [n_heads, NTw]  bit t: a tile at distance t is kept whole
   const int* dlist;         // [n_heads, NT]   the set bits of dbits, ascending
   const int* dcount;        // [n_heads]
-  const int* v_idx;         // [n_heads, k_v]
-  int k_v;
+  const int* clist;         // [n_heads, MI_MAX_KV]  the selected columns, ascending
+  const int* ccount;        // [n_heads]
   int expand;               // block-expanded slashes: the host launches the kPatVSExp engine
   int Nw, NT, NTw;
   // block-sparse
@@ -87,7 +90,9 @@ struct AttnSmem {
   alignas(1024) uint8_t q[2][16384];
   alignas(1024) uint8_t k[2][16384];
   alignas(1024) uint8_t v[2][16384];
-  int list[MI_MAX_KV];  // VS: residual columns; block: per tile (block A << 4) | sub-block mask, block B
+  // VS: [0, 16) the column chunks with a residual column, [16, 80) the residual
+  // bits of the chunks' entries; block: per tile (block A << 4) | sub-block mask, block B
+  int list[MI_MAX_KV];
   int scan[192];
   uint32_t dfull[512];  // VS: the head's whole-tile distance bits (N <= 2^21)
   // VS: keep-masks of two tiles in flight (row i: bit c of word c / 32 keeps
@@ -101,6 +106,7 @@ struct AttnSmem {
   uint32_t tmem;
   int abort;
   int n_list;    // entries in list
+  int col_lo;    // VS: first entry of the compacted column list past tile 0
   int n_tiles;   // tiles this CTA processes
   int n_contig;  // leading contiguous tiles (VS)
   int has_t0;    // VS: tile 0 is prepended
@@ -149,7 +155,7 @@ __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a,
       }
     } else {
       ref.kind = 1;
-      ref.t = i - s.n_contig;
+      ref.t = s.list[i - s.n_contig];  // chunk of the compacted column list
     }
   } else if (PAT == kPatBlock) {
     const int e = s.list[2 * i];
@@ -260,12 +266,6 @@ template <int PAT>
 __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a, int r,
                                             const MaskRaw& m, int q, uint32_t out[4]) {
   const TileRef& ref = m.ref;
-  if (is_vs(PAT) && ref.kind == 1) {
-    const int valid = min(kBN, s.n_list - ref.t * kBN);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) out[w] = range_bits(32 * w, 0, valid);
-    return;
-  }
   const int j0 = ref.t * kBN;
   if (PAT == kPatDense) {
 #pragma unroll
@@ -357,6 +357,17 @@ template <int PAT>
 __device__ __forceinline__ void vs_masks4(const AttnSmem& s, const AttnArgs& a, int r, const VsRaw4& m,
                                           int q0, uint32_t out[4][4]) {
   const TileRef& ref = m.ref;
+  if (ref.kind == 1) {  // a column tile: the same residual bits for every row
+    const uint4 w = *reinterpret_cast<const uint4*>(&s.list[16 + 4 * ref.t]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[i][0] = w.x;
+      out[i][1] = w.y;
+      out[i][2] = w.z;
+      out[i][3] = w.w;
+    }
+    return;
+  }
   if (ref.kind == 0 && !m.whole && ref.t != r) {
     if (PAT == kPatVSExp) {
       const int d = r - ref.t;  // >= 1
@@ -455,28 +466,38 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
       s.n_contig = n_below + s.has_t0;
     }
     for (int w = tid; w < a.NTw; w += 192) s.dfull[w] = __ldg(a.dfull + (size_t)n * a.NTw + w);
-    // residual columns: selected keys in tiles 1..r-1 that no contiguous tile covers
-    const int* vi = a.v_idx + (size_t)n * a.k_v;
+    // column tiles: chunks of 128 entries of the head's compacted column list,
+    // from the first column past tile 0 (entry lo) to the last before this row
+    // block (entry hi); an entry is kept when its column is residual (no
+    // contiguous tile of this row block covers it), a chunk when it keeps one
+    const int* cl = a.clist + (size_t)n * MI_MAX_KV;
     const uint32_t* db = a.dbits + (size_t)n * a.NTw;
-    // each thread's columns are loaded at once (independent loads, then their
-    // bitmap words), kept in registers and written after the scan
-    constexpr int kPer = (MI_MAX_KV + 191) / 192;
-    const int per = cdiv(a.k_v, 192);
-    const int beg = min(tid * per, a.k_v), end = min(beg + per, a.k_v);
-    int jv[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) jv[u] = (beg + u < end) ? __ldg(vi + beg + u) : -1;
-    uint32_t keep = 0u;
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) keep |= (residual_column(jv[u], a.N, r, db) ? 1u : 0u) << u;
-    int total;
-    int pos = block_excl_scan(__popc(keep), s.scan, &total);
-#pragma unroll
-    for (int u = 0; u < kPer; ++u)
-      if ((keep >> u) & 1u) s.list[pos++] = jv[u];
+    const int cnt = __ldg(a.ccount + n);
+    uint32_t* resbits = reinterpret_cast<uint32_t*>(&s.list[16]);  // 64 words: entries lo .. lo + 2047
+    if (tid < 64) resbits[tid] = 0u;
+    int c_lo = 0, c_hi = 0;
+    for (int e = tid; e < cnt; e += 192) {
+      const int j = __ldg(cl + e);
+      c_lo += (j < kBN) ? 1 : 0;
+      c_hi += (j < r * kBN) ? 1 : 0;
+    }
+    int lo, hi;
+    block_excl_scan(c_lo, s.scan, &lo);  // (its barriers also order the resbits clear)
+    block_excl_scan(c_hi, s.scan, &hi);
+    for (int e = lo + tid; e < hi; e += 192) {
+      if (residual_column(__ldg(cl + e), a.N, r, db))
+        atomicOr(&resbits[(e - lo) >> 5], 1u << ((e - lo) & 31));
+    }
+    __syncthreads();
     if (tid == 0) {
-      s.n_list = total;
-      s.n_tiles = s.n_contig + cdiv(total, kBN);
+      int nc = 0;
+      for (int c = 0; c < cdiv(hi - lo, kBN); ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(&resbits[4 * c]);
+        if (w.x | w.y | w.z | w.w) s.list[nc++] = c;
+      }
+      s.n_list = nc;
+      s.col_lo = lo;
+      s.n_tiles = s.n_contig + nc;
     }
   } else {  // block-sparse: the two 64-row halves' selected 64-key blocks, paired into 128-key tiles
     // A tile holds any two blocks A (keys 0-63) and B (keys 64-127).  Blocks
@@ -675,20 +696,17 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
           tma_load_3d(buf[1] + 8192, map, full, 64, kb, g);
         }
       } else {
-        // up to 128 residual columns, four rows per tile::gather4 load: lane l
-        // loads rows 4l..4l+3 of both 64-column halves; rows past the list
-        // repeat its last column (their scores are masked)
-        const int* cols = s.list + ref.t * kBN;
-        const int last = min(kBN, s.n_list - ref.t * kBN) - 1;
-        const int base_row = g * a.ld;
-        if (lane_id() == 0) mbar_arrive_expect_tx(full, 2 * 16384);
-        __syncwarp();
-        const int l = lane_id();
-        int y[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) y[i] = base_row + cols[min(4 * l + i, last)];
-        tma_gather4(buf[0] + 512 * l, rows_map, full, 0, y[0], y[1], y[2], y[3]);
-        tma_gather4(buf[1] + 512 * l, rows_map, full, 64, y[0], y[1], y[2], y[3]);
+        // a column tile: 128 consecutive rows of the head's compacted K or V
+        // columns (rows_map: [listed heads, MI_MAX_KV, 128]), two 64-row boxes
+        // per 64-column half
+        if (lane_id() == 0) {
+          const int row0 = s.col_lo + ref.t * kBN;
+          mbar_arrive_expect_tx(full, 2 * 16384);
+          tma_load_3d(buf[0], rows_map, full, 0, row0, n);
+          tma_load_3d(buf[0] + 8192, rows_map, full, 0, row0 + kBlk, n);
+          tma_load_3d(buf[1], rows_map, full, 64, row0, n);
+          tma_load_3d(buf[1] + 8192, rows_map, full, 64, row0 + kBlk, n);
+        }
       }
     };
     // vertical-slash: this warp also builds the keep-masks, lane l for rows
@@ -806,7 +824,6 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
       float2 rs4[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // independent partial sums
       const float2 sl2 = make_float2(sl, sl), nmb2 = make_float2(-mb, -mb);
       const bool resc = __any_sync(0xffffffffu, rescale_o);
-#pragma unroll
       constexpr int NQ = kPChunks<PAT>, CP = 64 / NQ;  // chunks, bf16 pairs per chunk
 #pragma unroll
       for (int qq = 0; qq < NQ; ++qq) {

@@ -165,20 +165,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Four rows y0..y3 of a 2-D tensor, 64 columns from x, to `dst` as four
-// consecutive 128-byte rows (tile::gather4; the tensor map's box is 64 x 1).
-// The 128-byte swizzle follows the shared-memory address, so rows gathered to
-// dst = tile + 512 * j take the pattern of rows 4j..4j+3 of the tile.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                            int y0, int y1, int y2, int y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2),
-      "r"(y3)
-      : "memory");
-}
-
 // Generic-proxy writes to shared memory -> visible to the async proxy (UMMA, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -12,6 +12,10 @@
 //   dfull    bit delta (> 0) set when every offset a 128x128 tile at distance
 //            delta can meet, [128*delta - 127, 128*delta + 127] (within
 //            [0, N)), is selected: such a tile is kept whole for every row.
+//   clist    the valid selected columns, ascending, ccount of them; the
+//            columns' K and V rows are then copied side by side
+//            (vs_colgather_kernel), so that the attention kernel loads the
+//            column tiles with plain TMA boxes.
 // Block-expanded mode (every 64x64 block a selected diagonal crosses is kept):
 //   offbits then holds D64, bit e set for the 64-block distances e = o/64 and
 //            (o % 64 != 0) o/64 + 1 of the selected offsets, and e = 0;
@@ -40,6 +44,8 @@ struct VsIndexArgs {
   uint32_t* dfull;
   int* dlist;
   int* dcount;
+  int* clist;   // [n_heads, MI_MAX_KV]
+  int* ccount;  // [n_heads]
   int* status;
 };
 
@@ -95,6 +101,28 @@ __global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ V
   }
   if (tid == 0) atomicOr(&db[0], 1u);
   __syncthreads();
+  {
+    // the valid columns, ascending (the bitmap was just built with atomics: read
+    // back through L2); their count is at most k_v <= MI_MAX_KV
+    __shared__ int cs[512];
+    const int per = (a.Nw + 511) / 512;
+    const int w0 = min(tid * per, a.Nw), w1 = min(w0 + per, a.Nw);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(__ldcg(col + w));
+    cs[tid] = cnt;
+    __syncthreads();
+    for (int o = 1; o < 512; o <<= 1) {
+      const int y = (tid >= o) ? cs[tid - o] : 0;
+      __syncthreads();
+      cs[tid] += y;
+      __syncthreads();
+    }
+    int pos = cs[tid] - cnt;
+    int* cl = a.clist + (size_t)n * MI_MAX_KV;
+    for (int w = w0; w < w1; ++w)
+      for (uint32_t m = __ldcg(col + w); m; m &= m - 1) cl[pos++] = 32 * w + __ffs(m) - 1;
+    if (tid == 511) a.ccount[n] = cs[511];
+  }
   if (a.expanded) {
     // 128-tile distance delta: its sub-blocks sit at 64-block distances
     // 2 delta - 1 .. 2 delta + 1 (read back through L2: built with atomics)
@@ -146,6 +174,30 @@ __global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ V
   int* dl = a.dlist + (size_t)n * a.NT;
   for (uint32_t w = word; w; w &= w - 1) dl[pos++] = tid * 32 + (__ffs(w) - 1);
   if (tid == 511) a.dcount[n] = scan[511];
+}
+
+// Compacted K and V rows of the selected columns: row i of head slot n is row
+// clist[n][i] of its KV head for i < ccount[n], and zero up to the next 128
+// rows past it (a column tile starting below ccount may read that far; TMA
+// reads past MI_MAX_KV rows as zero).  One warp per row: lanes 0-15 copy K,
+// 16-31 copy V, 16 bytes each.
+__global__ void vs_colgather_kernel(const __nv_bfloat16* k, const __nv_bfloat16* v, int64_t ld, int group,
+                                    HeadList heads, const int* clist, const int* ccount,
+                                    __nv_bfloat16* kc, __nv_bfloat16* vc) {
+  const int n = blockIdx.y;
+  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int cnt = ccount[n];
+  if (i >= min(cnt + 128, MI_MAX_KV)) return;
+  const int g = heads.h[n] / group;
+  const __nv_bfloat16* src = (lane < 16) ? k : v;
+  __nv_bfloat16* dst = ((lane < 16) ? kc : vc) + ((size_t)n * MI_MAX_KV + i) * kD + (lane & 15) * 8;
+  uint4 val = make_uint4(0u, 0u, 0u, 0u);
+  if (i < cnt) {
+    const int j = clist[(size_t)n * MI_MAX_KV + i];
+    val = *reinterpret_cast<const uint4*>(src + ((size_t)g * ld + j) * kD + (lane & 15) * 8);
+  }
+  *reinterpret_cast<uint4*>(dst) = val;
 }
 
 }  // namespace mi

@@ -15,6 +15,7 @@ the column and offset indicators, done with one FFT.
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 D = 128
@@ -150,17 +151,22 @@ def vs_tiles(N: int, v_idx, s_idx, expanded: bool = False) -> int:
     r = torch.arange(NT)
     has_t0 = ~d[r]                                        # tile 0 added unless distance r is set
     contig = dcum + has_t0.long()
+    # column tiles: chunks of 128 entries of the sorted column list from the first
+    # column past tile 0 to the last before the row block; a chunk is issued when
+    # one of its columns is residual (its key tile is not at a kept distance)
     v = torch.as_tensor(v_idx).long()
-    v = v[(v >= 0) & (v < N)]
-    cols = torch.bincount(v >> 7, minlength=NT).double()  # selected columns per key tile
-    notd = (~d).double()
-    notd[0] = 0.0
-    # residual columns of row block r: sum_t cols[t] * notd[r - t] over 1 <= t < r
-    L = 1 << (2 * NT).bit_length()
-    colsx = cols.clone()
-    colsx[0] = 0.0
-    resid = torch.fft.irfft(torch.fft.rfft(colsx, L) * torch.fft.rfft(notd, L), L)[:NT].round().long()
-    return int((contig + (resid + 127) // 128).sum())
+    v = torch.unique(v[(v >= 0) & (v < N)]).numpy()
+    t = v >> 7
+    dn = d.numpy()
+    lo = int((t < 1).sum())
+    col_tiles = 0
+    for rr in range(2, NT):
+        hi = int(np.searchsorted(t, rr))  # entries with key tile < rr
+        if hi <= lo:
+            continue
+        res = ~dn[rr - t[lo:hi]]
+        col_tiles += int(np.unique(np.nonzero(res)[0] // 128).size)
+    return int(contig.sum()) + col_tiles
 
 
 def dense_tiles(N: int) -> int:

@@ -35,9 +35,22 @@ def _vs_tiles_brute(N, v, s):
     total = 0
     for r in range(NT):
         contig = {0} | {r - d for d in D if d <= r}
-        resid = [j for j in v if 1 <= (j >> 7) < r and (j >> 7) not in contig]
-        total += len(contig) + math.ceil(len(resid) / 128)
+        total += len(contig) + _column_chunks(v, r, contig)
     return total
+
+
+def _column_chunks(v, r, contig):
+    """Column tiles of row block r: 128-entry chunks of the sorted column list, counted
+    from the first column past key tile 0, up to the last column before the row block;
+    a chunk is issued when it holds a column whose key tile no contiguous tile covers."""
+    cols = sorted(v)
+    entries = [j for j in cols if 1 <= (j >> 7) < r]
+    lo = sum(1 for j in cols if (j >> 7) < 1)
+    issued = set()
+    for e, j in enumerate(cols):
+        if j in entries and (j >> 7) not in contig:
+            issued.add((e - lo) // 128)
+    return len(issued)
 
 
 @pytest.mark.parametrize("N,kv,ks,seed", [(4096, 300, 7, 0), (8192, 1000, 40, 1), (2112, 50, 0, 2)])
@@ -75,8 +88,7 @@ def _vs_expanded_tiles_brute(N, v, s):
     for r in range(NT):
         contig = {0} | {t for t in range(r + 1)
                         if any((2 * r + rh) - (2 * t + kh) in D for rh in (0, 1) for kh in (0, 1))}
-        resid = [j for j in v if 1 <= (j >> 7) < r and (j >> 7) not in contig]
-        total += len(contig) + math.ceil(len(resid) / 128)
+        total += len(contig) + _column_chunks(v, r, contig)
     return total
 
 

@@ -34,6 +34,18 @@ Three families of inputs:
     highest-scoring diagonals cluster at small offsets, the locality that real
     heads show.
 
+``grid`` (grid-planted)
+    As ``margin``, but the planted key columns are a whole lattice j = phi
+    (mod sigma): the last ``last_q`` query rows attend to it, so its columns
+    carry almost all of the vertical score.
+
+``modality`` (modality-planted, two modalities)
+    Tokens are split into runs of modality 0 and 1.  For each modality m the
+    ``last_q`` rows that end at its last token are one-hot in the dimensions
+    64 m .. 64 m + 63, and the keys of its planted columns and offsets carry
+    the planted values in those dimensions only, so each modality's window
+    selects its own planted sets with a wide margin.
+
 ``pattern heads`` (for the offline pattern search)
     Three heads, one KV head each, each shaped like one of the slides' three
     patterns: head 0 attends to a sink (the first keys) and a local window,
@@ -55,6 +67,8 @@ __all__ = [
     "margin_inputs",
     "local_inputs",
     "pattern_head_inputs",
+    "grid_inputs",
+    "modality_inputs",
     "uniform_choice",
 ]
 
@@ -323,3 +337,106 @@ def pattern_head_inputs(
     v[2] = _randn((N, d), gen, device, sd).to(torch.bfloat16)
     empty = torch.empty(0, dtype=torch.int64)
     return Inputs(q, k, v, [empty, cols, empty], [empty, offs, empty], seed, "pattern_heads")
+
+
+def grid_inputs(
+    Hq: int,
+    Hkv: int,
+    N: int,
+    sigma: int,
+    phi: int,
+    d: int = 128,
+    last_q: int = 64,
+    seed: int = 301,
+    device: str = "cpu",
+    beta: float = 8.0,
+    alpha: float = 12.0,
+) -> Inputs:
+    """Inputs whose last ``last_q`` query rows attend to the lattice j = phi (mod sigma).
+
+    Dimensions ``0..last_q`` of every lattice key are ``alpha`` and of every other key
+    zero; the last ``last_q`` query rows are ``beta * e_i``; all other values are
+    N(0, 1/d).  ``planted_cols[g]`` holds the lattice, ``planted_offsets[g]`` is empty.
+    """
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    g_per = Hq // Hkv
+    gen = _gen(device, seed)
+    sd = 1.0 / math.sqrt(d)
+    q = torch.empty((Hq, N, d), dtype=torch.bfloat16, device=device)
+    k = torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=device)
+    v = torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=device)
+    lattice = torch.arange(phi, N, sigma, dtype=torch.int64)
+    rows = torch.arange(last_q, device=device)
+    for grp in range(Hkv):
+        kf = _randn((N, d), gen, device, sd)
+        kf[:, :last_q] = 0.0
+        kf[lattice.to(device), :last_q] = alpha
+        k[grp] = kf.to(torch.bfloat16)
+        v[grp] = _randn((N, d), gen, device, sd).to(torch.bfloat16)
+        qf = _randn((g_per, N, d), gen, device, sd)
+        qf[:, N - last_q:, :] = 0.0
+        qf[:, N - last_q + rows, rows] = beta
+        q[grp * g_per:(grp + 1) * g_per] = qf.to(torch.bfloat16)
+    return Inputs(q, k, v, [lattice] * Hkv, [torch.empty(0, dtype=torch.int64)] * Hkv, seed, "grid")
+
+
+def modality_inputs(
+    Hq: int,
+    Hkv: int,
+    runs,
+    k_v: int,
+    k_s: int,
+    last_q: int = 64,
+    seed: int = 311,
+    device: str = "cpu",
+    beta: float = 8.0,
+    alpha_v: float = 9.5,
+    alpha_s: float = 8.5,
+):
+    """Two-modality inputs with planted index sets per modality (d = 128).
+
+    ``runs``: [(modality, length), ...] in token order, modalities 0 and 1.  Each
+    modality's last run must hold at least ``last_q`` tokens and the two windows of
+    ``last_q`` rows ending at the modalities' last tokens must not overlap.  Returns
+    (inputs, modality ids int32 [N] on ``device``, {m: (cols, offsets)} planted per
+    modality; the same sets for every KV head).
+    """
+    d = 128
+    mod = torch.cat([torch.full((n,), m, dtype=torch.int32) for m, n in runs])
+    N = int(mod.numel())
+    ends = {m: int(torch.nonzero(mod == m)[-1]) + 1 for m in (0, 1)}
+    for m in (0, 1):
+        if not bool((mod[ends[m] - last_q:ends[m]] == m).all()):
+            raise ValueError("each modality's last run needs at least last_q tokens")
+    if abs(ends[0] - ends[1]) < last_q:
+        raise ValueError("the two estimation windows overlap")
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    g_per = Hq // Hkv
+    gen = _gen(device, seed)
+    sd = 1.0 / math.sqrt(d)
+    planted = {}
+    for m in (0, 1):
+        R = ends[m]
+        planted[m] = (uniform_choice(k_v, 64, R - 64, gen), uniform_choice(k_s, 0, R - last_q + 1, gen))
+    q = torch.empty((Hq, N, d), dtype=torch.bfloat16, device=device)
+    k = torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=device)
+    v = torch.empty((Hkv, N, d), dtype=torch.bfloat16, device=device)
+    rows = torch.arange(last_q, device=device)
+    for grp in range(Hkv):
+        kf = torch.zeros((N, d), dtype=torch.float32, device=device)
+        qf = _randn((g_per, N, d), gen, device, sd)
+        for m in (0, 1):
+            R, dims = ends[m], 64 * m + rows
+            cols, offs = planted[m]
+            kf[cols.to(device)[:, None], dims[None, :]] += alpha_v
+            for o in offs.tolist():
+                kf[R - last_q + rows - o, dims] += alpha_s
+            qf[:, R - last_q:R, :] = 0.0
+            qf[:, R - last_q + rows, dims] = beta
+        k[grp] = kf.to(torch.bfloat16)
+        v[grp] = _randn((N, d), gen, device, sd).to(torch.bfloat16)
+        q[grp * g_per:(grp + 1) * g_per] = qf.to(torch.bfloat16)
+    x = Inputs(q, k, v, [planted[0][0]] * Hkv, [planted[0][1]] * Hkv, seed, "modality")
+    return x, mod.to(device), planted

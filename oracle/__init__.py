@@ -13,4 +13,8 @@ than itself: library routines (torch scaled-dot-product attention in fp64,
 here is "parity unpinned".
 """
 from .mi_oracle import *  # noqa: F401,F403
-from .mi_oracle import __all__  # noqa: F401
+from .mi_oracle import __all__ as _mi_all
+from .mm_oracle import *  # noqa: F401,F403
+from .mm_oracle import __all__ as _mm_all
+
+__all__ = list(_mi_all) + list(_mm_all)

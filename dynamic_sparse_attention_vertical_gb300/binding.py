@@ -32,6 +32,12 @@ MI_OP_VS_SPARSE_ATTN = 2
 MI_OP_BLOCK_SPARSE_ATTN = 3
 MI_OP_ASHAPE_ATTN = 4
 MI_OP_DENSE_CAUSAL_ATTN = 5
+MI_OP_GRID_ESTIMATE = 6
+MI_OP_GRID_ATTN = 7
+MI_OP_QBOUNDARY_ESTIMATE = 8
+MI_OP_QBOUNDARY_ATTN = 9
+MI_MAX_MODALITIES = 8
+MI_GRID_MAX_SIGMA = 4096
 MI_IDX_GIVEN = 1
 MI_VS_BLOCK_EXPANDED = 1
 MI_MAX_KV = 2048  # largest vertical budget; block-sparse top-k is at most half of it
@@ -49,6 +55,10 @@ SYMBOLS = (
     "mi_layer_attn",
     "mi_layer_workspace_bytes_varlen",
     "mi_layer_attn_varlen",
+    "mi_grid_estimate",
+    "mi_grid_attn",
+    "mi_qboundary_estimate",
+    "mi_qboundary_attn",
     "mi_read_status",
     "mi_strerror",
     "mi_debug_inject",
@@ -132,6 +142,14 @@ def load() -> ctypes.CDLL:
     lib.mi_layer_workspace_bytes_varlen.restype = S
     lib.mi_layer_attn_varlen.argtypes = [P, P, P, I, I, I, I, P, I, P, P, P, P, S, P]
     lib.mi_layer_attn_varlen.restype = I
+    lib.mi_grid_estimate.argtypes = [P, P, I, I, I, I, P, I, I, I, I, P, P, S, P]
+    lib.mi_grid_estimate.restype = I
+    lib.mi_grid_attn.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, P, S, P]
+    lib.mi_grid_attn.restype = I
+    lib.mi_qboundary_estimate.argtypes = [P, P, I, I, I, I, P, I, P, I, I, I, I, P, P, P, S, P]
+    lib.mi_qboundary_estimate.restype = I
+    lib.mi_qboundary_attn.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, I, P, I, P, P, P, S, P]
+    lib.mi_qboundary_attn.restype = I
     lib.mi_read_status.argtypes = [P, P]
     lib.mi_read_status.restype = I
     lib.mi_debug_inject.argtypes = [I, ctypes.c_uint64]
@@ -393,4 +411,79 @@ def mi_layer_attn_varlen(q, k, v, cu_seqlens, cfg, out=None, lse=None, workspace
                                      ctypes.cast(cu, ctypes.c_void_p), n, ctypes.cast(arr, ctypes.c_void_p),
                                      _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "mi_layer_attn_varlen")
+    return out
+
+
+# -------------------------------------------------------- multi-modal heads ----
+
+def mi_grid_estimate(q, k, sigma_min: int, sigma_max: int, heads=None, last_q: int = 64, grid=None,
+                     workspace=None, stream=None):
+    """(sigma, phi) of each listed grid head -> int32 [n_heads, 2] on the device."""
+    _check_qkv(q, k)
+    _check_idx(grid)
+    Hq, N, d = q.shape
+    Hkv = k.shape[0]
+    harr, n = _heads(heads, Hq)
+    if grid is None:
+        grid = torch.empty((n, 2), dtype=torch.int32, device=q.device)
+    ws = _workspace(MI_OP_GRID_ESTIMATE, n, Hkv, N, 0, 0, 0, workspace, q.device)
+    rc = load().mi_grid_estimate(_ptr(q), _ptr(k), Hq, Hkv, N, d, harr, n, last_q, sigma_min, sigma_max,
+                                 _ptr(grid), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "mi_grid_estimate")
+    return grid
+
+
+def mi_grid_attn(q, k, v, grid, sigma_min: int, heads=None, out=None, lse=None, workspace=None, stream=None):
+    """Grid attention of the listed heads with (sigma, phi) from ``grid`` (int32 [n_heads, 2])."""
+    _check_qkv(q, k, v, out)
+    _check_idx(grid)
+    Hq, N, d = q.shape
+    Hkv = k.shape[0]
+    harr, n = _heads(heads, Hq)
+    if out is None:
+        out = torch.zeros_like(q)
+    ws = _workspace(MI_OP_GRID_ATTN, n, Hkv, N, 0, 0, 0, workspace, q.device)
+    rc = load().mi_grid_attn(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, N, d, harr, n, _ptr(grid), sigma_min,
+                             _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "mi_grid_attn")
+    return out
+
+
+def mi_qboundary_estimate(q, k, modality, n_mod: int, heads=None, last_q: int = 64, k_v: int = 1000,
+                          k_s: int = 6096, v_idx=None, s_idx=None, workspace=None, stream=None):
+    """Per modality, the vertical-slash index sets of each listed head from the 64 query rows
+    ending at that modality's last token -> (v_idx [n_mod, n, k_v], s_idx [n_mod, n, k_s])."""
+    _check_qkv(q, k)
+    _check_idx(modality, v_idx, s_idx)
+    Hq, N, d = q.shape
+    Hkv = k.shape[0]
+    harr, n = _heads(heads, Hq)
+    if v_idx is None:
+        v_idx = torch.empty((n_mod, n, k_v), dtype=torch.int32, device=q.device)
+    if s_idx is None:
+        s_idx = torch.empty((n_mod, n, k_s), dtype=torch.int32, device=q.device)
+    ws = _workspace(MI_OP_QBOUNDARY_ESTIMATE, n, Hkv, N, 0, 0, 0, workspace, q.device)
+    rc = load().mi_qboundary_estimate(_ptr(q), _ptr(k), Hq, Hkv, N, d, harr, n, _ptr(modality), n_mod,
+                                      last_q, k_v, k_s, _ptr(v_idx), _ptr(s_idx), _ptr(ws), ws.numel(),
+                                      _stream(stream))
+    _raise(rc, "mi_qboundary_estimate")
+    return v_idx, s_idx
+
+
+def mi_qboundary_attn(q, k, v, modality, n_mod: int, v_idx, s_idx, heads=None, out=None, lse=None,
+                      workspace=None, stream=None):
+    """Q-boundary attention: each row with its modality's index sets (layouts as returned above)."""
+    _check_qkv(q, k, v, out)
+    _check_idx(modality, v_idx, s_idx)
+    Hq, N, d = q.shape
+    Hkv = k.shape[0]
+    harr, n = _heads(heads, Hq)
+    if out is None:
+        out = torch.zeros_like(q)
+    k_v, k_s = int(v_idx.shape[-1]), int(s_idx.shape[-1])
+    ws = _workspace(MI_OP_QBOUNDARY_ATTN, n, Hkv, N, 0, 0, 0, workspace, q.device)
+    rc = load().mi_qboundary_attn(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, N, d, harr, n, _ptr(modality), n_mod,
+                                  _ptr(v_idx), k_v, _ptr(s_idx), k_s, _ptr(out), _ptr(lse), _ptr(ws),
+                                  ws.numel(), _stream(stream))
+    _raise(rc, "mi_qboundary_attn")
     return out

@@ -13,6 +13,7 @@
 #include "attention.cuh"
 #include "block.cuh"
 #include "estimate.cuh"
+#include "mm.cuh"
 #include "select.cuh"
 #include "vs_index.cuh"
 
@@ -180,6 +181,33 @@ BlockLayout block_layout(int n_heads, int Hkv, int N) {
   return L;
 }
 
+// Multi-modal calls: grid estimation (lattice scores per sigma), grid attention
+// (lattice columns, then a vertical-slash workspace), Q-boundary estimation and
+// attention (modality ends and per-row-block modality bits, then the estimation
+// or vertical-slash workspace).
+struct MmLayout {
+  size_t status, aux, ends, blk, sub, total;
+};
+MmLayout mm_layout(int op, int n_heads, int N) {
+  MmLayout L;
+  Carve c;
+  L.status = c.take(256);
+  L.aux = L.ends = L.blk = 0;
+  if (op == MI_OP_GRID_ESTIMATE) {
+    L.aux = c.take(sizeof(float) * 2 * (size_t)n_heads * MI_GRID_MAX_SIGMA);
+    L.sub = c.take(est_layout(n_heads, N).total);
+  } else if (op == MI_OP_GRID_ATTN) {
+    L.aux = c.take(sizeof(int32_t) * (size_t)n_heads * MI_MAX_KV);
+    L.sub = c.take(vs_layout(n_heads, N).total);
+  } else {
+    L.ends = c.take(sizeof(int) * MI_MAX_MODALITIES);
+    L.blk = c.take(sizeof(uint32_t) * (size_t)cdiv(N, kBM));
+    L.sub = c.take(op == MI_OP_QBOUNDARY_ESTIMATE ? est_layout(n_heads, N).total : vs_layout(n_heads, N).total);
+  }
+  L.total = c.off;
+  return L;
+}
+
 int check_ws(void* ws, size_t ws_bytes, size_t need) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < need) return MI_ERR_WORKSPACE;
   return MI_OK;
@@ -213,7 +241,7 @@ int zero_status(int* status, cudaStream_t st) {
 template <int PAT>
 int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, int N,
                   mi_bf16* out, float* lse, int* status, AttnArgs& a, cudaStream_t st,
-                  const void* kc = nullptr, const void* vc = nullptr) {
+                  const void* kc = nullptr, const void* vc = nullptr, int n_blocks = 0) {
   CUtensorMap mq, mk, mv, mkr, mvr;
   int rc;
   if ((rc = make_map(&mq, q, Hq, N, kBM, N)) || (rc = make_map(&mk, k, Hkv, N, kBlk, N)) ||
@@ -227,6 +255,7 @@ int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, 
     mkr = mk;
     mvr = mv;
   }
+  a.q = reinterpret_cast<const __nv_bfloat16*>(q);
   a.N = N;
   a.ld = N;
   a.group = Hq / Hkv;
@@ -236,7 +265,7 @@ int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, 
   a.status = status;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.skip_q_load = g_fault_mode.load() == MI_FAULT_SKIP_Q_LOAD ? 1 : 0;
-  cudaError_t e = launch_attn<PAT>(mq, mk, mv, mkr, mvr, a, cdiv(N, kBM), st);
+  cudaError_t e = launch_attn<PAT>(mq, mk, mv, mkr, mvr, a, n_blocks > 0 ? n_blocks : cdiv(N, kBM), st);
   return e == cudaSuccess ? MI_OK : cuda_fail(e, "attention kernel");
 }
 
@@ -252,9 +281,10 @@ int attn_preamble(const void* q, const void* k, const void* v, int Hq, int Hkv, 
 
 // Estimation of the listed heads (E1, E2, T1) into rows of ld_v / ld_s entries of
 // v_idx / s_idx; ws is an est_layout(heads.n, N) workspace.
+// row_end (device int, nullable): the query rows end there instead of at N.
 int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, const HeadList& heads,
             int k_v, int k_s, int32_t* v_idx, int ld_v, int32_t* s_idx, int ld_s, char* ws,
-            int* status, cudaStream_t st) {
+            int* status, cudaStream_t st, const int* row_end = nullptr) {
   EstArgs a;
   memset(&a, 0, sizeof(a));
   a.heads = heads;
@@ -293,6 +323,7 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
   a.ssc = reinterpret_cast<float*>(ws + L.ssc);
   a.status = status;
   a.wait_limit_ns = kWaitLimitNs;
+  a.row_end = row_end;
 
   static std::once_flag once;
   static int once_rc = MI_OK;
@@ -319,6 +350,60 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
     if ((rc = launched("top-k"))) return rc;
   }
   return MI_OK;
+}
+
+// Vertical-slash attention of the listed heads (a.heads) with given indices: index
+// build, column copy, attention.  vws is a vs_layout(a.heads.n, N) workspace; errors
+// of the data go to `status`.  a's row filter (modality) and grid fields are kept.
+int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int N, AttnArgs& a,
+                const int32_t* v_idx, int k_v, const int32_t* s_idx, int k_s, int expanded,
+                mi_bf16* out, float* lse, char* vws, int* status, cudaStream_t st) {
+  int rc;
+  const int n_heads = a.heads.n;
+  const VsLayout L = vs_layout(n_heads, N);
+  char* ws = vws;
+  VsIndexArgs ia;
+  ia.N = N;
+  ia.k_v = k_v;
+  ia.k_s = k_s;
+  ia.Nw = L.Nw;
+  ia.NT = L.NT;
+  ia.NTw = L.NTw;
+  ia.expanded = expanded;
+  ia.v_idx = v_idx;
+  ia.s_idx = s_idx;
+  ia.offbits = reinterpret_cast<uint32_t*>(ws + L.offbits);
+  ia.colbits = reinterpret_cast<uint32_t*>(ws + L.colbits);
+  ia.dbits = reinterpret_cast<uint32_t*>(ws + L.dbits);
+  ia.dfull = reinterpret_cast<uint32_t*>(ws + L.dfull);
+  ia.dlist = reinterpret_cast<int*>(ws + L.dlist);
+  ia.dcount = reinterpret_cast<int*>(ws + L.dcount);
+  ia.clist = reinterpret_cast<int*>(ws + L.clist);
+  ia.ccount = reinterpret_cast<int*>(ws + L.ccount);
+  ia.status = status;
+  vs_index_kernel<<<n_heads, 512, 0, st>>>(ia);
+  if ((rc = launched("vertical-slash index build"))) return rc;
+  __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(ws + L.kc);
+  __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(ws + L.vc);
+  vs_colgather_kernel<<<dim3(cdiv(std::min(k_v + kBN, MI_MAX_KV), 8), n_heads), 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), N, Hq / Hkv,
+      a.heads, ia.clist, ia.ccount, kc, vc);
+  if ((rc = launched("vertical-slash column copy"))) return rc;
+
+  a.offbits = ia.offbits;
+  a.colbits = ia.colbits;
+  a.dbits = ia.dbits;
+  a.dfull = ia.dfull;
+  a.dlist = ia.dlist;
+  a.dcount = ia.dcount;
+  a.clist = ia.clist;
+  a.ccount = ia.ccount;
+  a.expand = expanded;
+  a.Nw = L.Nw;
+  a.NT = L.NT;
+  a.NTw = L.NTw;
+  return expanded ? run_attention<kPatVSExp>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc)
+                  : run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc);
 }
 
 // ------------------------------------------------------------ layer calls ----
@@ -575,6 +660,22 @@ int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int 
   return e == cudaSuccess ? MI_OK : cuda_fail(e, "layer attention kernel");
 }
 
+int check_modality(const int32_t* modality, int n_mod) {
+  if (!modality || n_mod < 1 || n_mod > MI_MAX_MODALITIES) return MI_ERR_ARG;
+  return MI_OK;
+}
+
+// Modality ends and per-row-block modality bits into the workspace (zeroed first).
+int modality_scan(const int32_t* modality, int N, int n_mod, char* ws, const MmLayout& L, int* status,
+                  cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ws + L.ends, 0, sizeof(int) * MI_MAX_MODALITIES, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.blk, 0, sizeof(uint32_t) * (size_t)cdiv(N, kBM), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  modality_scan_kernel<<<cdiv(N, 256), 256, 0, st>>>(modality, N, n_mod, reinterpret_cast<int*>(ws + L.ends),
+                                                     reinterpret_cast<uint32_t*>(ws + L.blk), status);
+  return launched("modality scan");
+}
+
 }  // namespace
 
 // ====================================================================== ABI ==
@@ -592,6 +693,10 @@ size_t mi_workspace_bytes(int op, int n_heads, int Hkv, int N, int k_v, int k_s,
     case MI_OP_BLOCK_SPARSE_ATTN: return Hkv > 0 ? block_layout(n_heads, Hkv, N).total : 0;
     case MI_OP_ASHAPE_ATTN:
     case MI_OP_DENSE_CAUSAL_ATTN: return 256;
+    case MI_OP_GRID_ESTIMATE:
+    case MI_OP_GRID_ATTN:
+    case MI_OP_QBOUNDARY_ESTIMATE:
+    case MI_OP_QBOUNDARY_ATTN: return mm_layout(op, n_heads, N).total;
     default: return 0;
   }
 }
@@ -634,48 +739,7 @@ int mi_vs_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
   int* status = reinterpret_cast<int*>(ws + L.status);
   if ((rc = zero_status(status, st))) return rc;
 
-  VsIndexArgs ia;
-  ia.N = N;
-  ia.k_v = k_v;
-  ia.k_s = k_s;
-  ia.Nw = L.Nw;
-  ia.NT = L.NT;
-  ia.NTw = L.NTw;
-  ia.expanded = expanded;
-  ia.v_idx = v_idx;
-  ia.s_idx = s_idx;
-  ia.offbits = reinterpret_cast<uint32_t*>(ws + L.offbits);
-  ia.colbits = reinterpret_cast<uint32_t*>(ws + L.colbits);
-  ia.dbits = reinterpret_cast<uint32_t*>(ws + L.dbits);
-  ia.dfull = reinterpret_cast<uint32_t*>(ws + L.dfull);
-  ia.dlist = reinterpret_cast<int*>(ws + L.dlist);
-  ia.dcount = reinterpret_cast<int*>(ws + L.dcount);
-  ia.clist = reinterpret_cast<int*>(ws + L.clist);
-  ia.ccount = reinterpret_cast<int*>(ws + L.ccount);
-  ia.status = status;
-  vs_index_kernel<<<n_heads, 512, 0, st>>>(ia);
-  if ((rc = launched("vertical-slash index build"))) return rc;
-  __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(ws + L.kc);
-  __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(ws + L.vc);
-  vs_colgather_kernel<<<dim3(cdiv(std::min(k_v + kBN, MI_MAX_KV), 8), n_heads), 256, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), N, Hq / Hkv,
-      a.heads, ia.clist, ia.ccount, kc, vc);
-  if ((rc = launched("vertical-slash column copy"))) return rc;
-
-  a.offbits = ia.offbits;
-  a.colbits = ia.colbits;
-  a.dbits = ia.dbits;
-  a.dfull = ia.dfull;
-  a.dlist = ia.dlist;
-  a.dcount = ia.dcount;
-  a.clist = ia.clist;
-  a.ccount = ia.ccount;
-  a.expand = expanded;
-  a.Nw = L.Nw;
-  a.NT = L.NT;
-  a.NTw = L.NTw;
-  return expanded ? run_attention<kPatVSExp>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc)
-                  : run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc);
+  return vs_attn_run(q, k, v, Hq, Hkv, N, a, v_idx, k_v, s_idx, k_s, expanded, out, lse, ws, status, st);
 }
 
 int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv,
@@ -866,6 +930,125 @@ int mi_debug_inject(int mode, uint64_t wait_limit_ns) {
     return MI_ERR_ARG;
   g_wait_limit_ns.store(wait_limit_ns);
   g_fault_mode.store(mode);
+  return MI_OK;
+}
+
+// ---------------------------------------------------- multi-modal heads ----
+
+int mi_grid_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
+                     const int32_t* heads, int n_heads, int last_q, int sigma_min, int sigma_max,
+                     int32_t* grid, void* workspace, size_t ws_bytes, mi_stream_t stream) {
+  int rc = check_device();
+  if (rc) return rc;
+  HeadList hl;
+  if ((rc = check_common(q, k, Hq, Hkv, N, d, heads, n_heads, &hl))) return rc;
+  if (last_q != kLastQ || N < kLastQ) return MI_ERR_SHAPE;
+  if (!grid || sigma_min < 1 || sigma_max < sigma_min || sigma_max > N ||
+      sigma_max - sigma_min + 1 > MI_GRID_MAX_SIGMA)
+    return MI_ERR_ARG;
+  const MmLayout L = mm_layout(MI_OP_GRID_ESTIMATE, n_heads, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+  // the vertical scores of the last 64 queries (no top-k), then the lattice fit
+  if ((rc = est_run(q, k, Hq, Hkv, N, N, hl, 0, 0, nullptr, 0, nullptr, 0, ws + L.sub, status, st))) return rc;
+  const EstLayout E = est_layout(n_heads, N);
+  const float* vsc = reinterpret_cast<const float*>(ws + L.sub + E.vsc);
+  float2* best = reinterpret_cast<float2*>(ws + L.aux);
+  const int n_sigma = sigma_max - sigma_min + 1;
+  grid_fit_kernel<<<dim3(n_sigma, n_heads), kFitThreads, 0, st>>>(vsc, N, sigma_min, n_sigma,
+                                                                 static_cast<float>(kLastQ), best);
+  if ((rc = launched("grid lattice scores"))) return rc;
+  grid_pick_kernel<<<cdiv(n_heads, 128), 128, 0, st>>>(best, n_heads, sigma_min, n_sigma, grid);
+  return launched("grid lattice choice");
+}
+
+int mi_grid_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N, int d,
+                 const int32_t* heads, int n_heads, const int32_t* grid, int sigma_min, mi_bf16* out,
+                 float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream) {
+  AttnArgs a;
+  int rc = attn_preamble(q, k, v, Hq, Hkv, N, d, heads, n_heads, out, &a);
+  if (rc) return rc;
+  if (!grid || sigma_min < 1 || sigma_min < cdiv(N, MI_MAX_KV)) return MI_ERR_ARG;
+  const MmLayout L = mm_layout(MI_OP_GRID_ATTN, n_heads, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+  // vertical lines: the lattice columns through the vertical-slash engine (no
+  // diagonals), with the first block and the own block; every row is written
+  int32_t* vidx = reinterpret_cast<int32_t*>(ws + L.aux);
+  grid_lattice_kernel<<<n_heads, 256, 0, st>>>(grid, N, sigma_min, MI_MAX_KV, vidx, status);
+  if ((rc = launched("grid lattice columns"))) return rc;
+  AttnArgs base = a;
+  if ((rc = vs_attn_run(q, k, v, Hq, Hkv, N, a, vidx, MI_MAX_KV, nullptr, 0, 0, out, lse, ws + L.sub, status, st)))
+    return rc;
+  // horizontal lines: the lattice rows, gathered 128 at a time, dense and causal;
+  // they overwrite those rows (same stream, after the pass above)
+  base.grid = grid;
+  return run_attention<kPatRows>(q, k, v, Hq, Hkv, N, out, lse, status, base, st, nullptr, nullptr,
+                                 cdiv(cdiv(N, sigma_min), kBM));
+}
+
+
+int mi_qboundary_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
+                          const int32_t* heads, int n_heads, const int32_t* modality, int n_mod,
+                          int last_q, int k_v, int k_s, int32_t* v_idx, int32_t* s_idx, void* workspace,
+                          size_t ws_bytes, mi_stream_t stream) {
+  int rc = check_device();
+  if (rc) return rc;
+  HeadList hl;
+  if ((rc = check_common(q, k, Hq, Hkv, N, d, heads, n_heads, &hl))) return rc;
+  if (last_q != kLastQ || N < kLastQ) return MI_ERR_SHAPE;
+  if ((rc = check_modality(modality, n_mod))) return rc;
+  if (k_v < 0 || k_s < 0) return MI_ERR_ARG;
+  if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
+  const MmLayout L = mm_layout(MI_OP_QBOUNDARY_ESTIMATE, n_heads, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+  if ((rc = modality_scan(modality, N, n_mod, ws, L, status, st))) return rc;
+  const int* ends = reinterpret_cast<const int*>(ws + L.ends);
+  for (int m = 0; m < n_mod; ++m) {  // one estimation per modality, its window ending at its last token
+    if ((rc = est_run(q, k, Hq, Hkv, N, N, hl, k_v, k_s, v_idx + (size_t)m * n_heads * k_v, k_v,
+                      s_idx + (size_t)m * n_heads * k_s, k_s, ws + L.sub, status, st, ends + m)))
+      return rc;
+  }
+  return MI_OK;
+}
+
+int mi_qboundary_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N, int d,
+                      const int32_t* heads, int n_heads, const int32_t* modality, int n_mod,
+                      const int32_t* v_idx, int k_v, const int32_t* s_idx, int k_s, mi_bf16* out,
+                      float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream) {
+  AttnArgs a;
+  int rc = attn_preamble(q, k, v, Hq, Hkv, N, d, heads, n_heads, out, &a);
+  if (rc) return rc;
+  if ((rc = check_modality(modality, n_mod))) return rc;
+  if (k_v < 0 || k_s < 0 || k_v > MI_MAX_KV) return MI_ERR_ARG;
+  if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
+  const MmLayout L = mm_layout(MI_OP_QBOUNDARY_ATTN, n_heads, N);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+  if ((rc = modality_scan(modality, N, n_mod, ws, L, status, st))) return rc;
+  for (int m = 0; m < n_mod; ++m) {  // each modality's rows with its own index sets
+    AttnArgs am = a;
+    am.modality = modality;
+    am.blk_mods = reinterpret_cast<const uint32_t*>(ws + L.blk);
+    am.row_mod = m;
+    if ((rc = vs_attn_run(q, k, v, Hq, Hkv, N, am, v_idx ? v_idx + (size_t)m * n_heads * k_v : nullptr, k_v,
+                          s_idx ? s_idx + (size_t)m * n_heads * k_s : nullptr, k_s, 0, out, lse, ws + L.sub,
+                          status, st)))
+      return rc;
+  }
   return MI_OK;
 }
 

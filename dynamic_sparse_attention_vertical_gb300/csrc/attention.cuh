@@ -43,12 +43,17 @@
 
 namespace mi {
 
-enum Pattern : int { kPatDense = 0, kPatVS = 1, kPatBlock = 2, kPatAShape = 3, kPatVSExp = 4 };
+enum Pattern : int { kPatDense = 0, kPatVS = 1, kPatBlock = 2, kPatAShape = 3, kPatVSExp = 4, kPatRows = 5 };
+// kPatRows: the horizontal lines of grid heads (MMInference, "Grid Head in
+// Multi-Modality"): the rows q = phi (mod sigma) gathered 128 at a time (CTA
+// "row block" r holds rows phi + sigma (128 r + i)), each attending densely to
+// its causal prefix: the permuted form of the grid's horizontal lines.
 // kPatVSExp is the vertical-slash engine with block-expanded slashes: a
 // compile-time variant of kPatVS (its heads use the kPatVS slots and arrays).
 __host__ __device__ constexpr bool is_vs(int p) { return p == kPatVS || p == kPatVSExp; }
 
 struct AttnArgs {
+  const __nv_bfloat16* q;  // grid rows: the query rows are gathered from here
   int N;
   int ld;            // rows between consecutive heads of q, k, v, out and lse (N, or a
                      // packed batch's token count)
@@ -76,6 +81,13 @@ struct AttnArgs {
   int topk;
   // A-shape
   int n_init, window;
+  // grid rows (kPatRows): (sigma, phi) per listed head
+  const int* grid;
+  // Q-boundary passes: write only the rows of modality row_mod, skip the row
+  // blocks without it (modality == nullptr: every row)
+  const int32_t* modality;  // [N]
+  const uint32_t* blk_mods;  // [ceil(N / 128)] bit m: modality m present
+  int row_mod;
   int ash_n;              // layer launches: A-shape heads with their own sizes in ash_pairs
   int ash_pairs[2 * MI_MAX_HEADS];  // [A-shape slot][2] = n_init, window
   HeadList heads;
@@ -113,6 +125,7 @@ struct AttnSmem {
   int d_cnt;     // VS: number of tile distances <= r
   int ash_init;  // A-shape: sink tokens of this head
   int ash_window;  // A-shape: window of this head
+  int g_sigma, g_phi, g_lines;  // grid rows: stride, phase, rows on the lattice
 };
 
 constexpr int kAttnThreads = 192;
@@ -143,7 +156,7 @@ template <int PAT>
 __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a, int n, int r,
                                            int i) {
   TileRef ref{0, 0, 0xF, 0};
-  if (PAT == kPatDense) {
+  if (PAT == kPatDense || PAT == kPatRows) {
     ref.t = i;
   } else if (is_vs(PAT)) {
     if (i < s.n_contig) {
@@ -267,6 +280,11 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
                                             const MaskRaw& m, int q, uint32_t out[4]) {
   const TileRef& ref = m.ref;
   const int j0 = ref.t * kBN;
+  if (PAT == kPatRows) {  // q is this row's position: keys j <= q
+#pragma unroll
+    for (int w = 0; w < 4; ++w) out[w] = range_bits(j0 + 32 * w, 0, q + 1);
+    return;
+  }
   if (PAT == kPatDense) {
 #pragma unroll
     for (int w = 0; w < 4; ++w) out[w] = 0xFFFFFFFFu;
@@ -442,6 +460,11 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
   const int tid = threadIdx.x;
   if (PAT == kPatDense) {
     if (tid == 0) s.n_tiles = r + 1;
+  } else if (PAT == kPatRows) {
+    if (tid == 0) {  // key tiles up to the block's last row
+      const int last = s.g_phi + s.g_sigma * min(r * kBM + kBM - 1, s.g_lines - 1);
+      s.n_tiles = last / kBN + 1;
+    }
   } else if (PAT == kPatAShape) {
     if (tid == 0) {
       const int t_lo = max(0, r * kBM - s.ash_window + 1) / kBN;
@@ -586,8 +609,22 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
                                              ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5;
   const int g = h / a.group;
+  // Work-free CTAs leave before any set-up (the same decision in every thread):
+  // a Q-boundary pass's row block without its modality, a grid-rows block past
+  // the head's lattice rows.
+  if (a.modality && !((__ldg(a.blk_mods + r) >> a.row_mod) & 1u)) return;
+  int g_sigma = 1, g_phi = 0, g_lines = 0;
+  if (PAT == kPatRows) {
+    g_sigma = __ldg(a.grid + 2 * n);
+    g_phi = __ldg(a.grid + 2 * n + 1);
+    if (g_sigma >= 1 && g_phi >= 0 && g_phi < g_sigma && g_phi < a.N) g_lines = (a.N - 1 - g_phi) / g_sigma + 1;
+    if (r * kBM >= g_lines) return;
+  }
 
   if (tid == 0) {
+    s.g_sigma = g_sigma;
+    s.g_phi = g_phi;
+    s.g_lines = g_lines;
     mbar_init(&s.q_full, 1);
     mbar_init(&s.k_full, 1);
     mbar_init(&s.k_empty, 1);
@@ -621,7 +658,28 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     }
   }
   __syncthreads();  // barriers initialised
-  if (tid == 160 && !a.skip_q_load) {  // Q does not depend on the tile list: load it first
+  if (PAT == kPatRows) {
+    // the lattice rows phi + sigma (128 r + i), copied by the loader warp into the
+    // 128-byte-swizzled Q tile (rows past the lattice are zero), then made
+    // visible to the tensor core's proxy
+    if (warp == 5 && !a.skip_q_load) {
+      const int l = lane_id();
+#pragma unroll 1
+      for (int i = l; i < kBM; i += 32) {
+        const bool live = r * kBM + i < g_lines;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + ((size_t)h * a.ld + (live ? g_phi + g_sigma * (r * kBM + i) : 0)) * kD);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const uint4 val = live ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(s.q[u >> 3] + sw128_offset(i, u & 7)) = val;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (l == 0) mbar_arrive(&s.q_full);
+    }
+  } else if (tid == 160 && !a.skip_q_load) {  // Q does not depend on the tile list: load it first
     mbar_arrive_expect_tx(&s.q_full, 2 * 16384);
     tma_load_3d(s.q[0], &map_q, &s.q_full, 0, r * kBM, h);
     tma_load_3d(s.q[1], &map_q, &s.q_full, 64, r * kBM, h);
@@ -752,7 +810,8 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
   } else if (warp < 4) {
     // --------------------------------------------------------- softmax ----
     const int row = tid;  // TMEM lane and row within the block
-    const int q = r * kBM + row;
+    // the row's position: the block's row, or for grid rows the lattice row
+    const int q = (PAT == kPatRows) ? g_phi + g_sigma * (r * kBM + row) : r * kBM + row;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t s_addr = tmem + lane_base, o_addr = tmem + lane_base + kTmemO;
     const float sl = a.scale_log2;
@@ -872,7 +931,8 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     if (ok && T > 0) ok = mbar_wait_warp(&s.pv_done, (T - 1) & 1, abort, lim);
     if (ok) {
       tc_fence_after();
-      const bool in_range = q < a.N;
+      const bool in_range = ((PAT == kPatRows) ? (r * kBM + row < g_lines) : (q < a.N)) &&
+                            (!a.modality || __ldg(a.modality + q) == a.row_mod);
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       __nv_bfloat16* orow = a.out + ((size_t)h * a.ld + q) * kD;
 #pragma unroll 1
@@ -916,10 +976,9 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_kr,
             const __grid_constant__ CUtensorMap map_vr, const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  const int NRB = cdiv(a.N, kBM);
   const int n = blockIdx.y;
   attn_body<PAT>(smem_raw, map_q, map_k, map_v, map_kr, map_vr, a,
-                 NRB - 1 - static_cast<int>(blockIdx.x), n, a.heads.h[n]);
+                 static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x), n, a.heads.h[n]);
 }
 
 }  // namespace mi

@@ -38,6 +38,9 @@ struct EstArgs {
   float* ssc;    // [n_heads, N]          slash scores, indexed by offset
   int* status;
   uint64_t wait_limit_ns;
+  // nullptr: the query rows are the last 64 (p_i = N - 64 + i); otherwise the
+  // rows end at *row_end (device int): p_i = R - 64 + i, R = min(max(*row_end, 64), N)
+  const int* row_end;
   HeadList heads;
   int16_t pair_a[MI_MAX_HEADS];  // list slots; pair_b = -1: single head
   int16_t pair_b[MI_MAX_HEADS];
@@ -81,6 +84,7 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int hb = slot_b >= 0 ? a.heads.h[slot_b] : ha;
   const int g = ha / a.group;
   const int N = a.N;
+  const int R = a.row_end ? min(max(__ldg(a.row_end), kLastQ), N) : N;  // one past the last query row
   const int k_lo = chunk * kChunkKeys - ((PASS == 2 && chunk > 0) ? kBN : 0);
   const int k_hi = min(N, (chunk + 1) * kChunkKeys);
   const int T = cdiv(k_hi - k_lo, kBN);
@@ -140,8 +144,8 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     if (lane_id() == 0) {
       mbar_arrive_expect_tx(&s.q_full, 4 * 8192);
       for (int c = 0; c < 2; ++c) {
-        tma_load_3d(s.q[c], &map_q, &s.q_full, 64 * c, N - kLastQ, ha);
-        tma_load_3d(s.q[c] + 8192, &map_q, &s.q_full, 64 * c, N - kLastQ, hb);
+        tma_load_3d(s.q[c], &map_q, &s.q_full, 64 * c, R - kLastQ, ha);
+        tma_load_3d(s.q[c] + 8192, &map_q, &s.q_full, 64 * c, R - kLastQ, hb);
       }
       int issued = 0;
       for (int t = 0; t < T; ++t) {
@@ -165,7 +169,7 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const int ch = (warp - 4) >> 2;
     const int hs = row >> 6, i = row & 63;
     const int slot = hs ? slot_b : slot_a;
-    const int p_i = N - kLastQ + i;  // position of this query row
+    const int p_i = R - kLastQ + i;  // position of this query row
     const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64 * ch;
     float m = -INFINITY, z = 0.f, invz = 0.f;
     if (PASS == 2 && slot >= 0) {
@@ -176,6 +180,13 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     // 0-95 take four adjacent diagonals (of head mt / 48), threads 96-255 one or
     // two key columns (of the 256 columns of both heads)
     float* sk_row = Sk + hs * kSkHead + i * (kSkPitch - 1) + 63 + 64 * ch;  // + c: key 64 ch + c
+    if (PASS == 2 && R < N) {
+      // offsets R .. N-1 meet no query row: zero, this chunk's share of them
+      for (int o = R + chunk * kChunkKeys + mt; o < min(N, R + (chunk + 1) * kChunkKeys); o += kEstMath) {
+        a.ssc[(size_t)slot_a * N + o] = 0.f;
+        if (slot_b >= 0) a.ssc[(size_t)slot_b * N + o] = 0.f;
+      }
+    }
     for (int t = 0; t < T; ++t) {
       const int b = t & 1;
       // On a failed (timed-out) wait the loop still runs to the end with zeros, so
@@ -242,8 +253,8 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             float v = d4[u];
             if (e < 63) v += cin[hh * 64 + e];
             if (e < 128) {
-              const int d = j0 + e;
-              if (!halo && sl >= 0 && d < N) a.ssc[(size_t)sl * N + (N - 1 - d)] = v;
+              const int d = j0 + e;  // offset R - 1 - d (a key past R - 1 has no row: o < 0)
+              if (!halo && sl >= 0 && d < R) a.ssc[(size_t)sl * N + (R - 1 - d)] = v;
             } else if (e < 191) {
               cout[hh * 64 + (e - 128)] = v;
             }

@@ -74,6 +74,8 @@ typedef struct CUstream_st* mi_stream_t; /* a cudaStream_t */
 #define MI_LAST_Q 64
 #define MI_BLOCK 64
 #define MI_MAX_KV 2048 /* largest vertical budget the sparse attention kernel accepts */
+#define MI_MAX_MODALITIES 8    /* modalities a Q-boundary call accepts */
+#define MI_GRID_MAX_SIGMA 4096 /* largest stride range a grid estimation scans */
 
 /* ops for mi_workspace_bytes */
 #define MI_OP_VS_ESTIMATE 1
@@ -81,6 +83,10 @@ typedef struct CUstream_st* mi_stream_t; /* a cudaStream_t */
 #define MI_OP_BLOCK_SPARSE_ATTN 3
 #define MI_OP_ASHAPE_ATTN 4
 #define MI_OP_DENSE_CAUSAL_ATTN 5
+#define MI_OP_GRID_ESTIMATE 6
+#define MI_OP_GRID_ATTN 7
+#define MI_OP_QBOUNDARY_ESTIMATE 8
+#define MI_OP_QBOUNDARY_ATTN 9
 
 /* flags for mi_block_sparse_attn */
 #define MI_IDX_GIVEN 1
@@ -244,6 +250,75 @@ int mi_layer_attn_varlen(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
                          int total, int d, const int32_t* cu_seqlens, int n_seqs,
                          const mi_head_cfg* cfg, mi_bf16* out, float* lse, void* workspace,
                          size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * Multi-modal heads (MMInference).  README mirror, "TL;DR": modality-aware,
+ * permutation-based sparse attention for the grid pattern of visual inputs and
+ * for the modality boundaries of mixed inputs.  Slides: "MMInference: Grid Head
+ * in Multi-Modality" (horizontal and vertical lines, evenly spaced, often
+ * symmetrical; stride and starting position vary with the context) and
+ * "MMInference: Q-Boundary pattern" (intra-modality consistency).
+ *
+ * Grid head: one lattice L = {j : j = phi (mod sigma)} gives both the vertical
+ * lines and the horizontal lines.  Row q keeps key j iff j <= q and (j < 64 or
+ * j/64 == q/64 or j in L or q in L): a row on the lattice keeps its whole
+ * causal row.
+ *
+ * mi_grid_estimate: (sigma, phi) per listed head from the vertical scores v of
+ * the last 64 queries (as in mi_vs_estimate): the lattice with the largest
+ * E(sigma, phi) = sum over j in L of v[j] - |L| * 64 / N over
+ * sigma_min <= sigma <= sigma_max and 0 <= phi < sigma; ties go to the smaller
+ * sigma, then the smaller phi (fp32 scores).  grid: DEVICE int32 [n_heads, 2]
+ * = (sigma, phi).  1 <= sigma_min <= sigma_max <= N and
+ * sigma_max - sigma_min < MI_GRID_MAX_SIGMA, else MI_ERR_ARG; last_q must be 64.
+ * Workspace: mi_workspace_bytes(MI_OP_GRID_ESTIMATE, n_heads, Hkv, N, 0, 0, 0).
+ */
+int mi_grid_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
+                     const int32_t* heads, int n_heads, int last_q, int sigma_min, int sigma_max,
+                     int32_t* grid, void* workspace, size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * mi_grid_attn: grid attention with given (sigma, phi) (DEVICE int32 [n_heads, 2],
+ * e.g. from mi_grid_estimate).  The vertical lines run as vertical-slash columns;
+ * the horizontal lines are gathered 128 rows at a time (the "permuted grid")
+ * and attend densely to their causal prefix.  sigma_min is a lower bound on
+ * every head's sigma, at least ceil(N / MI_MAX_KV) (at most MI_MAX_KV lattice
+ * columns), else MI_ERR_ARG; a (sigma, phi) below it or with phi outside
+ * [0, sigma) sets MI_ERR_INDEX in the status word and that head's lattice is
+ * left out.  Workspace: mi_workspace_bytes(MI_OP_GRID_ATTN, n_heads, Hkv, N, 0, 0, 0).
+ */
+int mi_grid_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N, int d,
+                 const int32_t* heads, int n_heads, const int32_t* grid, int sigma_min, mi_bf16* out,
+                 float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * Q-Boundary head: every token j carries a modality id modality[j] in
+ * [0, n_mod) (DEVICE int32 [N], n_mod <= MI_MAX_MODALITIES), and a query row
+ * follows the vertical-slash pattern of its own modality.
+ *
+ * mi_qboundary_estimate: for each modality m, the vertical-slash estimation of
+ * mi_vs_estimate with the 64 query rows that end at the last token of m (rows
+ * R - 64 .. R - 1, R = max(one past that token, 64)); v_idx [n_mod, n_heads, k_v]
+ * and s_idx [n_mod, n_heads, k_s] DEVICE int32, each row as mi_vs_estimate
+ * writes it.  An id outside [0, n_mod) sets MI_ERR_INDEX in the status word.
+ * Workspace: mi_workspace_bytes(MI_OP_QBOUNDARY_ESTIMATE, n_heads, Hkv, N, 0, 0, 0).
+ */
+int mi_qboundary_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N, int d,
+                          const int32_t* heads, int n_heads, const int32_t* modality, int n_mod,
+                          int last_q, int k_v, int k_s, int32_t* v_idx, int32_t* s_idx, void* workspace,
+                          size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * mi_qboundary_attn: row q of modality m keeps what mi_vs_sparse_attn (exact
+ * diagonals) keeps with v_idx[m] / s_idx[m] (layouts as above, original token
+ * positions).  One vertical-slash pass per modality writes that modality's rows;
+ * row blocks without it are skipped.  Index errors as mi_vs_sparse_attn.
+ * Workspace: mi_workspace_bytes(MI_OP_QBOUNDARY_ATTN, n_heads, Hkv, N, 0, 0, 0).
+ */
+int mi_qboundary_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N, int d,
+                      const int32_t* heads, int n_heads, const int32_t* modality, int n_mod,
+                      const int32_t* v_idx, int k_v, const int32_t* s_idx, int k_s, mi_bf16* out,
+                      float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream);
 
 /*
  * mi_vs_estimate_noalloc: mi_vs_estimate for callers that cannot allocate device

@@ -31,6 +31,15 @@ vertical-slash pattern of its own modality.  The index sets of modality m are
 estimated, as for a vertical-slash head, from the ``last_q`` query rows that
 end at the last token of modality m (the first ``last_q`` rows when that token
 comes earlier), over all keys in original positions.
+
+2D-Boundary head (slides, "MMInference: 2D-Boundary pattern"; the boundary
+splits both axes).  Each modality's tokens, taken in order, form a
+sub-sequence of their own, in which the modality is a vertical-slash head:
+its index sets are estimated from the sub-sequence's last ``last_q`` tokens
+and its columns, offsets, first block and own block are counted in the
+sub-sequence's positions (so a diagonal continues across the other modality's
+tokens: "modality-separated continuity").  A query keeps every key of another
+modality before it (the cross-modality blocks are kept whole).
 """
 from __future__ import annotations
 
@@ -49,6 +58,9 @@ __all__ = [
     "grid_fit",
     "grid_estimate",
     "grid_mask_rows",
+    "modality_positions",
+    "boundary2d_estimate",
+    "boundary2d_mask_rows",
 ]
 
 
@@ -144,3 +156,59 @@ def grid_mask_rows(N: int, rows, sigma: int, phi: int, blk: int = BLK) -> np.nda
     j = np.arange(N, dtype=np.int64)[None, :]
     keep = (j < blk) | ((j // blk) == (r // blk)) | ((j % sigma) == phi) | ((r % sigma) == phi)
     return (j <= r) & keep
+
+
+# ---------------------------------------------------------------------------
+# 2D-Boundary: each modality a vertical-slash head in its own sub-sequence
+# ---------------------------------------------------------------------------
+
+def modality_positions(modality) -> np.ndarray:
+    """Position of every token inside its modality's sub-sequence (0-based rank)."""
+    mod = np.asarray(modality)
+    pos = np.zeros(mod.shape[0], dtype=np.int64)
+    for m in np.unique(mod):
+        idx = np.nonzero(mod == m)[0]
+        pos[idx] = np.arange(idx.size)
+    return pos
+
+
+def boundary2d_estimate(q_h, k_g, modality, n_mod: int, last_q: int, k_v: int, k_s: int):
+    """Per modality m: (v_idx_m, s_idx_m) of the vertical-slash estimation of its own
+    sub-sequence (positions inside the sub-sequence)."""
+    from .mi_oracle import vs_estimate
+    mod = np.asarray(modality)
+    q_h = as_f64(q_h)
+    k_g = as_f64(k_g)
+    out = []
+    for m in range(n_mod):
+        idx = np.nonzero(mod == m)[0]
+        if idx.size < last_q:
+            out.append((np.zeros(0, dtype=np.int64), np.zeros(0, dtype=np.int64)))
+            continue
+        vi, si, _, _ = vs_estimate(q_h[idx], k_g[idx], last_q, k_v, k_s)
+        out.append((vi, si))
+    return out
+
+
+def boundary2d_mask_rows(N: int, rows, modality, idx_sets, blk: int = BLK, min_len: int = 64) -> np.ndarray:
+    """Row q (modality a, sub-sequence position p) keeps key j <= q when j has another
+    modality, or when j has modality a and the vertical-slash rule with idx_sets[a] keeps
+    sub-sequence positions (p, pos(j)).  A modality with fewer than ``min_len`` tokens
+    (too short to estimate) keeps its whole causal sub-sequence."""
+    rows = np.asarray(rows, dtype=np.int64)
+    mod = np.asarray(modality)
+    pos = modality_positions(mod)
+    out = np.zeros((rows.shape[0], N), dtype=bool)
+    for n, q in enumerate(rows):
+        a = int(mod[q])
+        same = np.nonzero(mod[: q + 1] == a)[0]
+        cross = np.nonzero(mod[: q + 1] != a)[0]
+        out[n, cross] = True
+        Na = int((mod == a).sum())
+        if Na < min_len:
+            out[n, same] = True
+            continue
+        v_idx, s_idx = idx_sets[a]
+        keep = vs_mask_rows(Na, [pos[q]], v_idx, s_idx, blk=blk)[0]
+        out[n, same] = keep[pos[same]]
+    return out

@@ -116,3 +116,44 @@ def test_grid_fit_closed_forms():
 def test_grid_estimate_recovers_a_planted_lattice(sigma, phi):
     x = I.grid_inputs(1, 1, 4096, sigma, phi, seed=sigma)
     assert O.grid_estimate(x.q[0], x.k[0], 64, 16, 160) == (sigma, phi)
+
+
+def test_boundary2d_mask_hand_worked():
+    fx = read_fixture("boundary2d_mask_n8_blk1.txt")
+    N, blk = int(fx["N"][0]), int(fx["blk"][0])
+    sets = [(_ints(fx["V0"]), _ints(fx["S0"])), (_ints(fx["V1"]), _ints(fx["S1"]))]
+    got = O.boundary2d_mask_rows(N, np.arange(N), _ints(fx["modality"]), sets, blk=blk, min_len=0)
+    np.testing.assert_array_equal(got, fx["mask"])
+
+
+def test_boundary2d_mask_with_one_modality_is_the_vertical_slash_mask():
+    rng = np.random.default_rng(1)
+    N = 300
+    v = np.sort(rng.choice(N, 9, replace=False))
+    s = np.sort(rng.choice(N, 7, replace=False))
+    got = O.boundary2d_mask_rows(N, np.arange(N), np.zeros(N, dtype=np.int64), [(v, s)])
+    np.testing.assert_array_equal(got, O.vs_mask_rows(N, np.arange(N), v, s))
+
+
+def test_boundary2d_estimate_recovers_sets_planted_in_each_sub_sequence():
+    """Closed form: two margin-planted sequences (planted sets in their own positions),
+    interleaved by runs into one input, are recovered per modality."""
+    a = I.margin_inputs(1, 1, 1024, 16, 12, seed=21)
+    b = I.margin_inputs(1, 1, 768, 10, 8, seed=22)
+    runs = [(0, 300), (1, 200), (0, 500), (1, 568), (0, 224)]
+    mod = np.concatenate([np.full(n, m) for m, n in runs])
+    q = torch.empty((1792, 128), dtype=torch.bfloat16)
+    k = torch.empty((1792, 128), dtype=torch.bfloat16)
+    q[mod == 0], k[mod == 0] = a.q[0], a.k[0]
+    q[mod == 1], k[mod == 1] = b.q[0], b.k[0]
+    got = O.boundary2d_estimate(q, k, mod, 2, 64, 16, 12)
+    assert got[0][0].tolist() == a.planted_cols[0].tolist()
+    assert got[0][1].tolist() == a.planted_offsets[0].tolist()
+    got = O.boundary2d_estimate(q, k, mod, 2, 64, 10, 8)
+    assert got[1][0].tolist() == b.planted_cols[0].tolist()
+    assert got[1][1].tolist() == b.planted_offsets[0].tolist()
+
+
+def test_modality_positions():
+    np.testing.assert_array_equal(O.modality_positions(np.array([0, 1, 0, 0, 1, 0, 1, 0])),
+                                  [0, 0, 1, 2, 1, 3, 2, 4])

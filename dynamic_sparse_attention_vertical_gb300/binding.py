@@ -36,6 +36,8 @@ MI_OP_GRID_ESTIMATE = 6
 MI_OP_GRID_ATTN = 7
 MI_OP_QBOUNDARY_ESTIMATE = 8
 MI_OP_QBOUNDARY_ATTN = 9
+MI_OP_BOUNDARY2D_ATTN = 10
+MI_MAX_RUNS = 64
 MI_MAX_MODALITIES = 8
 MI_GRID_MAX_SIGMA = 4096
 MI_IDX_GIVEN = 1
@@ -59,6 +61,7 @@ SYMBOLS = (
     "mi_grid_attn",
     "mi_qboundary_estimate",
     "mi_qboundary_attn",
+    "mi_boundary2d_attn",
     "mi_read_status",
     "mi_strerror",
     "mi_debug_inject",
@@ -150,6 +153,8 @@ def load() -> ctypes.CDLL:
     lib.mi_qboundary_estimate.restype = I
     lib.mi_qboundary_attn.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, I, P, I, P, P, P, S, P]
     lib.mi_qboundary_attn.restype = I
+    lib.mi_boundary2d_attn.argtypes = [P, P, P, I, I, I, I, P, I, I, I, P, P, I, P, P, P, S, P]
+    lib.mi_boundary2d_attn.restype = I
     lib.mi_read_status.argtypes = [P, P]
     lib.mi_read_status.restype = I
     lib.mi_debug_inject.argtypes = [I, ctypes.c_uint64]
@@ -487,3 +492,29 @@ def mi_qboundary_attn(q, k, v, modality, n_mod: int, v_idx, s_idx, heads=None, o
                                   ws.numel(), _stream(stream))
     _raise(rc, "mi_qboundary_attn")
     return out
+
+
+def mi_boundary2d_attn(q, k, v, runs, k_v: int = 1000, k_s: int = 6096, v_idx=None, s_idx=None,
+                       given: bool = False, out=None, lse=None, workspace=None, stream=None):
+    """2D-boundary attention of every q-head over two modalities given as ``runs``
+    [(modality 0|1, length), ...] in token order -> (out, v_idx [2, Hq, k_v], s_idx [2, Hq, k_s]);
+    with ``given`` the index sets (sub-sequence positions) are read instead of estimated."""
+    _check_qkv(q, k, v, out)
+    _check_idx(v_idx, s_idx)
+    Hq, N, d = q.shape
+    Hkv = k.shape[0]
+    flat = [int(x) for r in runs for x in r]
+    rarr = (ctypes.c_int32 * len(flat))(*flat)
+    if out is None:
+        out = torch.zeros_like(q)
+    if v_idx is None:
+        v_idx = torch.full((2, Hq, k_v), -1, dtype=torch.int32, device=q.device)
+    if s_idx is None:
+        s_idx = torch.full((2, Hq, k_s), -1, dtype=torch.int32, device=q.device)
+    k_v, k_s = int(v_idx.shape[-1]), int(s_idx.shape[-1])
+    ws = _workspace(MI_OP_BOUNDARY2D_ATTN, Hq, Hkv, N, 0, 0, 0, workspace, q.device)
+    rc = load().mi_boundary2d_attn(_ptr(q), _ptr(k), _ptr(v), Hq, Hkv, N, d, rarr, len(runs), k_v, k_s,
+                                   _ptr(v_idx), _ptr(s_idx), MI_IDX_GIVEN if given else 0, _ptr(out), _ptr(lse),
+                                   _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "mi_boundary2d_attn")
+    return out, v_idx, s_idx

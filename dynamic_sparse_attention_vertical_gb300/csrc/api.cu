@@ -186,9 +186,9 @@ BlockLayout block_layout(int n_heads, int Hkv, int N) {
 // attention (modality ends and per-row-block modality bits, then the estimation
 // or vertical-slash workspace).
 struct MmLayout {
-  size_t status, aux, ends, blk, sub, total;
+  size_t status, aux, ends, blk, sub, vsw, qp, kp, vp, op, lse1, lse2, total;
 };
-MmLayout mm_layout(int op, int n_heads, int N) {
+MmLayout mm_layout(int op, int n_heads, int N, int Hkv = 0) {
   MmLayout L;
   Carve c;
   L.status = c.take(256);
@@ -199,6 +199,19 @@ MmLayout mm_layout(int op, int n_heads, int N) {
   } else if (op == MI_OP_GRID_ATTN) {
     L.aux = c.take(sizeof(int32_t) * (size_t)n_heads * MI_MAX_KV);
     L.sub = c.take(vs_layout(n_heads, N).total);
+  } else if (op == MI_OP_BOUNDARY2D_ATTN) {
+    // n_heads is Hq here: the permuted copy holds every q-head
+    L.ends = 0;
+    L.blk = c.take(sizeof(uint32_t) * 4 * (size_t)cdiv(N, kBM));              // modality bits (whole tiles)
+    L.aux = c.take(sizeof(uint32_t) * (size_t)cdiv(N, kBM));                  // modalities per 128 tokens
+    L.sub = c.take(est_layout(n_heads, N).total);                             // estimation
+    L.vsw = c.take(vs_layout(n_heads, N).total);                              // vertical-slash passes
+    L.qp = c.take(sizeof(uint16_t) * kD * (size_t)n_heads * N);               // permuted q, k, v, o
+    L.kp = c.take(sizeof(uint16_t) * kD * (size_t)std::max(Hkv, 1) * N);
+    L.vp = c.take(sizeof(uint16_t) * kD * (size_t)std::max(Hkv, 1) * N);
+    L.op = c.take(sizeof(uint16_t) * kD * (size_t)n_heads * N);
+    L.lse1 = c.take(sizeof(float) * (size_t)n_heads * N);                     // within-modality lse
+    L.lse2 = c.take(sizeof(float) * (size_t)n_heads * N);                     // cross-modality lse
   } else {
     L.ends = c.take(sizeof(int) * MI_MAX_MODALITIES);
     L.blk = c.take(sizeof(uint32_t) * (size_t)cdiv(N, kBM));
@@ -241,11 +254,12 @@ int zero_status(int* status, cudaStream_t st) {
 template <int PAT>
 int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, int N,
                   mi_bf16* out, float* lse, int* status, AttnArgs& a, cudaStream_t st,
-                  const void* kc = nullptr, const void* vc = nullptr, int n_blocks = 0) {
+                  const void* kc = nullptr, const void* vc = nullptr, int n_blocks = 0, int64_t ld = 0) {
   CUtensorMap mq, mk, mv, mkr, mvr;
   int rc;
-  if ((rc = make_map(&mq, q, Hq, N, kBM, N)) || (rc = make_map(&mk, k, Hkv, N, kBlk, N)) ||
-      (rc = make_map(&mv, v, Hkv, N, kBlk, N)))
+  if (ld <= 0) ld = N;  // rows between heads (a sequence inside a longer buffer: that buffer's rows)
+  if ((rc = make_map(&mq, q, Hq, N, kBM, ld)) || (rc = make_map(&mk, k, Hkv, N, kBlk, ld)) ||
+      (rc = make_map(&mv, v, Hkv, N, kBlk, ld)))
     return rc;
   if (is_vs(PAT)) {  // column tiles
     if ((rc = make_map(&mkr, kc, a.heads.n, MI_MAX_KV, kBlk, MI_MAX_KV)) ||
@@ -257,7 +271,7 @@ int run_attention(const void* q, const void* k, const void* v, int Hq, int Hkv, 
   }
   a.q = reinterpret_cast<const __nv_bfloat16*>(q);
   a.N = N;
-  a.ld = N;
+  a.ld = static_cast<int>(ld);
   a.group = Hq / Hkv;
   a.scale_log2 = kScaleLog2;
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
@@ -357,7 +371,8 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
 // of the data go to `status`.  a's row filter (modality) and grid fields are kept.
 int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int N, AttnArgs& a,
                 const int32_t* v_idx, int k_v, const int32_t* s_idx, int k_s, int expanded,
-                mi_bf16* out, float* lse, char* vws, int* status, cudaStream_t st) {
+                mi_bf16* out, float* lse, char* vws, int* status, cudaStream_t st, int64_t ld = 0) {
+  if (ld <= 0) ld = N;
   int rc;
   const int n_heads = a.heads.n;
   const VsLayout L = vs_layout(n_heads, N);
@@ -386,7 +401,7 @@ int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, in
   __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(ws + L.kc);
   __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(ws + L.vc);
   vs_colgather_kernel<<<dim3(cdiv(std::min(k_v + kBN, MI_MAX_KV), 8), n_heads), 256, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), N, Hq / Hkv,
+      reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), ld, Hq / Hkv,
       a.heads, ia.clist, ia.ccount, kc, vc);
   if ((rc = launched("vertical-slash column copy"))) return rc;
 
@@ -402,8 +417,8 @@ int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, in
   a.Nw = L.Nw;
   a.NT = L.NT;
   a.NTw = L.NTw;
-  return expanded ? run_attention<kPatVSExp>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc)
-                  : run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc);
+  return expanded ? run_attention<kPatVSExp>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc, 0, ld)
+                  : run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc, 0, ld);
 }
 
 // ------------------------------------------------------------ layer calls ----
@@ -697,6 +712,7 @@ size_t mi_workspace_bytes(int op, int n_heads, int Hkv, int N, int k_v, int k_s,
     case MI_OP_GRID_ATTN:
     case MI_OP_QBOUNDARY_ESTIMATE:
     case MI_OP_QBOUNDARY_ATTN: return mm_layout(op, n_heads, N).total;
+    case MI_OP_BOUNDARY2D_ATTN: return Hkv > 0 ? mm_layout(op, n_heads, N, Hkv).total : 0;
     default: return 0;
   }
 }
@@ -1050,6 +1066,99 @@ int mi_qboundary_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
       return rc;
   }
   return MI_OK;
+}
+
+int mi_boundary2d_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N, int d,
+                       const int32_t* runs, int n_runs, int k_v, int k_s, int32_t* v_idx, int32_t* s_idx,
+                       int flags, mi_bf16* out, float* lse, void* workspace, size_t ws_bytes,
+                       mi_stream_t stream) {
+  AttnArgs a;
+  int rc = attn_preamble(q, k, v, Hq, Hkv, N, d, nullptr, Hq, out, &a);
+  if (rc) return rc;
+  if (flags & ~MI_IDX_GIVEN) return MI_ERR_UNIMPLEMENTED;
+  if (!runs || n_runs < 1 || n_runs > MI_MAX_RUNS) return MI_ERR_ARG;
+  if (k_v < 0 || k_s < 0 || k_v > MI_MAX_KV) return MI_ERR_ARG;
+  if ((k_v > 0 && !v_idx) || (k_s > 0 && !s_idx)) return MI_ERR_ARG;
+  // the runs: original starts, and permuted starts (modality 0's tokens first)
+  RunTable rt;
+  rt.n = n_runs;
+  int seg[2] = {0, 0};
+  int64_t total = 0;
+  for (int u = 0; u < n_runs; ++u) {
+    const int m = runs[2 * u], len = runs[2 * u + 1];
+    if ((m != 0 && m != 1) || len < 1) return MI_ERR_ARG;
+    rt.start[u] = static_cast<int>(total);
+    rt.len[u] = len;
+    rt.mod[u] = m;
+    total += len;
+    if (total > N) return MI_ERR_ARG;
+    seg[m] += len;
+  }
+  if (total != N) return MI_ERR_ARG;
+  {
+    int at[2] = {0, seg[0]};
+    for (int u = 0; u < n_runs; ++u) {
+      rt.pstart[u] = at[rt.mod[u]];
+      at[rt.mod[u]] += rt.len[u];
+    }
+  }
+  const MmLayout L = mm_layout(MI_OP_BOUNDARY2D_ATTN, Hq, N, Hkv);
+  if ((rc = check_ws(workspace, ws_bytes, L.total))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  if ((rc = zero_status(status, st))) return rc;
+  uint32_t* modbits = reinterpret_cast<uint32_t*>(ws + L.blk);
+  uint32_t* mods128 = reinterpret_cast<uint32_t*>(ws + L.aux);
+  cudaError_t e = cudaMemsetAsync(modbits, 0, sizeof(uint32_t) * 4 * (size_t)cdiv(N, kBM), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(mods128, 0, sizeof(uint32_t) * (size_t)cdiv(N, kBM), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  boundary_bits_kernel<<<cdiv(N, 256), 256, 0, st>>>(N, rt, modbits, mods128);
+  if ((rc = launched("modality bits"))) return rc;
+  __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(ws + L.qp);
+  __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(ws + L.kp);
+  __nv_bfloat16* vp = reinterpret_cast<__nv_bfloat16*>(ws + L.vp);
+  __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(ws + L.op);
+  float* lse1 = reinterpret_cast<float*>(ws + L.lse1);
+  float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
+  const int64_t rows = (int64_t)(Hq + 2 * Hkv) * N;
+  boundary_gather_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
+      reinterpret_cast<const __nv_bfloat16*>(v), Hq, Hkv, N, rt, qp, kp, vp);
+  if ((rc = launched("modality permutation"))) return rc;
+  // each modality's sub-sequence as a vertical-slash head of its own (rows N apart);
+  // one too short to estimate (fewer than 64 tokens) is dense
+  for (int m = 0; m < 2; ++m) {
+    const int n_m = seg[m], off = m ? seg[0] : 0;
+    if (n_m == 0) continue;
+    const size_t eo = (size_t)off * kD;
+    AttnArgs am = a;
+    int32_t* vm = v_idx ? v_idx + (size_t)m * Hq * k_v : nullptr;
+    int32_t* sm = s_idx ? s_idx + (size_t)m * Hq * k_s : nullptr;
+    if (n_m >= kLastQ) {
+      if (!(flags & MI_IDX_GIVEN) &&
+          (rc = est_run(qp + eo, kp + eo, Hq, Hkv, n_m, N, a.heads, k_v, k_s, vm, k_v, sm, k_s, ws + L.sub,
+                        status, st)))
+        return rc;
+      if ((rc = vs_attn_run(qp + eo, kp + eo, vp + eo, Hq, Hkv, n_m, am, vm, k_v, sm, k_s, 0,
+                            reinterpret_cast<mi_bf16*>(op + eo), lse1 + off, ws + L.vsw, status, st, N)))
+        return rc;
+    } else {
+      if ((rc = run_attention<kPatDense>(qp + eo, kp + eo, vp + eo, Hq, Hkv, n_m,
+                                         reinterpret_cast<mi_bf16*>(op + eo), lse1 + off, status, am, st,
+                                         nullptr, nullptr, 0, N)))
+        return rc;
+    }
+  }
+  // the cross-modality pairs in original positions, into out / lse2
+  AttnArgs ax = a;
+  ax.modbits = modbits;
+  ax.mods128 = mods128;
+  if ((rc = run_attention<kPatCross>(q, k, v, Hq, Hkv, N, out, lse2, status, ax, st))) return rc;
+  const int64_t mrows = (int64_t)Hq * N;
+  boundary_merge_kernel<<<static_cast<unsigned>((mrows + 7) / 8), 256, 0, st>>>(
+      N, rt, a.heads, op, lse1, lse2, reinterpret_cast<__nv_bfloat16*>(out), lse);
+  return launched("2D-boundary merge");
 }
 
 int mi_read_status(const void* workspace, mi_stream_t stream) {

@@ -43,7 +43,12 @@
 
 namespace mi {
 
-enum Pattern : int { kPatDense = 0, kPatVS = 1, kPatBlock = 2, kPatAShape = 3, kPatVSExp = 4, kPatRows = 5 };
+enum Pattern : int {
+  kPatDense = 0, kPatVS = 1, kPatBlock = 2, kPatAShape = 3, kPatVSExp = 4, kPatRows = 5, kPatCross = 6
+};
+// kPatCross: the cross-modality pairs of 2D-boundary heads (two modalities):
+// row q keeps key j <= q of the other modality; only the key tiles holding the
+// other modality of some row of the block are visited.
 // kPatRows: the horizontal lines of grid heads (MMInference, "Grid Head in
 // Multi-Modality"): the rows q = phi (mod sigma) gathered 128 at a time (CTA
 // "row block" r holds rows phi + sigma (128 r + i)), each attending densely to
@@ -88,6 +93,10 @@ struct AttnArgs {
   const int32_t* modality;  // [N]
   const uint32_t* blk_mods;  // [ceil(N / 128)] bit m: modality m present
   int row_mod;
+  // 2D-boundary cross pass (kPatCross): bit j of modbits = token j is of
+  // modality 1; mods128[t] bit m = 128-token block t holds modality m
+  const uint32_t* modbits;
+  const uint32_t* mods128;
   int ash_n;              // layer launches: A-shape heads with their own sizes in ash_pairs
   int ash_pairs[2 * MI_MAX_HEADS];  // [A-shape slot][2] = n_init, window
   HeadList heads;
@@ -170,6 +179,15 @@ __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a,
       ref.kind = 1;
       ref.t = s.list[i - s.n_contig];  // chunk of the compacted column list
     }
+  } else if (PAT == kPatCross) {
+    // intervals of consecutive tiles: list[2 k] first tile, list[2 k + 1] count,
+    // list[128 + k] tiles before interval k (binary search for the one holding i)
+    int lo = 0, hi = s.n_list - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s.list[128 + mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    ref.t = s.list[2 * lo] + (i - s.list[128 + lo]);
   } else if (PAT == kPatBlock) {
     const int e = s.list[2 * i];
     ref.t = e >> 4;
@@ -205,12 +223,16 @@ struct MaskRaw {
 
 // Dense, block-sparse and A-shape tiles: the reference is all a mask needs.
 template <int PAT>
-__device__ __forceinline__ MaskRaw mask_fetch(const TileRef& ref) {
+__device__ __forceinline__ MaskRaw mask_fetch(const AttnArgs& a, const TileRef& ref) {
   static_assert(!is_vs(PAT), "vertical-slash masks are built by the loader warp");
   MaskRaw m;
   m.ref = ref;
   m.base = 0;
   m.whole = false;
+  if (PAT == kPatCross) {  // the modality bits of the tile's keys (read a tile ahead)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) m.col[w] = ldg_ahead(a.modbits + ref.t * 4 + w);
+  }
   return m;
 }
 
@@ -280,6 +302,13 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
                                             const MaskRaw& m, int q, uint32_t out[4]) {
   const TileRef& ref = m.ref;
   const int j0 = ref.t * kBN;
+  if (PAT == kPatCross) {  // keys of the other modality, j <= q
+    const uint32_t rowm = (q < a.N) ? ((__ldg(a.modbits + (q >> 5)) >> (q & 31)) & 1u) : 0u;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      out[w] = (q < a.N) ? ((rowm ? ~m.col[w] : m.col[w]) & range_bits(j0 + 32 * w, 0, q + 1)) : 0u;
+    return;
+  }
   if (PAT == kPatRows) {  // q is this row's position: keys j <= q
 #pragma unroll
     for (int w = 0; w < 4; ++w) out[w] = range_bits(j0 + 32 * w, 0, q + 1);
@@ -460,6 +489,37 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
   const int tid = threadIdx.x;
   if (PAT == kPatDense) {
     if (tid == 0) s.n_tiles = r + 1;
+  } else if (PAT == kPatCross) {
+    // key tiles t <= r holding the other modality of some row of the block:
+    // (mods128[t] | mods128[r]) == both modalities; as intervals of consecutive
+    // tiles (each holds a run of a modality, so there are at most MI_MAX_RUNS)
+    const uint32_t mr = __ldg(a.mods128 + r);
+    auto need = [&](int t) { return t >= 0 && t <= r && ((__ldg(a.mods128 + t) | mr) == 3u); };
+    const int per = cdiv(r + 1, kAttnThreads);
+    const int t0 = min(tid * per, r + 1), t1 = min(t0 + per, r + 1);
+    int ns = 0;
+    for (int t = t0; t < t1; ++t) ns += (need(t) && !need(t - 1)) ? 1 : 0;
+    int total;
+    int pos = block_excl_scan(ns, s.scan, &total);
+    for (int t = t0; t < t1; ++t) {
+      if (!(need(t) && !need(t - 1)) || pos >= 64) continue;
+      int e = t;
+      while (need(e + 1)) ++e;
+      s.list[2 * pos] = t;
+      s.list[2 * pos + 1] = e - t + 1;
+      ++pos;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const int ni = min(total, 64);
+      int acc = 0;
+      for (int k = 0; k < ni; ++k) {
+        s.list[128 + k] = acc;
+        acc += s.list[2 * k + 1];
+      }
+      s.n_list = ni;
+      s.n_tiles = acc;
+    }
   } else if (PAT == kPatRows) {
     if (tid == 0) {  // key tiles up to the block's last row
       const int last = s.g_phi + s.g_sigma * min(r * kBM + kBM - 1, s.g_lines - 1);
@@ -823,7 +883,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     MaskRaw raw_next{};
     if constexpr (!is_vs(PAT)) {
       ref_next2 = (T > 1) ? tile_at<PAT>(s, a, n, r, 1) : TileRef{0, 0, 0, 0};
-      raw_next = mask_fetch<PAT>((T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0, 0});
+      raw_next = mask_fetch<PAT>(a, (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0, 0});
     }
     for (int t = 0; t < T; ++t) {
       uint32_t mk[4];
@@ -840,7 +900,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         tc_fence_after();
       } else {
         const MaskRaw raw = raw_next;
-        if (t + 1 < T) raw_next = mask_fetch<PAT>(ref_next2);
+        if (t + 1 < T) raw_next = mask_fetch<PAT>(a, ref_next2);
         if (t + 2 < T) ref_next2 = tile_at<PAT>(s, a, n, r, t + 2);
         ok = mbar_wait_warp(&s.s_full, t & 1, abort, lim);
         if (!ok) break;
@@ -945,8 +1005,11 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
             uint32_t pk[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 bb =
-                  __floats2bfloat162_rn(o[u * 8 + 2 * e] * inv, o[u * 8 + 2 * e + 1] * inv);
+              // a row that kept no key (possible in the cross-modality pass, whose
+              // O may never have been written) is written as zeros
+              __nv_bfloat162 bb = (l > 0.f) ? __floats2bfloat162_rn(o[u * 8 + 2 * e] * inv,
+                                                                    o[u * 8 + 2 * e + 1] * inv)
+                                            : __floats2bfloat162_rn(0.f, 0.f);
               pk[e] = *reinterpret_cast<uint32_t*>(&bb);
             }
             *reinterpret_cast<uint4*>(orow + c * 32 + u * 8) =

@@ -1,4 +1,4 @@
-// Dense causal, A-shape and grid-row variants of the attention engine.
+// Dense causal, A-shape, grid-row and cross-modality variants of the attention engine.
 #include "attn_launch.cuh"
 
 namespace mi {
@@ -7,5 +7,6 @@ namespace mi {
 template cudaError_t launch_attn<kPatDense>(MI_ATTN_MAPS, const AttnArgs&, int, cudaStream_t);
 template cudaError_t launch_attn<kPatAShape>(MI_ATTN_MAPS, const AttnArgs&, int, cudaStream_t);
 template cudaError_t launch_attn<kPatRows>(MI_ATTN_MAPS, const AttnArgs&, int, cudaStream_t);
+template cudaError_t launch_attn<kPatCross>(MI_ATTN_MAPS, const AttnArgs&, int, cudaStream_t);
 #undef MI_ATTN_MAPS
 }  // namespace mi

@@ -10,7 +10,12 @@
 //     scores v over the lattice - lattice size * last_q / N over
 //     sigma_min..sigma_max, ties to the smaller sigma, then phi;
 //   Q-boundary: a query row follows the vertical-slash pattern of its own
-//     modality, estimated from the 64 rows ending at that modality's last token.
+//     modality, estimated from the 64 rows ending at that modality's last token;
+//   2D-boundary (two modalities, given as runs): each modality's tokens, in
+//     order, are a sub-sequence in which the modality is a vertical-slash head
+//     (the tokens are permuted so that each sub-sequence is contiguous); keys of
+//     the other modality before a query are all kept (the cross-modality pass),
+//     and the two partial softmaxes are merged by their log-sum-exps.
 #pragma once
 
 #include "common.cuh"
@@ -140,6 +145,93 @@ __global__ void modality_scan_kernel(const int32_t* modality, int N, int n_mod, 
   }
   atomicMax(&ends[m], j + 1);
   atomicOr(&blk_mods[j / kBM], 1u << m);
+}
+
+// The token runs of a 2D-boundary call: run u covers original tokens
+// start[u] .. start[u] + len[u] - 1, all of modality mod[u] (0 or 1), which sit
+// at permuted positions pstart[u] .. (modality 0's tokens first, in order).
+constexpr int kMaxRuns = MI_MAX_RUNS;
+struct RunTable {
+  int n;
+  int start[kMaxRuns], pstart[kMaxRuns], len[kMaxRuns], mod[kMaxRuns];
+};
+
+__device__ __forceinline__ int run_of(const RunTable& rt, int j) {
+  int lo = 0, hi = rt.n - 1;  // the last run starting at or before j
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (rt.start[mid] <= j) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Rows of q (heads 0..hq-1), k and v (heads 0..hkv-1), all [heads, N, 128] bf16,
+// copied to their permuted positions; one warp per (tensor, head, token) row.
+__global__ void boundary_gather_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                                       int hq, int hkv, int N, const __grid_constant__ RunTable rt,
+                                       __nv_bfloat16* qp, __nv_bfloat16* kp, __nv_bfloat16* vp) {
+  const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t rows_q = (int64_t)hq * N, rows_kv = (int64_t)hkv * N;
+  if (w >= rows_q + 2 * rows_kv) return;
+  const __nv_bfloat16* src;
+  __nv_bfloat16* dst;
+  int64_t r;
+  if (w < rows_q) {
+    src = q; dst = qp; r = w;
+  } else if (w < rows_q + rows_kv) {
+    src = k; dst = kp; r = w - rows_q;
+  } else {
+    src = v; dst = vp; r = w - rows_q - rows_kv;
+  }
+  const int h = static_cast<int>(r / N), j = static_cast<int>(r - (int64_t)h * N);
+  const int u = run_of(rt, j);
+  const int p = rt.pstart[u] + (j - rt.start[u]);
+  const uint2* s2 = reinterpret_cast<const uint2*>(src + ((size_t)h * N + j) * kD);
+  uint2* d2 = reinterpret_cast<uint2*>(dst + ((size_t)h * N + p) * kD);
+  d2[lane] = s2[lane];
+}
+
+// Bit j of modbits: token j is of modality 1; mods128[t]: bit m set when the
+// 128-token block t holds a token of modality m.  modbits and mods128 must be
+// zero on entry.
+__global__ void boundary_bits_kernel(int N, const __grid_constant__ RunTable rt, uint32_t* modbits,
+                                     uint32_t* mods128) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= N) return;
+  const int m = rt.mod[run_of(rt, j)];
+  if (m) atomicOr(&modbits[j >> 5], 1u << (j & 31));
+  atomicOr(&mods128[j >> 7], 1u << m);
+}
+
+// out[h][j] (and lse) = the merge of the within-modality result (op / lse_in at the
+// permuted position of j) and the cross-modality result already in out / lse_x:
+// O = (e^{L1} O1 + e^{L2} O2) / (e^{L1} + e^{L2}).  One warp per (listed head, token).
+__global__ void boundary_merge_kernel(int N, const __grid_constant__ RunTable rt, HeadList heads,
+                                      const __nv_bfloat16* op, const float* lse_in, const float* lse_x,
+                                      __nv_bfloat16* out, float* lse) {
+  const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= (int64_t)heads.n * N) return;
+  const int n = static_cast<int>(w / N), j = static_cast<int>(w - (int64_t)n * N);
+  const int h = heads.h[n];
+  const int u = run_of(rt, j);
+  const int p = rt.pstart[u] + (j - rt.start[u]);
+  const float l1 = lse_in[(size_t)h * N + p], l2 = lse_x[(size_t)h * N + j];
+  const float m = fmaxf(l1, l2);
+  const float w1 = (l1 == -INFINITY) ? 0.f : __expf(l1 - m), w2 = (l2 == -INFINITY) ? 0.f : __expf(l2 - m);
+  const float inv = 1.f / (w1 + w2);
+  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(op + ((size_t)h * N + p) * kD) + 2 * lane;
+  __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(out + ((size_t)h * N + j) * kD) + 2 * lane;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const float2 x1 = __bfloat1622float2(a[e]), x2 = __bfloat1622float2(b[e]);
+    // a side with weight 0 (no key) takes no part, whatever its output holds
+    const float2 y1 = (w1 > 0.f) ? make_float2(w1 * x1.x, w1 * x1.y) : make_float2(0.f, 0.f);
+    const float2 y2 = (w2 > 0.f) ? make_float2(w2 * x2.x, w2 * x2.y) : make_float2(0.f, 0.f);
+    b[e] = __floats2bfloat162_rn((y1.x + y2.x) * inv, (y1.y + y2.y) * inv);
+  }
+  if (lse && lane == 0) lse[(size_t)h * N + j] = m + logf(w1 + w2);
 }
 
 }  // namespace mi

@@ -76,6 +76,7 @@ typedef struct CUstream_st* mi_stream_t; /* a cudaStream_t */
 #define MI_MAX_KV 2048 /* largest vertical budget the sparse attention kernel accepts */
 #define MI_MAX_MODALITIES 8    /* modalities a Q-boundary call accepts */
 #define MI_GRID_MAX_SIGMA 4096 /* largest stride range a grid estimation scans */
+#define MI_MAX_RUNS 64         /* modality runs a 2D-boundary call accepts */
 
 /* ops for mi_workspace_bytes */
 #define MI_OP_VS_ESTIMATE 1
@@ -87,6 +88,7 @@ typedef struct CUstream_st* mi_stream_t; /* a cudaStream_t */
 #define MI_OP_GRID_ATTN 7
 #define MI_OP_QBOUNDARY_ESTIMATE 8
 #define MI_OP_QBOUNDARY_ATTN 9
+#define MI_OP_BOUNDARY2D_ATTN 10
 
 /* flags for mi_block_sparse_attn */
 #define MI_IDX_GIVEN 1
@@ -319,6 +321,32 @@ int mi_qboundary_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int 
                       const int32_t* heads, int n_heads, const int32_t* modality, int n_mod,
                       const int32_t* v_idx, int k_v, const int32_t* s_idx, int k_s, mi_bf16* out,
                       float* lse, void* workspace, size_t ws_bytes, mi_stream_t stream);
+
+/*
+ * 2D-Boundary head (slides, "MMInference: 2D-Boundary pattern": the modality
+ * boundary splits both axes; "modality-separated continuity").  Two modalities,
+ * given as runs: runs is a HOST int32 array [n_runs][2] of (modality 0 or 1,
+ * length >= 1) in token order, the lengths summing to N, n_runs <= MI_MAX_RUNS.
+ * Each modality's tokens, in order, form a sub-sequence in which the modality is
+ * a vertical-slash head: its index sets are estimated from the sub-sequence's
+ * last 64 tokens (as mi_vs_estimate on the sub-sequence alone) and its columns,
+ * offsets, first block and own block count sub-sequence positions, so that a
+ * diagonal continues across the other modality's tokens.  A sub-sequence of
+ * fewer than 64 tokens is dense within itself.  Row q keeps, in addition, every
+ * key j <= q of the other modality.
+ * v_idx [2, Hq, k_v] and s_idx [2, Hq, k_s] (DEVICE int32, per modality, in
+ * sub-sequence positions) receive the estimated sets, or with flags =
+ * MI_IDX_GIVEN are read instead.  Every q-head is computed (no head list).
+ * The tokens are permuted so that each sub-sequence is contiguous (the
+ * "permutation-based" kernels of the README mirror's TL;DR), the within-modality
+ * and cross-modality passes run separately and are merged by their log-sum-exps.
+ * Workspace: mi_workspace_bytes(MI_OP_BOUNDARY2D_ATTN, Hq, Hkv, N, 0, 0, 0)
+ * (holds permuted copies of q, k, v and o).  Malformed runs: MI_ERR_ARG.
+ */
+int mi_boundary2d_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N, int d,
+                       const int32_t* runs, int n_runs, int k_v, int k_s, int32_t* v_idx, int32_t* s_idx,
+                       int flags, mi_bf16* out, float* lse, void* workspace, size_t ws_bytes,
+                       mi_stream_t stream);
 
 /*
  * mi_vs_estimate_noalloc: mi_vs_estimate for callers that cannot allocate device

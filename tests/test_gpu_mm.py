@@ -166,3 +166,72 @@ def test_qboundary_rejects_unknown_modalities():
     assert B.mi_read_status(ws) == B.MI_ERR_INDEX
     with pytest.raises(B.MIError):
         B.mi_qboundary_estimate(q, k, mod, B.MI_MAX_MODALITIES + 1, k_v=8, k_s=8)
+
+
+def _runs_modality(runs):
+    return np.concatenate([np.full(n, m, dtype=np.int64) for m, n in runs])
+
+
+@pytest.mark.parametrize("runs", [[(0, 700), (1, 900), (0, 500), (1, 300)],
+                                  [(1, 40), (0, 1500), (1, 100), (0, 333)],
+                                  [(0, 1000), (1, 50), (0, 500)],
+                                  [(0, 2048)]])
+def test_boundary2d_attention_every_row(runs):
+    N = sum(n for _, n in runs)
+    mod = _runs_modality(runs)
+    x = I.literal_inputs(4, 2, N, n_cols=6, n_offsets=3, seed=N + len(runs))
+    q, k, v = _dev(x)
+    k_v, k_s = 48, 40
+    lse = torch.full((4, N), float("nan"), dtype=torch.float32, device=DEV)
+    out, vi, si = B.mi_boundary2d_attn(q, k, v, runs, k_v=k_v, k_s=k_s, lse=lse)
+    torch.cuda.synchronize()
+    vi_n, si_n, o, l = vi.cpu().numpy(), si.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+    for h in range(4):
+        g = O.kv_head(h, 4, 2)
+        ref_sets = O.boundary2d_estimate(x.q[h], x.k[g], mod, 2, 64, k_v, k_s)
+        sets = []
+        for m in (0, 1):
+            idx = np.nonzero(mod == m)[0]
+            if idx.size >= 64:
+                vv, ss = O.vs_estimate_scores(x.q[h][torch.as_tensor(idx)], x.k[g][torch.as_tensor(idx)], 64)
+                band_agree(vi_n[m, h], ref_sets[m][0], vv, k_v)
+                band_agree(si_n[m, h], ref_sets[m][1], ss, k_s)
+            sets.append((vi_n[m, h][vi_n[m, h] >= 0], si_n[m, h][si_n[m, h] >= 0]))
+        ref, ref_lse = O.attention_rows(x.q[h], x.k[g], x.v[g], np.arange(N),
+                                        lambda r: O.boundary2d_mask_rows(N, r, mod, sets))
+        assert_close(o[h], ref, f"2D-boundary head {h}")
+        np.testing.assert_allclose(l[h], ref_lse, atol=2e-2)
+
+
+def test_boundary2d_attention_on_oracle_sets():
+    runs = [(0, 600), (1, 800), (0, 400), (1, 248)]
+    N = sum(n for _, n in runs)
+    mod = _runs_modality(runs)
+    x = I.literal_inputs(2, 1, N, n_cols=4, n_offsets=2, seed=99)
+    q, k, v = _dev(x)
+    k_v, k_s = 32, 24
+    gv = np.full((2, 2, k_v), -1, dtype=np.int32)
+    gs = np.full((2, 2, k_s), -1, dtype=np.int32)
+    refs = []
+    for h in range(2):
+        rs = O.boundary2d_estimate(x.q[h], x.k[0], mod, 2, 64, k_v, k_s)
+        refs.append(rs)
+        for m in (0, 1):
+            gv[m, h, :len(rs[m][0])] = rs[m][0]
+            gs[m, h, :len(rs[m][1])] = rs[m][1]
+    out, _, _ = B.mi_boundary2d_attn(q, k, v, runs, v_idx=torch.tensor(gv, device=DEV),
+                                     s_idx=torch.tensor(gs, device=DEV), given=True)
+    o = out.float().cpu().numpy()
+    for h in range(2):
+        ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], np.arange(N),
+                                  lambda r: O.boundary2d_mask_rows(N, r, mod, refs[h]))
+        assert_close(o[h], ref, f"2D-boundary given head {h}")
+
+
+def test_boundary2d_rejects_malformed_runs():
+    N = 256
+    x = I.literal_inputs(2, 1, N, n_cols=2, n_offsets=1, seed=3)
+    q, k, v = _dev(x)
+    for runs in ([(0, 100), (1, 100)], [(2, 256)], [(0, 0), (1, 256)]):
+        with pytest.raises(B.MIError):
+            B.mi_boundary2d_attn(q, k, v, runs, k_v=8, k_s=8)

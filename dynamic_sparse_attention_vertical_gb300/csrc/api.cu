@@ -629,8 +629,9 @@ int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int 
       const int s0 = P.bg_start[gi];
       hl.n = P.bg_start[gi + 1] - s0;
       for (int i = 0; i < hl.n; ++i) hl.h[i] = P.blk_head[s0 + i];
-      block_select_kernel<<<dim3(NB, hl.n), 256, sizeof(float) * NB, st>>>(
-          qbar + (size_t)s0 * NB * kD, kbar, NB, group, hl, P.bg_tk[gi], P.TK,
+      const int R = block_select_rows(NB, 160 * 1024);
+      block_select_kernel<<<dim3(cdiv(NB, R), hl.n), 256, sizeof(float) * NB * R, st>>>(
+          qbar + (size_t)s0 * NB * kD, kbar, NB, group, hl, P.bg_tk[gi], P.TK, R,
           blk + (size_t)s0 * NB * P.TK);
       if ((rc = launched("block selection"))) return rc;
     }
@@ -791,8 +792,9 @@ int mi_block_sparse_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, i
       once_rc = set_smem(reinterpret_cast<const void*>(block_select_kernel), 160 * 1024);
     });
     if (once_rc) return once_rc;
-    block_select_kernel<<<dim3(NB, n_heads), 256, sizeof(float) * NB, st>>>(
-        qbar, kbar, NB, Hq / Hkv, a.heads, topk, topk, blk_idx);
+    const int R = block_select_rows(NB, 160 * 1024);
+    block_select_kernel<<<dim3(cdiv(NB, R), n_heads), 256, sizeof(float) * NB * R, st>>>(
+        qbar, kbar, NB, Hq / Hkv, a.heads, topk, topk, R, blk_idx);
     if ((rc = launched("block selection"))) return rc;
   } else {
     const int rows = n_heads * NB;

@@ -9,6 +9,8 @@
 #pragma once
 
 #include "common.cuh"
+#include <algorithm>
+
 #include "select.cuh"
 
 namespace mi {
@@ -41,33 +43,81 @@ __global__ void block_pool_kernel(const __nv_bfloat16* src, int N, int64_t ld, i
   *reinterpret_cast<float4*>(out + ((size_t)o * NB + blk) * kD + lane * 4) = res;
 }
 
-// Per (query block r, listed head): sigma over c <= r, then top-k into blk_idx
-// (rows of ld >= topk entries, padded with -1).
+// Per R consecutive query blocks r0 .. r0+R-1 of one listed head (blockIdx.x,
+// blockIdx.y): sigma over c <= r for each of them, then one top-k per block into
+// blk_idx (rows of ld >= topk entries, padded with -1).  Each pooled key block is
+// read once for the R query blocks: warp w takes c = w, w + 8, ...; lane l holds
+// dims 4l..4l+3 of the R pooled queries, forms R partial dots and reduces them
+// over the warp by a butterfly that leaves query block i's sum in lanes 4i..4i+3
+// (9 shuffles for 8 sums).  Then warp i selects for query block r0 + i.  R <= 8;
+// the host picks R so that R * NB floats fit in shared memory.
+constexpr int kSelRows = 8;
 __global__ void __launch_bounds__(256)
 block_select_kernel(const float* qbar, const float* kbar, int NB, int group, HeadList heads,
-                    int topk, int ld, int32_t* blk_idx) {
-  extern __shared__ float sig[];  // [NB]
-  __shared__ SelectSmem sm;
-  __shared__ __align__(16) float qrow[kD];
-  const int r = blockIdx.x, slot = blockIdx.y;
+                    int topk, int ld, int R, int32_t* blk_idx) {
+  extern __shared__ float sig[];  // [R][NB]
+  __shared__ int hist[kSelRows][256];
+  const int r0 = blockIdx.x * R, slot = blockIdx.y;
+  const int nr = min(R, NB - r0);
+  const int rmax = r0 + nr - 1;
   const int g = heads.h[slot] / group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < kD) qrow[tid] = qbar[((size_t)slot * NB + r) * kD + tid];
-  __syncthreads();
-  const float4 qv = *reinterpret_cast<const float4*>(qrow + lane * 4);
-  for (int c = warp; c <= r; c += 8) {
-    const float4 kv = *reinterpret_cast<const float4*>(kbar + ((size_t)g * NB + c) * kD + lane * 4);
-    float d = qv.x * kv.x + qv.y * kv.y + qv.z * kv.z + qv.w * kv.w;
+  float4 qv[kSelRows];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-    if (lane == 0) sig[c] = d;
+  for (int i = 0; i < kSelRows; ++i)
+    qv[i] = (i < nr) ? *reinterpret_cast<const float4*>(qbar + ((size_t)slot * NB + r0 + i) * kD + lane * 4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
+  const int mine = (b16 ? 4 : 0) + (b8 ? 2 : 0) + (b4 ? 1 : 0);  // the query block this lane ends with
+  // four pooled key blocks in flight per warp (independent loads ahead of their use)
+  for (int c0 = warp; c0 <= rmax; c0 += 32) {
+    float4 kv4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + 8 * u;
+      kv4[u] = (c <= rmax) ? *reinterpret_cast<const float4*>(kbar + ((size_t)g * NB + c) * kD + lane * 4)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + 8 * u;
+      const float4 kv = kv4[u];
+      float v[kSelRows];
+#pragma unroll
+      for (int i = 0; i < kSelRows; ++i) v[i] = qv[i].x * kv.x + qv[i].y * kv.y + qv[i].z * kv.z + qv[i].w * kv.w;
+      float w4[4], w2[2];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float keep = b16 ? v[j + 4] : v[j], send = b16 ? v[j] : v[j + 4];
+        w4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float keep = b8 ? w4[j + 2] : w4[j], send = b8 ? w4[j] : w4[j + 2];
+        w2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+      float y = (b4 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b4 ? w2[0] : w2[1], 4);
+      y += __shfl_xor_sync(0xffffffffu, y, 2);
+      y += __shfl_xor_sync(0xffffffffu, y, 1);
+      if ((lane & 3) == 0 && mine < nr && c <= rmax) sig[(size_t)mine * NB + c] = y;
+    }
   }
   __syncthreads();
-  int32_t* out = blk_idx + ((size_t)slot * NB + r) * ld;
-  const int kk = min(topk, r + 1);  // >= 1
-  const float* sp = sig;
-  topk_select_sorted<256>([sp](int i) { return float_key(sp[i]); }, r + 1, kk, out, sm);
-  for (int i = kk + tid; i < ld; i += 256) out[i] = -1;
+  // one query block per warp
+  if (warp < nr) {
+    const int r = r0 + warp;
+    int32_t* out = blk_idx + ((size_t)slot * NB + r) * ld;
+    const int kk = min(topk, r + 1);  // >= 1
+    const float* sp = sig + (size_t)warp * NB;
+    warp_topk_sorted([sp](int j) { return float_key(sp[j]); }, r + 1, kk, out, hist[warp]);
+    for (int j = kk + lane; j < ld; j += 32) out[j] = -1;
+  }
+}
+
+// Query blocks per selection CTA: up to kSelRows, as many as fit max_smem bytes of scores.
+inline int block_select_rows(int NB, size_t max_smem) {
+  const size_t per = sizeof(float) * (size_t)NB;
+  return static_cast<int>(std::max<size_t>(1, std::min<size_t>(kSelRows, max_smem / per)));
 }
 
 // With caller-given block lists: flag any row that is not ascending, out of

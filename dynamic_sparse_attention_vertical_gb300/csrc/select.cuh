@@ -141,6 +141,87 @@ __device__ void topk_select_sorted(F key_at, int n, int k, int* out, SelectSmem&
   take_sorted<NT>(key_at, n, kth, rem, out, sm);
 }
 
+// The same selection by one warp (for small n: the block selection of 64x64
+// blocks, n <= N / 64), so that the warps of a CTA select for different rows at
+// once.  hist: 256 ints of shared memory owned by the warp.  The same 4-pass
+// 8-bit radix select for the k-th key, then one ordered sweep; ties to the lower
+// index, output ascending.  Requires 1 <= k <= n; every lane must call it.
+template <class F>
+__device__ void warp_topk_sorted(F key_at, int n, int k, int* out, int* hist) {
+  const int lane = threadIdx.x & 31;
+  uint32_t prefix = 0, pmask = 0;
+  int rem = k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      bool act = false;
+      uint32_t bin = 0;
+      if (i < n) {
+        const uint32_t u = key_at(i);
+        act = (u & pmask) == prefix;
+        bin = (u >> shift) & 255u;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, act ? bin : 256u + lane);
+      if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+    }
+    __syncwarp();
+    // lane L covers bins 255-8L .. 248-8L (descending): the bin where the count of
+    // larger keys first reaches rem
+    int c[8], tot = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c[e] = hist[255 - (lane * 8 + e)];
+      tot += c[e];
+    }
+    int incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const int excl = incl - tot;
+    const unsigned hit = __ballot_sync(0xffffffffu, excl < rem && rem <= incl);
+    const int leader = __ffs(hit) - 1;
+    int bin_sel = 0, rem_new = 0;
+    if (lane == leader) {
+      int cum = excl;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (cum + c[e] >= rem) {
+          bin_sel = 255 - (lane * 8 + e);
+          rem_new = rem - cum;
+          break;
+        }
+        cum += c[e];
+      }
+    }
+    bin_sel = __shfl_sync(0xffffffffu, bin_sel, leader);
+    rem = __shfl_sync(0xffffffffu, rem_new, leader);
+    prefix |= static_cast<uint32_t>(bin_sel) << shift;
+    pmask |= 0xFFu << shift;
+    __syncwarp();
+  }
+  const uint32_t kth = prefix;
+  const unsigned lt = (1u << lane) - 1u;
+  int gb = 0, eb = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const uint32_t u = (i < n) ? key_at(i) : 0u;
+    const bool isg = i < n && u > kth;
+    const bool ise = i < n && u == kth;
+    const unsigned bg = __ballot_sync(0xffffffffu, isg);
+    const unsigned be = __ballot_sync(0xffffffffu, ise);
+    const int G = gb + __popc(bg & lt), E = eb + __popc(be & lt);
+    if (isg) out[G + min(E, rem)] = i;
+    else if (ise && E < rem) out[G + E] = i;
+    gb += __popc(bg);
+    eb += __popc(be);
+  }
+}
+
 // T1: top-k of the vertical (y = 0) or slash (y = 1) scores of every listed head;
 // k > N keeps all N indices, and the row is padded with -1 up to the row stride.
 //

@@ -577,6 +577,72 @@ def run_sweep(args, B):
     print(json.dumps({"metric": METRIC, "unit": "ms/layer", "sweep": points}), flush=True)
 
 
+# --------------------------------------------------------- multi-modal heads ----
+
+MM_RUNS = [(0, 8192), (1, 98304), (0, 24576)]  # text, video, text: 131072 tokens
+
+
+def run_mm(args, B):
+    """The multi-modal heads on a 128K layer (32 q / 8 KV heads): grid (estimated lattice), Q-boundary
+    and 2D-boundary (two modalities as text / video / text runs), each timed as a whole layer against
+    the dense causal kernel on the same inputs.  One JSON line."""
+    from dynamic_sparse_attention_vertical_gb300 import inputs as I
+    dev = torch.device("cuda")
+    N, Hq, Hkv = 131072, 32, 8
+    res = {}
+    x = I.grid_inputs(Hq, Hkv, N, 256, 37, seed=7, device=dev)
+    out = torch.zeros_like(x.q)
+    ws_d = torch.empty(256, dtype=torch.uint8, device=dev)
+    B.mi_dense_causal_attn(x.q, x.k, x.v, out=out, workspace=ws_d)
+    dms, _ = timed(lambda e: B.mi_dense_causal_attn(x.q, x.k, x.v, out=out, workspace=ws_d), 2)
+    grid = torch.empty((Hq, 2), dtype=torch.int32, device=dev)
+    ws_ge = torch.empty(B.mi_workspace_bytes(B.MI_OP_GRID_ESTIMATE, Hq, Hkv, N), dtype=torch.uint8, device=dev)
+    ws_ga = torch.empty(B.mi_workspace_bytes(B.MI_OP_GRID_ATTN, Hq, Hkv, N), dtype=torch.uint8, device=dev)
+
+    def grid_step(_):
+        B.mi_grid_estimate(x.q, x.k, 64, 1024, grid=grid, workspace=ws_ge)
+        B.mi_grid_attn(x.q, x.k, x.v, grid, 64, out=out, workspace=ws_ga)
+    for _ in range(args.warmup):
+        grid_step(None)
+    ms, _ = timed(grid_step, args.steps)
+    res["grid"] = {"ms_per_layer": ms, "dense_ms": dms, "speedup": dms / ms,
+                   "lattice": grid[0].tolist(), "inputs": "lattice sigma 256, phi 37 planted; sigma searched in 64..1024"}
+    del x, out
+    torch.cuda.empty_cache()
+    x = I.literal_inputs(Hq, Hkv, N, n_cols=16, n_offsets=8, seed=8, device=dev)
+    mod = torch.cat([torch.full((n,), m, dtype=torch.int32) for m, n in MM_RUNS]).to(dev)
+    out = torch.zeros_like(x.q)
+    B.mi_dense_causal_attn(x.q, x.k, x.v, out=out, workspace=ws_d)
+    dms, _ = timed(lambda e: B.mi_dense_causal_attn(x.q, x.k, x.v, out=out, workspace=ws_d), 2)
+    vi = torch.empty((2, Hq, 1000), dtype=torch.int32, device=dev)
+    si = torch.empty((2, Hq, 6096), dtype=torch.int32, device=dev)
+    ws_qe = torch.empty(B.mi_workspace_bytes(B.MI_OP_QBOUNDARY_ESTIMATE, Hq, Hkv, N), dtype=torch.uint8, device=dev)
+    ws_qa = torch.empty(B.mi_workspace_bytes(B.MI_OP_QBOUNDARY_ATTN, Hq, Hkv, N), dtype=torch.uint8, device=dev)
+
+    def qb_step(_):
+        B.mi_qboundary_estimate(x.q, x.k, mod, 2, k_v=1000, k_s=6096, v_idx=vi, s_idx=si, workspace=ws_qe)
+        B.mi_qboundary_attn(x.q, x.k, x.v, mod, 2, vi, si, out=out, workspace=ws_qa)
+    for _ in range(args.warmup):
+        qb_step(None)
+    ms, _ = timed(qb_step, args.steps)
+    res["q_boundary"] = {"ms_per_layer": ms, "dense_ms": dms, "speedup": dms / ms, "runs": MM_RUNS,
+                         "budgets": "1000 columns / 6096 diagonals per modality"}
+    del ws_qe, ws_qa
+    torch.cuda.empty_cache()
+    ws_2d = torch.empty(B.mi_workspace_bytes(B.MI_OP_BOUNDARY2D_ATTN, Hq, Hkv, N), dtype=torch.uint8, device=dev)
+
+    def b2_step(_):
+        B.mi_boundary2d_attn(x.q, x.k, x.v, MM_RUNS, k_v=1000, k_s=6096, v_idx=vi, s_idx=si, out=out,
+                             workspace=ws_2d)
+    for _ in range(args.warmup):
+        b2_step(None)
+    ms, _ = timed(b2_step, args.steps)
+    res["boundary_2d"] = {"ms_per_layer": ms, "dense_ms": dms, "speedup": dms / ms, "runs": MM_RUNS,
+                          "budgets": "1000 columns / 6096 diagonals per modality sub-sequence"}
+    print(json.dumps({"metric": "ms/layer of the multi-modal heads at 128K (32 q / 8 KV heads)", "unit": "ms/layer",
+                      "steps": args.steps, "warmup": args.warmup, "mm": res}), flush=True)
+
+
 # -------------------------------------------------------------------- main ----
 
 def main():
@@ -599,6 +665,7 @@ def main():
                     help="also time the oracle on the whole layer (all-vertical-slash workloads up to 32K tokens; "
                          "single-core and all-core)")
     ap.add_argument("--sweep-n", default="", help="comma-separated N values for --sweep")
+    ap.add_argument("--mm", action="store_true", help="time the multi-modal heads (grid, Q-/2D-boundary) instead")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
     w = WORKLOADS[args.workload]
@@ -628,6 +695,9 @@ def main():
     B.load()
     if args.sweep:
         run_sweep(args, B)
+        return
+    if args.mm:
+        run_mm(args, B)
         return
     burst, sustained, hbm, peak_src = measured_peaks()
     dev = torch.device("cuda", local_rank)

@@ -235,3 +235,55 @@ def test_boundary2d_rejects_malformed_runs():
     for runs in ([(0, 100), (1, 100)], [(2, 256)], [(0, 0), (1, 256)]):
         with pytest.raises(B.MIError):
             B.mi_boundary2d_attn(q, k, v, runs, k_v=8, k_s=8)
+
+
+def test_mm_heads_128k_sampled():
+    """The three multi-modal calls at 128K tokens (the size bench.py --mm times): sampled rows
+    against the oracle, with the GPU's estimated lattice and index sets (the sets checked against
+    the oracle's within the top-k band)."""
+    N = 131072
+    runs = [(0, 8192), (1, 98304), (0, 24576)]
+    mod = _runs_modality(runs)
+    rng = np.random.default_rng(17)
+    # grid: a planted lattice, estimated, then attended
+    x = I.grid_inputs(2, 1, N, 256, 37, seed=71)
+    q, k, v = _dev(x)
+    grid = B.mi_grid_estimate(q, k, 64, 1024)
+    out = B.mi_grid_attn(q, k, v, grid, 64)
+    torch.cuda.synchronize()
+    assert grid.cpu().tolist() == [[256, 37]] * 2
+    rows = np.unique(np.concatenate([sample_rows(N, rng, n_random=16, blocks=1), np.arange(37, N, 256)[:8]]))
+    ref, _ = O.attention_rows(x.q[1], x.k[0], x.v[0], rows, lambda r: O.grid_mask_rows(N, r, 256, 37), chunk=32)
+    assert_close(out[1][torch.as_tensor(rows, device=DEV)].float().cpu().numpy(), ref, "grid 128K")
+    del x, q, k, v, out
+    torch.cuda.empty_cache()
+    # Q-boundary and 2D-boundary on literal inputs
+    x = I.literal_inputs(2, 1, N, n_cols=8, n_offsets=4, seed=72)
+    q, k, v = _dev(x)
+    dmod = torch.as_tensor(mod, dtype=torch.int32, device=DEV)
+    vi, si = B.mi_qboundary_estimate(q, k, dmod, 2, k_v=1000, k_s=6096)
+    out = B.mi_qboundary_attn(q, k, v, dmod, 2, vi, si)
+    torch.cuda.synchronize()
+    vi_n, si_n = vi.cpu().numpy(), si.cpu().numpy()
+    h = 1
+    sets = []
+    for m in (0, 1):
+        vv, ss = O.window_estimate_scores(x.q[h], x.k[0], O.modality_row_end(mod, m), 64)
+        band_agree(vi_n[m, h], O.topk_sorted(vv, 1000), vv, 1000)
+        band_agree(si_n[m, h], O.topk_sorted(ss, 6096), ss, 6096)
+        sets.append((vi_n[m, h][vi_n[m, h] >= 0], si_n[m, h][si_n[m, h] >= 0]))
+    rows = sample_rows(N, rng, n_random=24, blocks=1)
+    ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], rows, lambda r: O.qboundary_mask_rows(N, r, mod, sets),
+                              chunk=32)
+    assert_close(out[h][torch.as_tensor(rows, device=DEV)].float().cpu().numpy(), ref, "q-boundary 128K")
+    out2, vi2, si2 = B.mi_boundary2d_attn(q, k, v, runs, k_v=1000, k_s=6096)
+    torch.cuda.synchronize()
+    vi2_n, si2_n = vi2.cpu().numpy(), si2.cpu().numpy()
+    sets2 = [(vi2_n[m, h][vi2_n[m, h] >= 0], si2_n[m, h][si2_n[m, h] >= 0]) for m in (0, 1)]
+    idx1 = torch.as_tensor(np.nonzero(mod == 1)[0])
+    vv, ss = O.vs_estimate_scores(x.q[h][idx1], x.k[0][idx1], 64)
+    band_agree(vi2_n[1, h], O.topk_sorted(vv, 1000), vv, 1000)
+    band_agree(si2_n[1, h], O.topk_sorted(ss, 6096), ss, 6096)
+    ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], rows, lambda r: O.boundary2d_mask_rows(N, r, mod, sets2),
+                              chunk=32)
+    assert_close(out2[h][torch.as_tensor(rows, device=DEV)].float().cpu().numpy(), ref, "2D-boundary 128K")

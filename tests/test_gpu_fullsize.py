@@ -87,7 +87,7 @@ def _layer(workload):
     return w, x, L
 
 
-@pytest.mark.parametrize("workload,heads_checked", [("vs-32k", 3), ("vs-1m", 1)])
+@pytest.mark.parametrize("workload,heads_checked", [("vs-32k", 3), ("vs-1m", 3)])
 def test_vs_layer_sampled(workload, heads_checked):
     w, x, L = _layer(workload)
     N = w["N"]
@@ -100,8 +100,11 @@ def test_vs_layer_sampled(workload, heads_checked):
         vi_ref, si_ref, v, s = O.vs_estimate(x.q[h], x.k[g], 64, w["k_v"], w["k_s"])
         band_agree(vi_all[n], vi_ref, v, w["k_v"])
         band_agree(si_all[n], si_ref, s, w["k_s"])
-        if N > 200000:  # the fp64 oracle costs N*d per row: a smaller sample at 1M
-            rows = np.unique(np.concatenate([np.arange(16), np.arange(N - 64, N), rng.integers(0, N, 16)]))
+        if N > 200000:  # the fp64 oracle costs N*d per row: a smaller sample at 1M (first rows,
+            # the last 128-row block, one random block and random rows)
+            b = int(rng.integers(1, N // 128 - 1))
+            rows = np.unique(np.concatenate([np.arange(16), np.arange(N - 128, N), np.arange(128 * b, 128 * b + 128),
+                                             rng.integers(0, N, 32)]))
         else:
             rows = sample_rows(N, rng, n_random=32, blocks=4)
         ref = _check_vs_rows(x, h, vi_all[n], si_all[n], rows, workload)

@@ -1007,6 +1007,7 @@ int mi_grid_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, i
   // horizontal lines: the lattice rows, gathered 128 at a time, dense and causal;
   // they overwrite those rows (same stream, after the pass above)
   base.grid = grid;
+  base.grid_sigma_min = sigma_min;
   return run_attention<kPatRows>(q, k, v, Hq, Hkv, N, out, lse, status, base, st, nullptr, nullptr,
                                  cdiv(cdiv(N, sigma_min), kBM));
 }

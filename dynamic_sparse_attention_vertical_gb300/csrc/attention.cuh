@@ -86,8 +86,10 @@ struct AttnArgs {
   int topk;
   // A-shape
   int n_init, window;
-  // grid rows (kPatRows): (sigma, phi) per listed head
+  // grid rows (kPatRows): (sigma, phi) per listed head; a head whose sigma is below
+  // grid_sigma_min (rejected by the lattice step) has no rows here either
   const int* grid;
+  int grid_sigma_min;
   // Q-boundary passes: write only the rows of modality row_mod, skip the row
   // blocks without it (modality == nullptr: every row)
   const int32_t* modality;  // [N]
@@ -677,7 +679,8 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
   if (PAT == kPatRows) {
     g_sigma = __ldg(a.grid + 2 * n);
     g_phi = __ldg(a.grid + 2 * n + 1);
-    if (g_sigma >= 1 && g_phi >= 0 && g_phi < g_sigma && g_phi < a.N) g_lines = (a.N - 1 - g_phi) / g_sigma + 1;
+    if (g_sigma >= max(a.grid_sigma_min, 1) && g_phi >= 0 && g_phi < g_sigma && g_phi < a.N)
+      g_lines = (a.N - 1 - g_phi) / g_sigma + 1;
     if (r * kBM >= g_lines) return;
   }
 

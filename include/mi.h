@@ -286,8 +286,8 @@ int mi_grid_estimate(const mi_bf16* q, const mi_bf16* k, int Hq, int Hkv, int N,
  * and attend densely to their causal prefix.  sigma_min is a lower bound on
  * every head's sigma, at least ceil(N / MI_MAX_KV) (at most MI_MAX_KV lattice
  * columns), else MI_ERR_ARG; a (sigma, phi) below it or with phi outside
- * [0, sigma) sets MI_ERR_INDEX in the status word and that head's lattice is
- * left out.  Workspace: mi_workspace_bytes(MI_OP_GRID_ATTN, n_heads, Hkv, N, 0, 0, 0).
+ * [0, sigma) sets MI_ERR_INDEX in the status word and that head's lattice (its
+ * columns and its rows) is left out: its rows keep the first and own block only.  Workspace: mi_workspace_bytes(MI_OP_GRID_ATTN, n_heads, Hkv, N, 0, 0, 0).
  */
 int mi_grid_attn(const mi_bf16* q, const mi_bf16* k, const mi_bf16* v, int Hq, int Hkv, int N, int d,
                  const int32_t* heads, int n_heads, const int32_t* grid, int sigma_min, mi_bf16* out,

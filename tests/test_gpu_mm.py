@@ -97,8 +97,14 @@ def test_grid_attention_rejects_bad_lattices():
         B.mi_grid_attn(q, k, v, torch.tensor([[64, 0]] * 2, dtype=torch.int32, device=DEV), 0)
     ws = torch.empty(B.mi_workspace_bytes(B.MI_OP_GRID_ATTN, 2, 1, N), dtype=torch.uint8, device=DEV)
     bad = torch.tensor([[8, 9], [4, 1]], dtype=torch.int32, device=DEV)  # phi >= sigma; sigma < sigma_min
-    B.mi_grid_attn(q, k, v, bad, 6, workspace=ws)
+    out = B.mi_grid_attn(q, k, v, bad, 6, workspace=ws)
     assert B.mi_read_status(ws) == B.MI_ERR_INDEX
+    # a rejected head keeps only the first block and its own block (no lattice columns, no lattice rows)
+    o = out.float().cpu().numpy()
+    for h in range(2):
+        ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], np.arange(N),
+                                  lambda r: O.vs_mask_rows(N, r, np.zeros(0, np.int64), np.zeros(0, np.int64)))
+        assert_close(o[h], ref, f"rejected grid head {h}")
 
 
 def test_qboundary_estimate_recovers_each_modalitys_planted_sets():

@@ -354,7 +354,7 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
   const dim3 grid(np, L.NC);
   est_kernel<1><<<grid, kEstThreads, kEstSmem1, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 1"))) return rc;
-  est_combine<<<n_heads, kLastQ, 0, st>>>(a.part, a.stats, L.NC);
+  est_combine<<<cdiv(n_heads * kLastQ, 8), 256, 0, st>>>(a.part, a.stats, L.NC, n_heads * kLastQ);
   if ((rc = launched("estimation combine"))) return rc;
   est_kernel<2><<<grid, kEstThreads, kEstSmem2, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 2"))) return rc;

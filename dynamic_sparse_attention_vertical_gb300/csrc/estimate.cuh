@@ -12,7 +12,7 @@
 // K tile is read once for both heads.  Eight warps do the arithmetic, two
 // threads per row (64 keys of each tile each).
 //   pass 1  per row: running max m and sum z = sum exp2(x - m) over the chunk
-//   combine per row: merge the chunk partials in chunk order -> (m, 1/z)
+//   combine per row: merge the chunk partials (a warp per row) -> (m, 1/z)
 //   pass 2  per tile: a = exp2(x - m) / z into shared memory, skewed so that
 //           every diagonal is a column; column sums give v[j] for the tile's
 //           keys, sums down the skewed columns give s[o].
@@ -301,19 +301,28 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   }
 }
 
-// Merge the per-chunk (m, z) partials of every estimation row, in chunk order.
-__global__ void est_combine(const float* part, float* stats, int NC) {
-  const int slot = blockIdx.x, i = threadIdx.x;
-  const float* pp = part + ((size_t)slot * kLastQ + i) * NC * 2;
+// Merge the per-chunk (m, z) partials of every estimation row: one warp per row,
+// lane l takes chunks l, l + 32, ... (coalesced), then the maximum and the
+// rescaled sum are reduced over the warp in a fixed order.
+__global__ void est_combine(const float* part, float* stats, int NC, int n_rows) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  const float2* pp = reinterpret_cast<const float2*>(part + (size_t)row * NC * 2);
   float m = -INFINITY;
-  for (int c = 0; c < NC; ++c) m = fmaxf(m, pp[2 * c]);
+  for (int c = lane; c < NC; c += 32) m = fmaxf(m, pp[c].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float z = 0.f;
-  for (int c = 0; c < NC; ++c) {
-    const float mc = pp[2 * c];
-    if (mc != -INFINITY) z += pp[2 * c + 1] * fast_exp2(mc - m);
+  for (int c = lane; c < NC; c += 32) {
+    const float2 t = pp[c];
+    if (t.x != -INFINITY) z += t.y * fast_exp2(t.x - m);
   }
-  stats[((size_t)slot * kLastQ + i) * 2 + 0] = m;
-  stats[((size_t)slot * kLastQ + i) * 2 + 1] = 1.f / z;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (lane == 0) {
+    stats[(size_t)row * 2 + 0] = m;
+    stats[(size_t)row * 2 + 1] = 1.f / z;
+  }
 }
 
 }  // namespace mi

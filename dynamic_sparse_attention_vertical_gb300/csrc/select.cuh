@@ -233,6 +233,19 @@ __device__ void warp_topk_sorted(F key_at, int n, int k, int* out, int* hist) {
 // element of the top k (ties at the k-th key included) is among them, so the
 // result is the same as selecting over all N; otherwise, or if they do not fit,
 // the selection runs over all N.
+constexpr int kTopkU = 4;  // float4 quads per lane in flight in the threshold sweeps
+
+// Quads base + 128 u + 4 lane (u < U) of x, each read whole when it starts before
+// end (end and base multiples of 4, x 16-byte aligned); the others are zero.
+template <int U>
+__device__ __forceinline__ void load_quads(const float* x, int base, int end, int lane, float4* q) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int i = base + u * 128 + lane * 4;
+    q[u] = (i < end) ? __ldg(reinterpret_cast<const float4*>(x + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 constexpr int kTopkSample = 8192;
 constexpr int kTopkCand = 20480;
 struct TopkSmem {
@@ -269,13 +282,31 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
     int rem_s;
     const uint32_t* sp = sm.samp;
     const uint32_t tau = radix_kth_key<NT>([sp](int j) { return sp[j]; }, kTopkSample, rs, sm.sel, &rem_s);
-    // count the scores at or above the threshold, warp by warp over contiguous segments
-    const int seg = cdiv(cdiv(N, NW), 32) * 32;
+    // count the scores at or above the threshold, warp by warp over contiguous
+    // segments; with N a multiple of 4 each lane reads float4 quads, kTopkU of them
+    // in flight (the sweeps are bound by load latency), else one score at a time
+    const bool vec = (N & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+    constexpr int kSpan = 128 * kTopkU;  // scores per warp and vector step
+    const int seg = cdiv(cdiv(N, NW), kSpan) * kSpan;
     const int beg = min(warp * seg, N), end = min(beg + seg, N);
     int c = 0;
-    for (int base = beg; base < end; base += 32) {
-      const int i = base + lane;
-      c += __popc(__ballot_sync(0xffffffffu, i < end && gkey(i) >= tau));
+    if (vec) {
+      for (int base = beg; base < end; base += kSpan) {
+        float4 q[kTopkU];
+        load_quads<kTopkU>(x, base, end, lane, q);
+#pragma unroll
+        for (int u = 0; u < kTopkU; ++u) {
+          if (base + u * 128 + lane * 4 < end)  // then all four are (end is a multiple of 4)
+            c += (float_key(q[u].x) >= tau) + (float_key(q[u].y) >= tau) + (float_key(q[u].z) >= tau) +
+                 (float_key(q[u].w) >= tau);
+        }
+      }
+      c = __reduce_add_sync(0xffffffffu, c);
+    } else {
+      for (int base = beg; base < end; base += 32) {
+        const int i = base + lane;
+        c += __popc(__ballot_sync(0xffffffffu, i < end && gkey(i) >= tau));
+      }
     }
     if (lane == 0) sm.wcnt[warp] = c;
     __syncthreads();
@@ -286,17 +317,50 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
     }
     if (total >= kk && total <= kTopkCand) {  // the same for every thread
       const unsigned lt = (1u << lane) - 1u;
-      for (int base = beg; base < end; base += 32) {
-        const int i = base + lane;
-        const uint32_t u = (i < end) ? gkey(i) : 0u;
-        const bool in = i < end && u >= tau;
-        const unsigned b = __ballot_sync(0xffffffffu, in);
-        if (in) {
-          const int p = before + __popc(b & lt);
-          sm.ckey[p] = u;
-          sm.cidx[p] = i;
+      if (vec) {
+        for (int base = beg; base < end; base += kSpan) {
+          float4 q[kTopkU];
+          load_quads<kTopkU>(x, base, end, lane, q);
+#pragma unroll
+          for (int u = 0; u < kTopkU; ++u) {
+            const int i0 = base + u * 128 + lane * 4;
+            const uint32_t kq[4] = {float_key(q[u].x), float_key(q[u].y), float_key(q[u].z), float_key(q[u].w)};
+            bool in[4];
+            unsigned b[4];
+            int below = 0, all = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              in[e] = i0 < end && kq[e] >= tau;
+              b[e] = __ballot_sync(0xffffffffu, in[e]);
+              below += __popc(b[e] & lt);
+              all += __popc(b[e]);
+            }
+            // lane order, then the quad's own order: the list stays in index order
+            int p = before + below;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (in[e]) {
+                sm.ckey[p] = kq[e];
+                sm.cidx[p] = i0 + e;
+                ++p;
+              }
+            }
+            before += all;
+          }
         }
-        before += __popc(b);
+      } else {
+        for (int base = beg; base < end; base += 32) {
+          const int i = base + lane;
+          const uint32_t u = (i < end) ? gkey(i) : 0u;
+          const bool in = i < end && u >= tau;
+          const unsigned b = __ballot_sync(0xffffffffu, in);
+          if (in) {
+            const int p = before + __popc(b & lt);
+            sm.ckey[p] = u;
+            sm.cidx[p] = i;
+          }
+          before += __popc(b);
+        }
       }
       __syncthreads();
       const uint32_t* ck = sm.ckey;

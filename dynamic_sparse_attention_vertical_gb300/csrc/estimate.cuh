@@ -171,7 +171,8 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const int slot = hs ? slot_b : slot_a;
     const int p_i = R - kLastQ + i;  // position of this query row
     const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64 * ch;
-    float m = -INFINITY, z = 0.f, invz = 0.f;
+    // pass 2 without a second head: m = 0, 1/z = 0 gives zeros (no inf - inf)
+    float m = (PASS == 2) ? 0.f : -INFINITY, z = 0.f, invz = 0.f;
     if (PASS == 2 && slot >= 0) {
       m = a.stats[((size_t)slot * kLastQ + i) * 2 + 0];
       invz = a.stats[((size_t)slot * kLastQ + i) * 2 + 1];
@@ -205,24 +206,39 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       const int j0 = k_lo + t * kBN;
       // keys j0 + 64 ch + c with c <= lim_c are causal; rows of an absent second head are dropped
       const int lim_c = (slot >= 0) ? p_i - j0 - 64 * ch : -1;
+      // all 64 keys causal (every tile but the last ones): no per-key select
+      const bool whole = lim_c >= 63;
+      if (!whole) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = (c <= lim_c) ? x[c] : -INFINITY;
+      }
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
       if (PASS == 1) {
+        // the scale is positive, so the maximum of the scaled scores is the
+        // scaled maximum (rounding is monotone)
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x[c] = (c <= lim_c) ? x[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[c]);
-        }
-        const float mn = fmaxf(m, mx);
+        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+        const float mn = fmaxf(m, mx * a.scale_log2);
         const float mb = (mn == -INFINITY) ? 0.f : mn;
-        float acc = 0.f;
+        const float2 nmb2 = make_float2(-mb, -mb);
+        float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) acc += fast_exp2(x[c] - mb);
-        z = z * fast_exp2(m - mb) + acc;
+        for (int c = 0; c < 64; c += 2) {
+          const float2 y = fma2(make_float2(x[c], x[c + 1]), sc2, nmb2);
+          acc2 = add2(acc2, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+        }
+        z = z * fast_exp2(m - mb) + (acc2.x + acc2.y);
         m = mn;
       } else {
+        const float2 nm2 = make_float2(-m, -m), iz2 = make_float2(invz, invz);
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          sk_row[c] = (c <= lim_c) ? fast_exp2(x[c] * a.scale_log2 - m) * invz : 0.f;
+        for (int c = 0; c < 64; c += 2) {
+          const float2 y = fma2(make_float2(x[c], x[c + 1]), sc2, nm2);
+          const float2 p = mul2(make_float2(fast_exp2(y.x), fast_exp2(y.y)), iz2);
+          sk_row[c] = p.x;
+          sk_row[c + 1] = p.y;
+        }
         named_bar_sync(1, kEstMath);
         const bool halo = has_halo && t == 0;
         const float* cin = &s.carry[(t + 1) & 1][0][0];

@@ -13,15 +13,18 @@
 // threads per row (64 keys of each tile each).
 //   pass 1  per row: running max m and sum z = sum exp2(x - m) over the chunk
 //   combine per row: merge the chunk partials (a warp per row) -> (m, 1/z)
-//   pass 2  per tile: a = exp2(x - m) / z into shared memory, skewed so that
-//           every diagonal is a column; column sums give v[j] for the tile's
-//           keys, sums down the skewed columns give s[o].
+//   pass 2  per 64-key half tile: four producer warps (a thread per row) write
+//           a = exp2(x - m) / z into one of two shared-memory slots, skewed so
+//           that every diagonal is a column; four consumer warps meanwhile sum
+//           the other slot: column sums give v[j] for the half tile's keys,
+//           sums down the skewed columns give s[o].
 // A diagonal d (the key its row 63 meets) spans keys d-63..d, so it may start
-// in the previous tile: partial diagonal sums are carried from tile to tile,
-// and each pass-2 CTA also scores the 128 keys before its chunk (a halo tile
-// whose own outputs are discarded) so that every diagonal it writes is
-// complete.  Every output element is written by exactly one thread with a
-// fixed summation order: the scores are deterministic.
+// in the previous half tile: each consumer thread owns one diagonal position e
+// and carries the partial sum of diagonal e + 64 to the next half tile, and
+// each pass-2 CTA also scores the 64 keys before its chunk (a halo whose own
+// outputs are discarded) so that every diagonal it writes is complete.  Every
+// output element is written by exactly one thread with a fixed summation
+// order: the scores are deterministic.
 #pragma once
 
 #include "common.cuh"
@@ -50,22 +53,24 @@ struct EstSmem {
   alignas(1024) uint8_t q[2][16384];
   alignas(1024) uint8_t k[2][2][16384];
   uint64_t q_full, k_full[2], k_empty[2], s_full[2], s_empty[2], mma_done;
+  uint64_t sk_full[2], sk_empty[2];  // pass 2: the probability slots
   uint32_t tmem;
   int abort;
-  float carry[2][2][64];  // pass 2: [buffer][head of pair][diagonal]
-  float mz[2][128][2];    // pass 1: the two column halves' (m, z) of each row
 };
-// Pass 2 keeps each tile's probabilities in a skewed layout, per head of the
-// pair 64 rows x 192 fp32: row i's key c sits at column c + 63 - i, so that
-// diagonal e of the tile (the diagonal that meets key j0 + e at row 63) is
-// column e, and key column c runs along i -> c + 63 - i.  Positions outside a
-// row's 128 keys stay zero (written once).
-constexpr int kSkPitch = 192;
+// Pass 2 keeps each half tile's probabilities in a skewed layout, per head of
+// the pair 64 rows x 128 fp32: row i's key c (0..63) sits at column c + 63 - i,
+// so that diagonal e (the diagonal that meets key j0 + e at row 63) is column e,
+// and key column c runs along i -> c + 63 - i.  Positions outside a row's 64
+// keys stay zero (written once).  Two slots: one is written while the other is
+// summed.  Pass 1 uses the same space for the two column halves' (m, z).
+constexpr int kSkPitch = 128;
 constexpr int kSkHead = 64 * kSkPitch;
+constexpr int kSkSlot = 2 * kSkHead;
 constexpr int kEstThreads = 384;  // warp 0 MMA, warp 1 TMA, warps 4-11 the rows' arithmetic
 constexpr int kEstMath = 256;     // threads of warps 4-11
-constexpr size_t kEstSmem1 = sizeof(EstSmem) + 1024;
-constexpr size_t kEstSmem2 = sizeof(EstSmem) + 1024 + sizeof(float) * 2 * kSkHead;
+constexpr int kEstHalf = 128;     // pass 2: producer threads (warps 4-7) = consumer threads (8-11)
+constexpr size_t kEstSmem1 = sizeof(EstSmem) + 1024 + sizeof(float) * 2 * 128 * 2;
+constexpr size_t kEstSmem2 = sizeof(EstSmem) + 1024 + sizeof(float) * 2 * kSkSlot;
 
 template <int PASS>
 __global__ void __launch_bounds__(kEstThreads, 1)
@@ -75,7 +80,7 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   EstSmem& s = *reinterpret_cast<EstSmem*>(base);
-  float* Sk = reinterpret_cast<float*>(base + sizeof(EstSmem));  // pass 2 only: [2][64][kSkPitch]
+  float* Sk = reinterpret_cast<float*>(base + sizeof(EstSmem));  // pass 2: [slot][head][64][kSkPitch]
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int pr = blockIdx.x, chunk = blockIdx.y;
@@ -96,15 +101,19 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_init(&s.k_full[b], 1);
       mbar_init(&s.k_empty[b], 1);
       mbar_init(&s.s_full[b], 1);
-      mbar_init(&s.s_empty[b], kEstMath);
+      mbar_init(&s.s_empty[b], PASS == 1 ? kEstMath : kEstHalf);
     }
     mbar_init(&s.mma_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.sk_full[b], kEstHalf);
+      mbar_init(&s.sk_empty[b], kEstHalf);
+    }
     s.abort = 0;
     fence_mbar_init();
   }
-  if (tid < 128) (&s.carry[0][0][0])[tid + 128] = 0.f;  // buffer 1 = carry into tile 0
   if (PASS == 2) {
-    for (int e = tid; e < 2 * kSkHead; e += kEstThreads) Sk[e] = 0.f;
+    float4* z4 = reinterpret_cast<float4*>(Sk);
+    for (int e = tid; e < 2 * kSkSlot / 4; e += kEstThreads) z4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (warp == 0) {
     tmem_alloc(&s.tmem, 256);
@@ -161,37 +170,21 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         mbar_wait_drain(&s.k_full[t & 1], (t >> 1) & 1, lim);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && PASS == 1) {
     // two threads per row: warp w reads TMEM lanes 32 (w % 4) .. + 31 (the rows)
     // and the columns 64 ch .. 64 ch + 63 of each tile, ch = (w - 4) / 4
-    const int mt = tid - 128;                 // 0..255
     const int row = ((warp & 3) << 5) | static_cast<int>(lane_id());  // rows 0-63 head a, 64-127 head b
     const int ch = (warp - 4) >> 2;
     const int hs = row >> 6, i = row & 63;
     const int slot = hs ? slot_b : slot_a;
     const int p_i = R - kLastQ + i;  // position of this query row
     const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 64 * ch;
-    // pass 2 without a second head: m = 0, 1/z = 0 gives zeros (no inf - inf)
-    float m = (PASS == 2) ? 0.f : -INFINITY, z = 0.f, invz = 0.f;
-    if (PASS == 2 && slot >= 0) {
-      m = a.stats[((size_t)slot * kLastQ + i) * 2 + 0];
-      invz = a.stats[((size_t)slot * kLastQ + i) * 2 + 1];
-    }
-    // pass 2: this thread's place in the skewed tile, and its reductions: threads
-    // 0-95 take four adjacent diagonals (of head mt / 48), threads 96-255 one or
-    // two key columns (of the 256 columns of both heads)
-    float* sk_row = Sk + hs * kSkHead + i * (kSkPitch - 1) + 63 + 64 * ch;  // + c: key 64 ch + c
-    if (PASS == 2 && R < N) {
-      // offsets R .. N-1 meet no query row: zero, this chunk's share of them
-      for (int o = R + chunk * kChunkKeys + mt; o < min(N, R + (chunk + 1) * kChunkKeys); o += kEstMath) {
-        a.ssc[(size_t)slot_a * N + o] = 0.f;
-        if (slot_b >= 0) a.ssc[(size_t)slot_b * N + o] = 0.f;
-      }
-    }
+    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+    float m = -INFINITY, z = 0.f;
     for (int t = 0; t < T; ++t) {
       const int b = t & 1;
       // On a failed (timed-out) wait the loop still runs to the end with zeros, so
-      // that the math warps keep meeting at the named barriers below.
+      // that the math warps keep meeting at the named barrier below.
       const bool ok = mbar_wait_warp(&s.s_full[b], (t >> 1) & 1, abort, lim);
       float x[64];
       if (ok) {
@@ -206,105 +199,126 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       const int j0 = k_lo + t * kBN;
       // keys j0 + 64 ch + c with c <= lim_c are causal; rows of an absent second head are dropped
       const int lim_c = (slot >= 0) ? p_i - j0 - 64 * ch : -1;
-      // all 64 keys causal (every tile but the last ones): no per-key select
-      const bool whole = lim_c >= 63;
-      if (!whole) {
+      if (lim_c < 63) {  // all 64 keys causal (every tile but the last ones): no per-key select
 #pragma unroll
         for (int c = 0; c < 64; ++c) x[c] = (c <= lim_c) ? x[c] : -INFINITY;
       }
+      // the scale is positive, so the maximum of the scaled scores is the scaled
+      // maximum (rounding is monotone)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+      const float mn = fmaxf(m, mx * a.scale_log2);
+      const float mb = (mn == -INFINITY) ? 0.f : mn;
+      const float2 nmb2 = make_float2(-mb, -mb);
+      float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float2 y = fma2(make_float2(x[c], x[c + 1]), sc2, nmb2);
+        acc2 = add2(acc2, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+      }
+      z = z * fast_exp2(m - mb) + (acc2.x + acc2.y);
+      m = mn;
+    }
+    // merge the two column halves of each row, in a fixed order
+    float(*mz)[128][2] = reinterpret_cast<float(*)[128][2]>(Sk);
+    mz[ch][row][0] = m;
+    mz[ch][row][1] = z;
+    named_bar_sync(1, kEstMath);
+    if (ch == 0 && slot >= 0) {
+      const float m1 = mz[1][row][0], z1 = mz[1][row][1];
+      const float mn = fmaxf(m, m1);
+      const float mb = (mn == -INFINITY) ? 0.f : mn;
+      const float zz = z * fast_exp2(m - mb) + z1 * fast_exp2(m1 - mb);
+      float* pp = a.part + (((size_t)slot * kLastQ + i) * a.NC + chunk) * 2;
+      pp[0] = mn;
+      pp[1] = zz;
+    }
+  } else if (warp >= 4) {
+    const int mt = tid - 128;  // 0..255
+    if (R < N) {
+      // offsets R .. N-1 meet no query row: zero, this chunk's share of them
+      for (int o = R + chunk * kChunkKeys + mt; o < min(N, R + (chunk + 1) * kChunkKeys); o += kEstMath) {
+        a.ssc[(size_t)slot_a * N + o] = 0.f;
+        if (slot_b >= 0) a.ssc[(size_t)slot_b * N + o] = 0.f;
+      }
+    }
+    // the half tiles of this CTA: u = 2 t + h, from h = 1 of tile 0 when that tile
+    // is the halo (only its second half reaches into the chunk's diagonals)
+    const int u0 = has_halo ? 1 : 0, U = 2 * T;
+    if (warp < 8) {
+      // producers: thread = row (TMEM lane), 64 keys of each half tile
+      const int row = ((warp & 3) << 5) | static_cast<int>(lane_id());
+      const int hs = row >> 6, i = row & 63;
+      const int slot = hs ? slot_b : slot_a;
+      const int p_i = R - kLastQ + i;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+      // without a second head: m = 0, 1/z = 0 gives zeros (no inf - inf)
+      float m = 0.f, invz = 0.f;
+      if (slot >= 0) {
+        m = a.stats[((size_t)slot * kLastQ + i) * 2 + 0];
+        invz = a.stats[((size_t)slot * kLastQ + i) * 2 + 1];
+      }
       const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-      if (PASS == 1) {
-        // the scale is positive, so the maximum of the scaled scores is the
-        // scaled maximum (rounding is monotone)
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
-        const float mn = fmaxf(m, mx * a.scale_log2);
-        const float mb = (mn == -INFINITY) ? 0.f : mn;
-        const float2 nmb2 = make_float2(-mb, -mb);
-        float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float2 y = fma2(make_float2(x[c], x[c + 1]), sc2, nmb2);
-          acc2 = add2(acc2, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+      const float2 nm2 = make_float2(-m, -m), iz2 = make_float2(invz, invz);
+      float* sk_row = Sk + hs * kSkHead + i * (kSkPitch - 1) + 63;  // + c: key c of the half tile
+      for (int u = u0; u < U; ++u) {
+        const int t = u >> 1, h = u & 1, b = t & 1, sl = (u - u0) & 1;
+        if ((h == 0 || u == u0) && !mbar_wait_warp(&s.s_full[b], (t >> 1) & 1, abort, lim)) break;
+        float x[64];
+        tc_fence_after();
+        tmem_ld64(taddr + b * 128 + 64 * h, x);
+        if (h == 1) {  // the TMEM buffer is free for the MMA of tile t + 2
+          tc_fence_before();
+          mbar_arrive(&s.s_empty[b]);
         }
-        z = z * fast_exp2(m - mb) + (acc2.x + acc2.y);
-        m = mn;
-      } else {
-        const float2 nm2 = make_float2(-m, -m), iz2 = make_float2(invz, invz);
+        if (u - u0 >= 2 && !mbar_wait_warp(&s.sk_empty[sl], ((u - u0 - 2) >> 1) & 1, abort, lim)) break;
+        const int lim_c = (slot >= 0) ? p_i - (k_lo + t * kBN + 64 * h) : -1;
+        if (lim_c < 63) {  // all 64 keys causal (every half tile but the last ones): no per-key select
+#pragma unroll
+          for (int c = 0; c < 64; ++c) x[c] = (c <= lim_c) ? x[c] : -INFINITY;
+        }
+        float* dst = sk_row + sl * kSkSlot;
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           const float2 y = fma2(make_float2(x[c], x[c + 1]), sc2, nm2);
-          const float2 p = mul2(make_float2(fast_exp2(y.x), fast_exp2(y.y)), iz2);
-          sk_row[c] = p.x;
-          sk_row[c + 1] = p.y;
+          const float2 pv = mul2(make_float2(fast_exp2(y.x), fast_exp2(y.y)), iz2);
+          dst[c] = pv.x;
+          dst[c + 1] = pv.y;
         }
-        named_bar_sync(1, kEstMath);
-        const bool halo = has_halo && t == 0;
-        const float* cin = &s.carry[(t + 1) & 1][0][0];
-        float* cout = &s.carry[t & 1][0][0];
-        if (mt < 96) {
-          // diagonals e0 .. e0 + 3 of head hh: column sums of the skewed tile,
-          // 16-byte loads, rows in a fixed order (four partial sums per diagonal)
-          const int hh = mt / 48, e0 = 4 * (mt - 48 * hh);
-          const int sl = hh ? slot_b : slot_a;
-          const float* col = Sk + hh * kSkHead + e0;
-          float4 acc[4] = {};
-#pragma unroll
-          for (int r = 0; r < 64; ++r) {
-            const float4 v = *reinterpret_cast<const float4*>(col + r * kSkPitch);
-            float4& A = acc[r & 3];
-            A.x += v.x;
-            A.y += v.y;
-            A.z += v.z;
-            A.w += v.w;
-          }
-          const float d4[4] = {(acc[0].x + acc[1].x) + (acc[2].x + acc[3].x),
-                               (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y),
-                               (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z),
-                               (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w)};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = e0 + u;
-            float v = d4[u];
-            if (e < 63) v += cin[hh * 64 + e];
-            if (e < 128) {
-              const int d = j0 + e;  // offset R - 1 - d (a key past R - 1 has no row: o < 0)
-              if (!halo && sl >= 0 && d < R) a.ssc[(size_t)sl * N + (R - 1 - d)] = v;
-            } else if (e < 191) {
-              cout[hh * 64 + (e - 128)] = v;
-            }
-          }
-        } else {
-          // key columns J and J + 160 (J < 96) of both heads: column c of head hh
-          // runs along the skewed rows, i -> c + 63 - i
-          for (int J = mt - 96; J < 256; J += 160) {
-            const int hh = J >> 7, c = J & 127;
-            const int sl = hh ? slot_b : slot_a;
-            const float* col = Sk + hh * kSkHead + 63 + c;
-            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int r = 0; r < 64; ++r) acc4[r & 3] += col[r * (kSkPitch - 1)];
-            const float v = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-            if (!halo && sl >= 0 && j0 + c < N) a.vsc[(size_t)sl * N + j0 + c] = v;
-          }
-        }
-        named_bar_sync(1, kEstMath);
+        mbar_arrive(&s.sk_full[sl]);
       }
-    }
-    if (PASS == 1) {
-      // merge the two column halves of each row, in a fixed order
-      s.mz[ch][row][0] = m;
-      s.mz[ch][row][1] = z;
-      named_bar_sync(1, kEstMath);
-      if (ch == 0 && slot >= 0) {
-        const float m1 = s.mz[1][row][0], z1 = s.mz[1][row][1];
-        const float mn = fmaxf(m, m1);
-        const float mb = (mn == -INFINITY) ? 0.f : mn;
-        const float zz = z * fast_exp2(m - mb) + z1 * fast_exp2(m1 - mb);
-        float* pp = a.part + (((size_t)slot * kLastQ + i) * a.NC + chunk) * 2;
-        pp[0] = mn;
-        pp[1] = zz;
+    } else {
+      // consumers: thread = (head hh, position e < 64) of the half tile; sums
+      // column e (diagonal j0 + e, completed with the carry), column e + 64 (the
+      // part of diagonal j0 + 64 + e in this half tile: the next carry) and the
+      // skewed key column e
+      const int ct = tid - 256;  // 0..127
+      const int hh = ct >> 6, e = ct & 63;
+      const int sl_h = hh ? slot_b : slot_a;
+      float carry = 0.f;
+      for (int u = u0; u < U; ++u) {
+        const int t = u >> 1, h = u & 1, sl = (u - u0) & 1;
+        if (!mbar_wait_warp(&s.sk_full[sl], ((u - u0) >> 1) & 1, abort, lim)) break;
+        const float* src = Sk + sl * kSkSlot + hh * kSkHead;
+        float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+          lo[r & 3] += src[r * kSkPitch + e];
+          hi[r & 3] += src[r * kSkPitch + e + 64];
+          cs[r & 3] += src[r * (kSkPitch - 1) + e + 63];
+        }
+        mbar_arrive(&s.sk_empty[sl]);
+        const float dlo = (lo[0] + lo[1]) + (lo[2] + lo[3]);
+        const float dhi = (hi[0] + hi[1]) + (hi[2] + hi[3]);
+        const float col = (cs[0] + cs[1]) + (cs[2] + cs[3]);
+        const int j0 = k_lo + t * kBN + 64 * h;
+        if (!(has_halo && t == 0) && sl_h >= 0) {
+          const int d = j0 + e;  // offset R - 1 - d (a key past R - 1 has no row: o < 0)
+          if (d < R) a.ssc[(size_t)sl_h * N + (R - 1 - d)] = dlo + carry;
+          if (d < N) a.vsc[(size_t)sl_h * N + d] = col;
+        }
+        carry = dhi;
       }
     }
   }

@@ -144,7 +144,7 @@ EstLayout est_layout(int n_heads, int N) {
 
 struct VsLayout {
   size_t status, offbits, colbits, dbits, dfull, dlist, dcount, clist, ccount, kc, vc, total;
-  int Nw, NT, NTw;
+  int Nw, NT, NTw, Dw;
 };
 VsLayout vs_layout(int n_heads, int N) {
   VsLayout L;
@@ -152,10 +152,11 @@ VsLayout vs_layout(int n_heads, int N) {
   L.NT = cdiv(N, kBN);
   L.Nw = 4 * L.NT;  // padded to whole 128-key tiles
   L.NTw = cdiv(L.NT, 32);
+  L.Dw = L.Nw + 8;  // the windows' key-distance bits, x + 128 for x in [-127, N)
   L.status = c.take(256);
   L.offbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.Nw);
   L.colbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.Nw);
-  L.dbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.NTw);
+  L.dbits = c.take(sizeof(uint32_t) * (size_t)n_heads * L.Dw);
   L.dfull = c.take(sizeof(uint32_t) * (size_t)n_heads * L.NTw);
   L.dlist = c.take(sizeof(int) * (size_t)n_heads * L.NT);
   L.dcount = c.take(sizeof(int) * (size_t)n_heads);
@@ -366,17 +367,16 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
   return MI_OK;
 }
 
-// Vertical-slash attention of the listed heads (a.heads) with given indices: index
-// build, column copy, attention.  vws is a vs_layout(a.heads.n, N) workspace; errors
-// of the data go to `status`.  a's row filter (modality) and grid fields are kept.
-int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int N, AttnArgs& a,
-                const int32_t* v_idx, int k_v, const int32_t* s_idx, int k_s, int expanded,
-                mi_bf16* out, float* lse, char* vws, int* status, cudaStream_t st, int64_t ld = 0) {
-  if (ld <= 0) ld = N;
-  int rc;
-  const int n_heads = a.heads.n;
-  const VsLayout L = vs_layout(n_heads, N);
-  char* ws = vws;
+// Index build of the listed vertical-slash heads into a vs_layout workspace, and
+// the structures it leaves in the attention arguments.
+int vs_index_run(const VsLayout& L, char* ws, int n_heads, int N, const int32_t* v_idx, int k_v,
+                 const int32_t* s_idx, int k_s, int expanded, int* status, cudaStream_t st, AttnArgs& a) {
+  static std::once_flag once;
+  static int once_rc = MI_OK;
+  std::call_once(once, [] {
+    once_rc = set_smem(reinterpret_cast<const void*>(vs_index_kernel), vs_index_smem(cdiv(1 << 21, kBN)));
+  });
+  if (once_rc) return once_rc;
   VsIndexArgs ia;
   ia.N = N;
   ia.k_v = k_v;
@@ -384,6 +384,7 @@ int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, in
   ia.Nw = L.Nw;
   ia.NT = L.NT;
   ia.NTw = L.NTw;
+  ia.Dw = L.Dw;
   ia.expanded = expanded;
   ia.v_idx = v_idx;
   ia.s_idx = s_idx;
@@ -396,15 +397,9 @@ int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, in
   ia.clist = reinterpret_cast<int*>(ws + L.clist);
   ia.ccount = reinterpret_cast<int*>(ws + L.ccount);
   ia.status = status;
-  vs_index_kernel<<<n_heads, 512, 0, st>>>(ia);
+  vs_index_kernel<<<n_heads, 512, vs_index_smem(L.NT), st>>>(ia);
+  int rc;
   if ((rc = launched("vertical-slash index build"))) return rc;
-  __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(ws + L.kc);
-  __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(ws + L.vc);
-  vs_colgather_kernel<<<dim3(cdiv(std::min(k_v + kBN, MI_MAX_KV), 8), n_heads), 256, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), ld, Hq / Hkv,
-      a.heads, ia.clist, ia.ccount, kc, vc);
-  if ((rc = launched("vertical-slash column copy"))) return rc;
-
   a.offbits = ia.offbits;
   a.colbits = ia.colbits;
   a.dbits = ia.dbits;
@@ -417,6 +412,28 @@ int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, in
   a.Nw = L.Nw;
   a.NT = L.NT;
   a.NTw = L.NTw;
+  a.Dw = L.Dw;
+  return MI_OK;
+}
+
+// Vertical-slash attention of the listed heads (a.heads) with given indices: index
+// build, column copy, attention.  vws is a vs_layout(a.heads.n, N) workspace; errors
+// of the data go to `status`.  a's row filter (modality) and grid fields are kept.
+int vs_attn_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int N, AttnArgs& a,
+                const int32_t* v_idx, int k_v, const int32_t* s_idx, int k_s, int expanded,
+                mi_bf16* out, float* lse, char* vws, int* status, cudaStream_t st, int64_t ld = 0) {
+  if (ld <= 0) ld = N;
+  int rc;
+  const int n_heads = a.heads.n;
+  const VsLayout L = vs_layout(n_heads, N);
+  char* ws = vws;
+  if ((rc = vs_index_run(L, ws, n_heads, N, v_idx, k_v, s_idx, k_s, expanded, status, st, a))) return rc;
+  __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(ws + L.kc);
+  __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(ws + L.vc);
+  vs_colgather_kernel<<<dim3(cdiv(std::min(k_v + kBN, MI_MAX_KV), 8), n_heads), 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), ld, Hq / Hkv,
+      a.heads, a.clist, a.ccount, kc, vc);
+  if ((rc = launched("vertical-slash column copy"))) return rc;
   return expanded ? run_attention<kPatVSExp>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc, 0, ld)
                   : run_attention<kPatVS>(q, k, v, Hq, Hkv, N, out, lse, status, a, st, kc, vc, 0, ld);
 }
@@ -562,27 +579,9 @@ int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int 
     }
     const VsLayout V = vs_layout(P.n_vs, N);
     char* vw = ws + L.vs;
-    VsIndexArgs ia;
-    ia.N = N;
-    ia.k_v = P.KV;
-    ia.k_s = P.KS;
-    ia.Nw = V.Nw;
-    ia.NT = V.NT;
-    ia.NTw = V.NTw;
-    ia.expanded = (P.vs_flags & MI_VS_BLOCK_EXPANDED) ? 1 : 0;
-    ia.v_idx = vidx;
-    ia.s_idx = sidx;
-    ia.offbits = reinterpret_cast<uint32_t*>(vw + V.offbits);
-    ia.colbits = reinterpret_cast<uint32_t*>(vw + V.colbits);
-    ia.dbits = reinterpret_cast<uint32_t*>(vw + V.dbits);
-    ia.dfull = reinterpret_cast<uint32_t*>(vw + V.dfull);
-    ia.dlist = reinterpret_cast<int*>(vw + V.dlist);
-    ia.dcount = reinterpret_cast<int*>(vw + V.dcount);
-    ia.clist = reinterpret_cast<int*>(vw + V.clist);
-    ia.ccount = reinterpret_cast<int*>(vw + V.ccount);
-    ia.status = status;
-    vs_index_kernel<<<P.n_vs, 512, 0, st>>>(ia);
-    if ((rc = launched("vertical-slash index build"))) return rc;
+    if ((rc = vs_index_run(V, vw, P.n_vs, N, vidx, P.KV, sidx, P.KS, (P.vs_flags & MI_VS_BLOCK_EXPANDED) ? 1 : 0,
+                           status, st, a)))
+      return rc;
     HeadList hv;
     hv.n = P.n_vs;
     for (int i = 0; i < P.n_vs; ++i) hv.h[i] = P.vs_head[i];
@@ -590,20 +589,8 @@ int layer_run(const void* q, const void* k, const void* v, int Hq, int Hkv, int 
     vc = reinterpret_cast<__nv_bfloat16*>(vw + V.vc);
     vs_colgather_kernel<<<dim3(cdiv(std::min(P.KV + kBN, MI_MAX_KV), 8), P.n_vs), 256, 0, st>>>(
         reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), ld, group, hv,
-        ia.clist, ia.ccount, kc, vc);
+        a.clist, a.ccount, kc, vc);
     if ((rc = launched("vertical-slash column copy"))) return rc;
-    a.offbits = ia.offbits;
-    a.colbits = ia.colbits;
-    a.dbits = ia.dbits;
-    a.dfull = ia.dfull;
-    a.dlist = ia.dlist;
-    a.dcount = ia.dcount;
-    a.clist = ia.clist;
-    a.ccount = ia.ccount;
-    a.expand = ia.expanded;
-    a.Nw = V.Nw;
-    a.NT = V.NT;
-    a.NTw = V.NTw;
   }
   // block-sparse heads: pooling once, selection per top-k group
   if (P.n_blk) {

@@ -73,14 +73,20 @@ struct AttnArgs {
   const uint32_t* offbits;  // [n_heads, Nw]   bit o: offset o selected (block-expanded
                             //                 mode: bit e: 64-block distance e kept)
   const uint32_t* colbits;  // [n_heads, Nw]   bit j: column j selected
-  const uint32_t* dbits;    // [n_heads, NTw]  bit t: tile distance t touched by a diagonal
-  const uint32_t* dfull;    // [n_heads, NTw]  bit t: a tile at distance t is kept whole
-  const int* dlist;         // [n_heads, NT]   the set bits of dbits, ascending
+  // exact slashes: key windows p (row block r reads keys 128 r - p .. + 127 for
+  // every p < 128 r, besides tile 0); block-expanded: 128-aligned tile distances
+  const uint32_t* dbits;    // [n_heads, Dw]   exact: bit x + 128 when a window covers key
+                            //                 distance x = 128 r - j; expanded: bit t when
+                            //                 tile distance t is touched by a diagonal
+  const uint32_t* dfull;    // [n_heads, NTw]  exact: bit i when window i is kept whole;
+                            //                 expanded: bit t when distance t is
+  const int* dlist;         // [n_heads, NT]   exact: the windows, ascending; expanded: the
+                            //                 set bits of dbits, ascending
   const int* dcount;        // [n_heads]
   const int* clist;         // [n_heads, MI_MAX_KV]  the selected columns, ascending
   const int* ccount;        // [n_heads]
   int expand;               // block-expanded slashes: the host launches the kPatVSExp engine
-  int Nw, NT, NTw;
+  int Nw, NT, NTw, Dw;
   // block-sparse
   const int* blk_idx;  // [n_heads, ceil(N/64), topk]
   int topk;
@@ -157,10 +163,13 @@ constexpr int kPChunks = PAT == kPatDense ? 2 : 4;
 
 struct TileRef {
   int kind;  // 0 contiguous, 1 gathered
-  int t;     // contiguous: key tile index; gathered: chunk of the residual list;
+  int t;     // contiguous: key tile index (exact vertical-slash windows: their
+             // first key / 128); gathered: chunk of the residual list;
              // block pattern: the 64-key block in keys 0-63 of the tile
   int sub;   // block pattern: 4-bit mask (bit = rowhalf*2 + keyhalf)
-  int t2;    // block pattern: the 64-key block in keys 64-127 of the tile
+  int t2;    // block pattern: the 64-key block in keys 64-127 of the tile;
+             // exact vertical-slash windows: the window's list index (-1: tile 0)
+  int j0;    // vertical-slash contiguous tiles: the first key
 };
 
 template <int PAT>
@@ -173,9 +182,19 @@ __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a,
     if (i < s.n_contig) {
       if (s.has_t0 && i == 0) {
         ref.t = 0;
+        ref.t2 = -1;
+        ref.j0 = 0;
       } else {
-        const int idx = s.d_cnt - 1 - (i - s.has_t0);
-        ref.t = r - ldg_ahead(a.dlist + (size_t)n * a.NT + idx);
+        const int idx = s.d_cnt - 1 - (i - s.has_t0);  // keys ascending
+        const int p = ldg_ahead(a.dlist + (size_t)n * a.NT + idx);
+        if (PAT == kPatVS) {  // window p: keys 128 r - p ..
+          ref.j0 = r * kBN - p;
+          ref.t = ref.j0 >> 7;
+          ref.t2 = idx;
+        } else {  // tile distance p
+          ref.t = r - p;
+          ref.j0 = ref.t * kBN;
+        }
       }
     } else {
       ref.kind = 1;
@@ -258,13 +277,18 @@ __device__ __forceinline__ VsRaw4 vs_fetch4(const AttnSmem& s, const AttnArgs& a
   m.base = 0;
   m.whole = false;
   if (ref.kind == 0) {
-    const int d = r - ref.t;
-    m.whole = d > 0 && ((s.dfull[d >> 5] >> (d & 31)) & 1u);
+    if (PAT == kPatVS) {  // a window whose keys all lie past tile 0
+      const int i = ref.t2;
+      m.whole = i >= 0 && ref.j0 >= kBN && ((s.dfull[i >> 5] >> (i & 31)) & 1u);
+    } else {
+      const int d = r - ref.t;
+      m.whole = d > 0 && ((s.dfull[d >> 5] >> (d & 31)) & 1u);
+    }
   }
   if (ref.kind != 0 || m.whole) return m;
   const uint32_t* off = a.offbits + (size_t)n * a.Nw;
   const uint32_t* col = a.colbits + (size_t)n * a.Nw;
-  const int j0 = ref.t * kBN;
+  const int j0 = ref.j0;
   if (PAT == kPatVSExp) {
     const int e0 = max(2 * (r - ref.t) - 1, 0);
     m.base = e0;
@@ -275,13 +299,21 @@ __device__ __forceinline__ VsRaw4 vs_fetch4(const AttnSmem& s, const AttnArgs& a
     const int w0 = m.base >> 5;  // floor; >= -4
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int wi = w0 + i;  // the words of rows q0 .. q0 + 96, each < Nw as for one row
-      m.off[i] = ldg_ahead(off + max(wi, 0));
-      if (wi < 0) m.off[i] = 0u;
+      // the words of rows q0 .. q0 + 96; the bits the rows need are below 128 r + 127
+      // (< 32 Nw), a word past the bitmap only rounds out the last one
+      const int wi = w0 + i;
+      m.off[i] = ldg_ahead(off + min(max(wi, 0), a.Nw - 1));
+      if (wi < 0 || wi >= a.Nw) m.off[i] = 0u;
     }
   }
+  // the column bits of keys j0 .. j0 + 127: five words shifted by j0 % 32 (a window
+  // may start anywhere; the fifth word is past the bitmap only when j0 % 32 = 0)
+  const int cw = j0 >> 5, csh = j0 & 31;
+  uint32_t c5[5];
 #pragma unroll
-  for (int w = 0; w < 4; ++w) m.col[w] = ldg_ahead(col + (j0 >> 5) + w);
+  for (int w = 0; w < 5; ++w) c5[w] = ldg_ahead(col + min(cw + w, a.Nw - 1));
+#pragma unroll
+  for (int w = 0; w < 4; ++w) m.col[w] = __funnelshift_r(c5[w], c5[w + 1], csh);
   return m;
 }
 
@@ -303,7 +335,7 @@ template <int PAT>
 __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a, int r,
                                             const MaskRaw& m, int q, uint32_t out[4]) {
   const TileRef& ref = m.ref;
-  const int j0 = ref.t * kBN;
+  const int j0 = is_vs(PAT) ? ref.j0 : ref.t * kBN;
   if (PAT == kPatCross) {  // keys of the other modality, j <= q
     const uint32_t rowm = (q < a.N) ? ((__ldg(a.modbits + (q >> 5)) >> (q & 31)) & 1u) : 0u;
 #pragma unroll
@@ -360,6 +392,9 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
     if (j0 == 0) {  // the first 64 keys
       out[0] = 0xFFFFFFFFu;
       out[1] = 0xFFFFFFFFu;
+    } else if (j0 < kBN) {  // a window reaching into tile 0 leaves those keys to it
+#pragma unroll
+      for (int w = 0; w < 4; ++w) out[w] &= range_bits(j0 + 32 * w, kBN, 1 << 30);
     }
     if (ref.t == r) {  // the query's own 64-block
       const int lb = (q >> 6) << 6;
@@ -444,8 +479,16 @@ __device__ __forceinline__ void vs_masks4(const AttnSmem& s, const AttnArgs& a, 
 #pragma unroll
         for (int w = 0; w < 4; ++w) out[i][w] = e[i + 3 - w] | m.col[w];
       }
+      if (ref.j0 > 0 && ref.j0 < kBN) {  // a window reaching into tile 0 leaves those keys to it
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t keep = range_bits(ref.j0 + 32 * w, kBN, 1 << 30);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) out[i][w] &= keep;
+        }
+      }
     }
-    if (ref.t == 0) {  // the first 64 keys
+    if (ref.j0 == 0) {  // the first 64 keys
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         out[i][0] = 0xFFFFFFFFu;
@@ -479,9 +522,14 @@ __device__ __forceinline__ int block_excl_scan(int x, int* scratch, int* total) 
 }
 
 // A vertical column that no contiguous tile of row block r covers.
+template <int PAT>
 __device__ __forceinline__ bool residual_column(int j, int N, int r, const uint32_t* db) {
   const int t = j >> 7;
   if (j < 0 || j >= N || t < 1 || t >= r) return false;
+  if (PAT == kPatVS) {  // no window covers key distance x = 128 r - j (bit x + 128)
+    const int x = r * kBN - j + kBN;
+    return !((__ldg(db + (x >> 5)) >> (x & 31)) & 1u);
+  }
   const int d = r - t;
   return !((__ldg(db + (d >> 5)) >> (d & 31)) & 1u);
 }
@@ -534,15 +582,21 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
       s.n_tiles = n_sink + (r - t_lo + 1);
     }
   } else if (is_vs(PAT)) {
-    // contiguous tiles: r - delta for the tile distances delta <= r, plus tile 0.
-    // All threads count the distances <= r in parallel (independent loads).
+    // contiguous tiles: tile 0, then the windows p < 128 r (exact slashes: keys
+    // 128 r - p ..) or the tiles r - delta of the distances delta <= r
+    // (block-expanded: tile 0 is one of them when r is a distance).  All threads
+    // count in parallel (independent loads).
     const int* dl = a.dlist + (size_t)n * a.NT;
     const int dc = __ldg(a.dcount + n);
     int below = 0;  // s.has_t0 was set to 1 before the barrier-init sync
     for (int e = tid; e < dc; e += 192) {
       const int d = __ldg(dl + e);
-      below += (d <= r) ? 1 : 0;
-      if (d == r) s.has_t0 = 0;
+      if (PAT == kPatVS) {
+        below += (d < r * kBN) ? 1 : 0;
+      } else {
+        below += (d <= r) ? 1 : 0;
+        if (d == r) s.has_t0 = 0;
+      }
     }
     int n_below;
     block_excl_scan(below, s.scan, &n_below);
@@ -556,7 +610,7 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
     // block (entry hi); an entry is kept when its column is residual (no
     // contiguous tile of this row block covers it), a chunk when it keeps one
     const int* cl = a.clist + (size_t)n * MI_MAX_KV;
-    const uint32_t* db = a.dbits + (size_t)n * a.NTw;
+    const uint32_t* db = a.dbits + (size_t)n * a.Dw;
     const int cnt = __ldg(a.ccount + n);
     uint32_t* resbits = reinterpret_cast<uint32_t*>(&s.list[16]);  // 64 words: entries lo .. lo + 2047
     if (tid < 64) resbits[tid] = 0u;
@@ -570,7 +624,7 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
     block_excl_scan(c_lo, s.scan, &lo);  // (its barriers also order the resbits clear)
     block_excl_scan(c_hi, s.scan, &hi);
     for (int e = lo + tid; e < hi; e += 192) {
-      if (residual_column(__ldg(cl + e), a.N, r, db))
+      if (residual_column<PAT>(__ldg(cl + e), a.N, r, db))
         atomicOr(&resbits[(e - lo) >> 5], 1u << ((e - lo) & 31));
     }
     __syncthreads();
@@ -808,8 +862,8 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
         // two 64-key boxes per 64-column half: keys 0-63 and 64-127 of the
         // tile (for block-sparse tiles, blocks ref.t and ref.t2)
         if (lane_id() == 0) {
-          const int ka = (PAT == kPatBlock) ? ref.t * kBlk : ref.t * kBN;
-          const int kb = (PAT == kPatBlock) ? ref.t2 * kBlk : ref.t * kBN + kBlk;
+          const int ka = (PAT == kPatBlock) ? ref.t * kBlk : is_vs(PAT) ? ref.j0 : ref.t * kBN;
+          const int kb = (PAT == kPatBlock) ? ref.t2 * kBlk : is_vs(PAT) ? ref.j0 + kBlk : ref.t * kBN + kBlk;
           mbar_arrive_expect_tx(full, 2 * 16384);
           tma_load_3d(buf[0], map, full, 0, ka, g);
           tma_load_3d(buf[0] + 8192, map, full, 0, kb, g);

@@ -129,44 +129,69 @@ def dense_kept_per_row(N: int) -> torch.Tensor:
 
 # ------------------------------------------------------ executed tiles ----
 
+def vs_windows(N: int, s_idx) -> np.ndarray:
+    """Key windows of an exact vertical-slash head, as positions p (ascending, p < N).
+
+    Row block r (rows 128 r .. 128 r + 127) reads keys 128 r - p .. 128 r - p + 127
+    for every window p < 128 r, besides tile 0 (keys 0 .. 127).  A window at p meets
+    the offsets p + i - 127 .. p + i in row i of the block, so the windows must hit
+    every interval [x, x + 127] with x in [o - 127, o] for each selected offset o
+    (and o = 0, the query's own block): the greedy hitting set starts at p = 0 and
+    moves to p + 128 while a selected offset lies in (p, p + 128], else to the next
+    selected offset.
+    """
+    s = np.asarray(torch.as_tensor(s_idx).long())
+    o = np.unique(np.concatenate([[0], s[(s >= 0) & (s < N)]]))
+    ws = []
+    p = 0
+    while p < N:
+        ws.append(p)
+        i = int(np.searchsorted(o, p, side="right"))  # first offset > p
+        if i >= len(o):
+            break
+        p = p + 128 if o[i] <= p + 128 else int(o[i])
+    return np.asarray(ws, dtype=np.int64)
+
+
+def _column_tiles(N: int, v_idx, NT: int, residual) -> int:
+    """Column tiles: chunks of 128 entries of the sorted column list from the first
+    column past tile 0 to the last before the row block; a chunk is issued when one
+    of its columns is residual (residual(rr, t) over the entries' columns t)."""
+    v = torch.as_tensor(v_idx).long()
+    v = torch.unique(v[(v >= 0) & (v < N)]).numpy()
+    lo = int((v < 128).sum())
+    col_tiles = 0
+    for rr in range(2, NT):
+        hi = int(np.searchsorted(v, 128 * rr))  # entries with key < 128 rr
+        if hi <= lo:
+            continue
+        res = residual(rr, v[lo:hi])
+        col_tiles += int(np.unique(np.nonzero(res)[0] // 128).size)
+    return col_tiles
+
+
 def vs_tiles(N: int, v_idx, s_idx, expanded: bool = False) -> int:
     """128x128 tiles the vertical-slash kernel issues for one head (all row blocks)."""
     NT = (N + 127) // 128
-    if expanded:
-        # tile distance d holds the 64-blocks at block distances 2d-1 .. 2d+1
-        e = _expanded_dist(N, s_idx, 64)
-        ep = torch.zeros(2 * NT + 2, dtype=torch.bool)
-        ep[1:1 + e.numel()] = e                       # ep[x + 1] = e[x]
-        dd = torch.arange(NT)
-        d = ep[2 * dd] | ep[2 * dd + 1] | ep[2 * dd + 2]
-    else:
-        d = torch.zeros(NT + 1, dtype=torch.bool)
-        s = torch.as_tensor(s_idx).long()
-        s = s[(s >= 0) & (s < N)]
-        d[(s >> 7)] = True
-        d[torch.clamp((s >> 7) + 1, max=NT)[(s & 127) > 0]] = True
-        d[0] = True
-        d = d[:NT]
-    dcum = torch.cumsum(d.long(), 0)                      # distances <= r
-    r = torch.arange(NT)
-    has_t0 = ~d[r]                                        # tile 0 added unless distance r is set
-    contig = dcum + has_t0.long()
-    # column tiles: chunks of 128 entries of the sorted column list from the first
-    # column past tile 0 to the last before the row block; a chunk is issued when
-    # one of its columns is residual (its key tile is not at a kept distance)
-    v = torch.as_tensor(v_idx).long()
-    v = torch.unique(v[(v >= 0) & (v < N)]).numpy()
-    t = v >> 7
-    dn = d.numpy()
-    lo = int((t < 1).sum())
-    col_tiles = 0
-    for rr in range(2, NT):
-        hi = int(np.searchsorted(t, rr))  # entries with key tile < rr
-        if hi <= lo:
-            continue
-        res = ~dn[rr - t[lo:hi]]
-        col_tiles += int(np.unique(np.nonzero(res)[0] // 128).size)
-    return int(contig.sum()) + col_tiles
+    if not expanded:
+        W = vs_windows(N, s_idx)
+        q0 = 128 * np.arange(NT)
+        contig = 1 + np.searchsorted(W, q0, side="left")  # tile 0 and the windows p < 128 r
+        cov = np.zeros(N + 128, dtype=bool)                # x + 127 for x = 128 r - j
+        for p in W:
+            cov[p:p + 128] = True
+        return int(contig.sum()) + _column_tiles(N, v_idx, NT, lambda rr, j: ~cov[128 * rr - j + 127])
+    # tile distance d holds the 64-blocks at block distances 2d-1 .. 2d+1
+    e = _expanded_dist(N, s_idx, 64)
+    ep = torch.zeros(2 * NT + 2, dtype=torch.bool)
+    ep[1:1 + e.numel()] = e                       # ep[x + 1] = e[x]
+    dd = torch.arange(NT)
+    d = (ep[2 * dd] | ep[2 * dd + 1] | ep[2 * dd + 2]).numpy()
+    dcum = np.cumsum(d)                           # distances <= r
+    r = np.arange(NT)
+    has_t0 = ~d[r]                                # tile 0 added unless distance r is set
+    contig = dcum + has_t0
+    return int(contig.sum()) + _column_tiles(N, v_idx, NT, lambda rr, j: ~d[rr - (j >> 7)])
 
 
 def dense_tiles(N: int) -> int:

@@ -29,36 +29,77 @@ def test_block_ashape_dense_counts_match_oracle_masks():
     np.testing.assert_array_equal(F.dense_kept_per_row(N).numpy(), O.causal_mask_rows(N, np.arange(N)).sum(1))
 
 
+def _windows_brute(N, s):
+    """Windows as the textbook stabbing greedy: row i of a block needs, for each selected
+    offset o (and o = 0), a window p with o - i <= p <= o - i + 127; take the intervals
+    [x, x + 127] by ascending x and stab each one not yet hit at its right end."""
+    xs = sorted({o - i for o in set(s) | {0} for i in range(128)})
+    ws, last = [], None
+    for x in xs:
+        if last is None or x > last:
+            last = x + 127
+            ws.append(last)
+    return [p for p in ws if p < N]
+
+
 def _vs_tiles_brute(N, v, s):
     NT = (N + 127) // 128
-    D = {0} | {o >> 7 for o in s} | {(o >> 7) + 1 for o in s if o & 127}
+    W = _windows_brute(N, s)
+    cols = sorted(v)
+    lo = sum(1 for j in cols if j < 128)
     total = 0
     for r in range(NT):
-        contig = {0} | {r - d for d in D if d <= r}
-        total += len(contig) + _column_chunks(v, r, contig)
+        q0 = 128 * r
+        win = [p for p in W if p < q0]
+        total += 1 + len(win)
+        # column chunks: entries from the first column past tile 0 to the last before the
+        # row block; a chunk is issued when one of its columns no window covers
+        issued = set()
+        for e, j in enumerate(cols):
+            if 128 <= j < q0 and not any(q0 - p <= j <= q0 - p + 127 for p in win):
+                issued.add((e - lo) // 128)
+        total += len(issued)
     return total
 
 
-def _column_chunks(v, r, contig):
-    """Column tiles of row block r: 128-entry chunks of the sorted column list, counted
-    from the first column past key tile 0, up to the last column before the row block;
-    a chunk is issued when it holds a column whose key tile no contiguous tile covers."""
-    cols = sorted(v)
-    entries = [j for j in cols if 1 <= (j >> 7) < r]
-    lo = sum(1 for j in cols if (j >> 7) < 1)
-    issued = set()
-    for e, j in enumerate(cols):
-        if j in entries and (j >> 7) not in contig:
-            issued.add((e - lo) // 128)
-    return len(issued)
-
-
-@pytest.mark.parametrize("N,kv,ks,seed", [(4096, 300, 7, 0), (8192, 1000, 40, 1), (2112, 50, 0, 2)])
+@pytest.mark.parametrize("N,kv,ks,seed", [(4096, 300, 7, 0), (8192, 1000, 40, 1), (2112, 50, 0, 2), (3000, 20, 200, 3)])
 def test_vs_tile_count_matches_enumeration(N, kv, ks, seed):
     rng = np.random.default_rng(seed)
     v = np.sort(rng.choice(N, size=kv, replace=False))
     s = np.sort(rng.choice(N, size=ks, replace=False)) if ks else np.zeros(0, dtype=np.int64)
+    assert F.vs_windows(N, s).tolist() == _windows_brute(N, s.tolist())
     assert F.vs_tiles(N, v, s) == _vs_tiles_brute(N, v.tolist(), s.tolist())
+
+
+@pytest.mark.parametrize("N,kv,ks,seed", [(1500, 40, 60, 5), (1024, 5, 400, 6), (2048, 300, 9, 7)])
+def test_vs_windows_cover_every_kept_key_once(N, kv, ks, seed):
+    """Every kept (q, j) of the oracle mask falls in exactly one unit of its row block:
+    tile 0 (j < 128), one window (windows mask keys below 128), or the column tiles
+    (a column no window covers)."""
+    rng = np.random.default_rng(seed)
+    v = np.sort(rng.choice(N, size=kv, replace=False))
+    s = np.sort(rng.choice(N, size=ks, replace=False))
+    W = F.vs_windows(N, s)
+    mask = O.vs_mask_rows(N, np.arange(N), v, s)
+    vset = set(v.tolist())
+    for q in range(N):
+        q0 = 128 * (q // 128)
+        win = [int(p) for p in W if p < q0]
+        for j in np.nonzero(mask[q])[0]:
+            n_win = sum(1 for p in win if q0 - p <= j <= q0 - p + 127) if j >= 128 else 0
+            units = (1 if j < 128 else 0) + n_win + (1 if (j >= 128 and j < q0 and j in vset and n_win == 0) else 0)
+            if j >= q0:  # the own row block: window p = 0 (or tile 0 when q0 = 0)
+                assert units == 1 and (q0 == 0 or 0 in win), (q, j)
+            assert units == 1, (q, int(j), units)
+    # windows are disjoint in key space: consecutive positions at least 128 apart
+    assert np.all(np.diff(W) >= 128) and W[0] == 0
+
+
+def test_windows_of_a_dense_offset_band_are_aligned():
+    # offsets 0 .. 999 selected: the windows step by 128 from 0, as aligned tiles would
+    N = 4096
+    W = F.vs_windows(N, np.arange(1000))
+    assert W.tolist() == list(range(0, 1000 + 128, 128))
 
 
 def test_dense_and_ashape_tiles():
@@ -77,6 +118,20 @@ def test_vs_expanded_kept_counts_match_oracle_mask(N, kv, ks, seed):
     s = np.sort(rng.choice(N, size=min(ks, N), replace=False)) if ks else np.zeros(0, dtype=np.int64)
     ref = O.vs_expanded_mask_rows(N, np.arange(N), v, s).sum(axis=1)
     np.testing.assert_array_equal(F.vs_expanded_kept_per_row(N, v, s).numpy(), ref)
+
+
+def _column_chunks(v, r, contig):
+    """Column tiles of row block r (aligned key tiles): 128-entry chunks of the sorted column
+    list, counted from the first column past key tile 0, up to the last column before the row
+    block; a chunk is issued when it holds a column whose key tile no contiguous tile covers."""
+    cols = sorted(v)
+    entries = [j for j in cols if 1 <= (j >> 7) < r]
+    lo = sum(1 for j in cols if (j >> 7) < 1)
+    issued = set()
+    for e, j in enumerate(cols):
+        if j in entries and (j >> 7) not in contig:
+            issued.add((e - lo) // 128)
+    return len(issued)
 
 
 def _vs_expanded_tiles_brute(N, v, s):

@@ -189,3 +189,22 @@ def test_block_tiles_pairing_covers_each_selection_once():
             assert sorted(kept[0]) == sorted(s0) and sorted(kept[1]) == sorted(s1)
             total += len(tiles)
         assert total == F.block_tiles(sel)
+
+
+def _offsets_from_gaps(start, gaps, N):
+    o = [start]
+    for g in gaps:
+        if o[-1] + g >= N:
+            break
+        o.append(o[-1] + g)
+    return np.array(o, dtype=np.int64)
+
+
+@pytest.mark.parametrize("N,seed", [(6000, 0), (200_000, 7)])
+def test_windows_on_chain_gap_patterns_match_stabbing_greedy(N, seed):
+    """Gaps of 1, 64 and 128 (one run), 129-255 (a run that may continue the chain),
+    256 and 300 (a new chain), at sizes with more runs than the index kernel has threads."""
+    rng = np.random.default_rng(seed)
+    gaps = rng.choice([129, 170, 255, 256, 300, 128, 64, 1], size=3000)
+    s = _offsets_from_gaps(int(rng.integers(0, 100)), gaps, N)
+    assert F.vs_windows(N, s).tolist() == _windows_brute(N, s.tolist())

@@ -74,14 +74,11 @@ struct AttnArgs {
                             //                 mode: bit e: 64-block distance e kept)
   const uint32_t* colbits;  // [n_heads, Nw]   bit j: column j selected
   // exact slashes: key windows p (row block r reads keys 128 r - p .. + 127 for
-  // every p < 128 r, besides tile 0); block-expanded: 128-aligned tile distances
-  const uint32_t* dbits;    // [n_heads, Dw]   exact: bit x + 128 when a window covers key
-                            //                 distance x = 128 r - j; expanded: bit t when
-                            //                 tile distance t is touched by a diagonal
-  const uint32_t* dfull;    // [n_heads, NTw]  exact: bit i when window i is kept whole;
-                            //                 expanded: bit t when distance t is
-  const int* dlist;         // [n_heads, NT]   exact: the windows, ascending; expanded: the
-                            //                 set bits of dbits, ascending
+  // every p < 128 r, besides tile 0); block-expanded slashes need offbits alone
+  const uint32_t* dbits;    // [n_heads, Dw]   bit x + 128 when a window covers key
+                            //                 distance x = 128 r - j
+  const uint32_t* dfull;    // [n_heads, NTw]  bit i when window i is kept whole
+  const int* dlist;         // [n_heads, NT]   the windows, ascending
   const int* dcount;        // [n_heads]
   const int* clist;         // [n_heads, MI_MAX_KV]  the selected columns, ascending
   const int* ccount;        // [n_heads]
@@ -123,7 +120,7 @@ struct AttnSmem {
   // bits of the chunks' entries; block: per tile (block A << 4) | sub-block mask, block B
   int list[MI_MAX_KV];
   int scan[192];
-  uint32_t dfull[512];  // VS: the head's whole-tile distance bits (N <= 2^21)
+  uint32_t dfull[512];  // VS: the head's whole-window bits (N <= 2^21)
   // VS: keep-masks of two tiles in flight (row i: bit c of word c / 32 keeps
   // key c of the tile), built by the loader warp; tile t uses stage t & 1
   uint32_t vmask[2][kBM][4];
@@ -138,8 +135,8 @@ struct AttnSmem {
   int col_lo;    // VS: first entry of the compacted column list past tile 0
   int n_tiles;   // tiles this CTA processes
   int n_contig;  // leading contiguous tiles (VS)
-  int has_t0;    // VS: tile 0 is prepended
-  int d_cnt;     // VS: number of tile distances <= r
+  int has_t0;    // VS (exact): tile 0 is prepended
+  int d_cnt;     // VS: windows p < 128 r; block-expanded: needed 64-key blocks
   int ash_init;  // A-shape: sink tokens of this head
   int ash_window;  // A-shape: window of this head
   int g_sigma, g_phi, g_lines;  // grid rows: stride, phase, rows on the lattice
@@ -172,29 +169,52 @@ struct TileRef {
   int j0;    // vertical-slash contiguous tiles: the first key
 };
 
+// Block-expanded slashes: row block r needs key block kb = 2 r + 1 - x for the set
+// bits x of a bitmap over x in [0, 2 r + 1] (a kept 64-block distance x or x - 1,
+// and x = 2 r + 1: block 0), held in list[kVsxBits ..]; the tiles pair them in
+// order of x.  The loader walks the bitmap once with this cursor (the tiles are
+// taken in order), so each tile costs a few bit operations.
+constexpr int kVsxBits = 128;  // up to 1024 words (2 r + 2 <= 32768)
+struct VsxCursor {
+  int w;       // current word
+  uint32_t m;  // its bits not yet taken
+  __device__ __forceinline__ int next(const AttnSmem& s) {  // the next set bit (one exists)
+    const uint32_t* fb = reinterpret_cast<const uint32_t*>(&s.list[kVsxBits]);
+    while (m == 0u && w < 1023) m = fb[++w];  // (bounded by the bitmap's 1024 words)
+    const int x = 32 * w + __ffs(m) - 1;
+    m &= m - 1;
+    return x;
+  }
+  __device__ __forceinline__ TileRef tile(const AttnSmem& s, int r, int i) {  // tile i < n_contig
+    TileRef ref{0, 0, 0xF, -1, 0};
+    ref.t = 2 * r + 1 - next(s);
+    if (2 * i + 1 < s.d_cnt) ref.t2 = 2 * r + 1 - next(s);
+    ref.j0 = ref.t * kBlk;
+    return ref;
+  }
+};
+
 template <int PAT>
 __device__ __forceinline__ TileRef tile_at(const AttnSmem& s, const AttnArgs& a, int n, int r,
                                            int i) {
   TileRef ref{0, 0, 0xF, 0};
   if (PAT == kPatDense || PAT == kPatRows) {
     ref.t = i;
+  } else if (PAT == kPatVSExp) {  // the block pairs come from a VsxCursor (loader)
+    ref.kind = 1;
+    ref.t = s.list[i - s.n_contig];  // chunk of the compacted column list
   } else if (is_vs(PAT)) {
     if (i < s.n_contig) {
       if (s.has_t0 && i == 0) {
         ref.t = 0;
         ref.t2 = -1;
         ref.j0 = 0;
-      } else {
+      } else {  // window p: keys 128 r - p ..
         const int idx = s.d_cnt - 1 - (i - s.has_t0);  // keys ascending
         const int p = ldg_ahead(a.dlist + (size_t)n * a.NT + idx);
-        if (PAT == kPatVS) {  // window p: keys 128 r - p ..
-          ref.j0 = r * kBN - p;
-          ref.t = ref.j0 >> 7;
-          ref.t2 = idx;
-        } else {  // tile distance p
-          ref.t = r - p;
-          ref.j0 = ref.t * kBN;
-        }
+        ref.j0 = r * kBN - p;
+        ref.t = ref.j0 >> 7;
+        ref.t2 = idx;
       }
     } else {
       ref.kind = 1;
@@ -276,25 +296,38 @@ __device__ __forceinline__ VsRaw4 vs_fetch4(const AttnSmem& s, const AttnArgs& a
   m.ref = ref;
   m.base = 0;
   m.whole = false;
-  if (ref.kind == 0) {
-    if (PAT == kPatVS) {  // a window whose keys all lie past tile 0
-      const int i = ref.t2;
-      m.whole = i >= 0 && ref.j0 >= kBN && ((s.dfull[i >> 5] >> (i & 31)) & 1u);
-    } else {
-      const int d = r - ref.t;
-      m.whole = d > 0 && ((s.dfull[d >> 5] >> (d & 31)) & 1u);
-    }
-  }
-  if (ref.kind != 0 || m.whole) return m;
   const uint32_t* off = a.offbits + (size_t)n * a.Nw;
   const uint32_t* col = a.colbits + (size_t)n * a.Nw;
-  const int j0 = ref.j0;
   if (PAT == kPatVSExp) {
-    const int e0 = max(2 * (r - ref.t) - 1, 0);
-    m.base = e0;
-    m.off[0] = ldg_ahead(off + (e0 >> 5));
-    m.off[1] = ldg_ahead(off + min((e0 >> 5) + 1, a.Nw - 1));
-  } else {
+    if (ref.kind != 0) return m;
+    // the tile is 64-key blocks A (keys 0-63) and B (keys 64-127, none when
+    // t2 < 0); bit h + 2 k of base: 64-row half h keeps block k (0: A, 1: B),
+    // i.e. block 0, or 64-block distance 2 r + h - block kept
+    const int blk[2] = {ref.t, ref.t2};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = 2 * r + h - blk[k];
+        const uint32_t w = ldg_ahead(off + min(max(e, 0) >> 5, a.Nw - 1));
+        const bool kept = blk[k] == 0 || (blk[k] > 0 && e >= 0 && ((w >> (e & 31)) & 1u));
+        if (blk[k] >= 0 && kept) m.base |= 1 << (h + 2 * k);
+      }
+#pragma unroll
+      for (int w = 0; w < 2; ++w)
+        m.col[2 * k + w] = (blk[k] >= 0) ? ldg_ahead(col + min(2 * blk[k] + w, a.Nw - 1)) : 0u;
+    }
+    // kept whole: both blocks, both halves, neither a causal block of the row block
+    m.whole = m.base == 0xF && ref.t < 2 * r && ref.t2 < 2 * r;
+    return m;
+  }
+  if (ref.kind == 0) {  // a window whose keys all lie past tile 0
+    const int i = ref.t2;
+    m.whole = i >= 0 && ref.j0 >= kBN && ((s.dfull[i >> 5] >> (i & 31)) & 1u);
+  }
+  if (ref.kind != 0 || m.whole) return m;
+  const int j0 = ref.j0;
+  {
     m.base = q0 - j0 - 127;
     const int w0 = m.base >> 5;  // floor; >= -4
 #pragma unroll
@@ -356,30 +389,6 @@ __device__ __forceinline__ void mask_finish(const AttnSmem& s, const AttnArgs& a
 #pragma unroll
       for (int w = 0; w < 4; ++w) out[w] = 0xFFFFFFFFu;
       return;  // never the diagonal tile (distance > 0)
-    }
-    if (PAT == kPatVSExp) {
-      // sub-block (row half rh, key half kh) sits at 64-block distance 2d + rh - kh
-      const int d = r - ref.t;
-      const int rh = (q >> 6) & 1;
-      const uint64_t win = (static_cast<uint64_t>(m.off[1]) << 32) | m.off[0];
-      auto kept = [&](int e) -> bool {
-        return e >= 0 && ((win >> (e - (m.base & ~31))) & 1u);
-      };
-      const uint32_t lo = kept(2 * d + rh) ? 0xFFFFFFFFu : 0u;
-      const uint32_t hi = kept(2 * d + rh - 1) ? 0xFFFFFFFFu : 0u;
-      out[0] = lo | m.col[0];
-      out[1] = lo | m.col[1];
-      out[2] = hi | m.col[2];
-      out[3] = hi | m.col[3];
-      if (j0 == 0) {  // the first 64 keys
-        out[0] = 0xFFFFFFFFu;
-        out[1] = 0xFFFFFFFFu;
-      }
-      if (ref.t == r) {  // causal
-#pragma unroll
-        for (int w = 0; w < 4; ++w) out[w] &= range_bits(j0 + 32 * w, 0, q + 1);
-      }
-      return;
     }
     // offsets q - j0 - c for c = 0..127 are the 128 bits starting at base, reversed
     const int sh = m.base & 31;
@@ -452,24 +461,32 @@ __device__ __forceinline__ void vs_masks4(const AttnSmem& s, const AttnArgs& a, 
     }
     return;
   }
-  if (ref.kind == 0 && !m.whole && ref.t != r) {
-    if (PAT == kPatVSExp) {
-      const int d = r - ref.t;  // >= 1
-      const uint64_t win = (static_cast<uint64_t>(m.off[1]) << 32) | m.off[0];
-      const int b = m.base & ~31;
+  if (PAT == kPatVSExp) {
+    // row i (q0 + 32 i) lies in 64-row half i / 2; a block of the row block's own
+    // two (>= 2 r) is causal
+    const int A = ref.t, Bb = ref.t2;
 #pragma unroll
-      for (int rh = 0; rh < 2; ++rh) {
-        const uint32_t lo = ((win >> (2 * d + rh - b)) & 1u) ? 0xFFFFFFFFu : 0u;
-        const uint32_t hi = ((win >> (2 * d + rh - 1 - b)) & 1u) ? 0xFFFFFFFFu : 0u;
-#pragma unroll
-        for (int i = 2 * rh; i < 2 * rh + 2; ++i) {
-          out[i][0] = lo | m.col[0];
-          out[i][1] = lo | m.col[1];
-          out[i][2] = hi | m.col[2];
-          out[i][3] = hi | m.col[3];
-        }
+    for (int i = 0; i < 4; ++i) {
+      const int h = i >> 1, q = q0 + 32 * i;
+      const uint32_t lo = (m.whole || ((m.base >> h) & 1)) ? 0xFFFFFFFFu : 0u;
+      const uint32_t hi = (m.whole || ((m.base >> (2 + h)) & 1)) ? 0xFFFFFFFFu : 0u;
+      out[i][0] = lo | m.col[0];
+      out[i][1] = lo | m.col[1];
+      out[i][2] = (Bb >= 0) ? (hi | m.col[2]) : 0u;
+      out[i][3] = (Bb >= 0) ? (hi | m.col[3]) : 0u;
+      if (A >= 2 * r) {
+        out[i][0] &= range_bits(A * kBlk, 0, q + 1);
+        out[i][1] &= range_bits(A * kBlk + 32, 0, q + 1);
       }
-    } else {
+      if (Bb >= 2 * r) {
+        out[i][2] &= range_bits(Bb * kBlk, 0, q + 1);
+        out[i][3] &= range_bits(Bb * kBlk + 32, 0, q + 1);
+      }
+    }
+    return;
+  }
+  if (ref.kind == 0 && !m.whole && ref.t != r) {
+    {
       const int sh = m.base & 31;
       uint32_t e[7];
 #pragma unroll
@@ -497,8 +514,10 @@ __device__ __forceinline__ void vs_masks4(const AttnSmem& s, const AttnArgs& a, 
     }
     return;
   }
+  if constexpr (PAT != kPatVSExp) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) mask_finish<PAT>(s, a, r, vs_row_raw(m, i, PAT == kPatVSExp), q0 + 32 * i, out[i]);
+    for (int i = 0; i < 4; ++i) mask_finish<PAT>(s, a, r, vs_row_raw(m, i, false), q0 + 32 * i, out[i]);
+  }
 }
 
 // ------------------------------------------------------------- prologue ----
@@ -522,16 +541,21 @@ __device__ __forceinline__ int block_excl_scan(int x, int* scratch, int* total) 
 }
 
 // A vertical column that no contiguous tile of row block r covers.
+// db: exact slashes the windows' coverage bits; block-expanded the kept 64-block
+// distances.
 template <int PAT>
 __device__ __forceinline__ bool residual_column(int j, int N, int r, const uint32_t* db) {
+  if (PAT == kPatVSExp) {  // past block 0, before the row block, in a block it does not need
+    if (j < kBlk || j >= N || j >= r * kBN) return false;
+    const int e = 2 * r - (j >> 6);  // >= 1; the block is needed for distance e or e + 1
+    const uint32_t w0 = __ldg(db + (e >> 5)), w1 = __ldg(db + ((e + 1) >> 5));
+    return !(((w0 >> (e & 31)) & 1u) || ((w1 >> ((e + 1) & 31)) & 1u));
+  }
   const int t = j >> 7;
   if (j < 0 || j >= N || t < 1 || t >= r) return false;
-  if (PAT == kPatVS) {  // no window covers key distance x = 128 r - j (bit x + 128)
-    const int x = r * kBN - j + kBN;
-    return !((__ldg(db + (x >> 5)) >> (x & 31)) & 1u);
-  }
-  const int d = r - t;
-  return !((__ldg(db + (d >> 5)) >> (d & 31)) & 1u);
+  // no window covers key distance x = 128 r - j (bit x + 128)
+  const int x = r * kBN - j + kBN;
+  return !((__ldg(db + (x >> 5)) >> (x & 31)) & 1u);
 }
 
 template <int PAT>
@@ -582,42 +606,59 @@ __device__ __forceinline__ void attn_prologue(AttnSmem& s, const AttnArgs& a, in
       s.n_tiles = n_sink + (r - t_lo + 1);
     }
   } else if (is_vs(PAT)) {
-    // contiguous tiles: tile 0, then the windows p < 128 r (exact slashes: keys
-    // 128 r - p ..) or the tiles r - delta of the distances delta <= r
-    // (block-expanded: tile 0 is one of them when r is a distance).  All threads
-    // count in parallel (independent loads).
-    const int* dl = a.dlist + (size_t)n * a.NT;
-    const int dc = __ldg(a.dcount + n);
-    int below = 0;  // s.has_t0 was set to 1 before the barrier-init sync
-    for (int e = tid; e < dc; e += 192) {
-      const int d = __ldg(dl + e);
-      if (PAT == kPatVS) {
-        below += (d < r * kBN) ? 1 : 0;
-      } else {
-        below += (d <= r) ? 1 : 0;
-        if (d == r) s.has_t0 = 0;
+    if (PAT == kPatVSExp) {
+      // the key blocks this row block needs: x = 2 r + 1 - kb for x in [0, 2 r + 1]
+      // with 64-block distance x or x - 1 kept, and x = 2 r + 1 (block 0), as a
+      // bitmap over x in list[kVsxBits ..]
+      const uint32_t* eb = a.offbits + (size_t)n * a.Nw;
+      const int X = 2 * r + 2, nfw = cdiv(X, 32);
+      uint32_t* fb = reinterpret_cast<uint32_t*>(&s.list[kVsxBits]);
+      int mine = 0;
+      for (int w = tid; w < nfw; w += 192) {
+        const uint32_t ew = __ldg(eb + w), ep = (w > 0) ? __ldg(eb + w - 1) : 0u;
+        uint32_t f = ew | (ew << 1) | (ep >> 31);
+        if (w == nfw - 1) {
+          f |= 1u << ((X - 1) & 31);                   // x = 2 r + 1: block 0
+          if (X & 31) f &= (1u << (X & 31)) - 1u;     // nothing past x = 2 r + 1
+        }
+        fb[w] = f;
+        mine += __popc(f);
       }
+      int total;
+      block_excl_scan(mine, s.scan, &total);  // (its barriers also publish the bitmap)
+      if (tid == 0) {
+        s.d_cnt = total;                // needed blocks, paired two per tile
+        s.n_contig = (total + 1) >> 1;
+      }
+    } else {
+      // contiguous tiles: tile 0, then the windows p < 128 r (keys 128 r - p ..).
+      // All threads count in parallel (independent loads).
+      const int* dl = a.dlist + (size_t)n * a.NT;
+      const int dc = __ldg(a.dcount + n);
+      int below = 0;  // s.has_t0 was set to 1 before the barrier-init sync
+      for (int e = tid; e < dc; e += 192) below += (__ldg(dl + e) < r * kBN) ? 1 : 0;
+      int n_below;
+      block_excl_scan(below, s.scan, &n_below);
+      if (tid == 0) {
+        s.d_cnt = n_below;
+        s.n_contig = n_below + s.has_t0;
+      }
+      for (int w = tid; w < a.NTw; w += 192) s.dfull[w] = __ldg(a.dfull + (size_t)n * a.NTw + w);
     }
-    int n_below;
-    block_excl_scan(below, s.scan, &n_below);
-    if (tid == 0) {
-      s.d_cnt = n_below;
-      s.n_contig = n_below + s.has_t0;
-    }
-    for (int w = tid; w < a.NTw; w += 192) s.dfull[w] = __ldg(a.dfull + (size_t)n * a.NTw + w);
     // column tiles: chunks of 128 entries of the head's compacted column list,
     // from the first column past tile 0 (entry lo) to the last before this row
     // block (entry hi); an entry is kept when its column is residual (no
     // contiguous tile of this row block covers it), a chunk when it keeps one
     const int* cl = a.clist + (size_t)n * MI_MAX_KV;
-    const uint32_t* db = a.dbits + (size_t)n * a.Dw;
+    const uint32_t* db = (PAT == kPatVSExp) ? a.offbits + (size_t)n * a.Nw : a.dbits + (size_t)n * a.Dw;
     const int cnt = __ldg(a.ccount + n);
+    const int j_first = (PAT == kPatVSExp) ? kBlk : kBN;  // past block 0, or past tile 0
     uint32_t* resbits = reinterpret_cast<uint32_t*>(&s.list[16]);  // 64 words: entries lo .. lo + 2047
     if (tid < 64) resbits[tid] = 0u;
     int c_lo = 0, c_hi = 0;
     for (int e = tid; e < cnt; e += 192) {
       const int j = __ldg(cl + e);
-      c_lo += (j < kBN) ? 1 : 0;
+      c_lo += (j < j_first) ? 1 : 0;
       c_hi += (j < r * kBN) ? 1 : 0;
     }
     int lo, hi;
@@ -855,15 +896,24 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
     int issued = 0;
     // the next tile's reference (a global load for vertical-slash heads) is read
     // before waiting for the buffers, so its latency overlaps those waits
-    TileRef ref_next = (T > 0) ? tile_at<PAT>(s, a, n, r, 0) : TileRef{0, 0, 0, 0};
+    VsxCursor cur{0, (PAT == kPatVSExp) ? reinterpret_cast<const uint32_t*>(&s.list[kVsxBits])[0] : 0u};
+    auto next_ref = [&](int i) -> TileRef {
+      if (PAT == kPatVSExp && i < s.n_contig) return cur.tile(s, r, i);
+      return tile_at<PAT>(s, a, n, r, i);
+    };
+    TileRef ref_next = (T > 0) ? next_ref(0) : TileRef{0, 0, 0, 0};
     auto load = [&](const TileRef& ref, const CUtensorMap* map, const CUtensorMap* rows_map,
                     uint64_t* full, uint8_t (*buf)[16384]) {
       if (ref.kind == 0) {
         // two 64-key boxes per 64-column half: keys 0-63 and 64-127 of the
         // tile (for block-sparse tiles, blocks ref.t and ref.t2)
         if (lane_id() == 0) {
-          const int ka = (PAT == kPatBlock) ? ref.t * kBlk : is_vs(PAT) ? ref.j0 : ref.t * kBN;
-          const int kb = (PAT == kPatBlock) ? ref.t2 * kBlk : is_vs(PAT) ? ref.j0 + kBlk : ref.t * kBN + kBlk;
+          // block pattern: blocks t and t2; block-expanded slashes: blocks t and t2 (t
+          // again when there is no second block: loaded, masked out)
+          const int ka = (PAT == kPatBlock || PAT == kPatVSExp) ? ref.t * kBlk : is_vs(PAT) ? ref.j0 : ref.t * kBN;
+          const int kb = (PAT == kPatBlock) ? ref.t2 * kBlk
+                         : (PAT == kPatVSExp) ? (ref.t2 >= 0 ? ref.t2 : ref.t) * kBlk
+                         : is_vs(PAT) ? ref.j0 + kBlk : ref.t * kBN + kBlk;
           mbar_arrive_expect_tx(full, 2 * 16384);
           tma_load_3d(buf[0], map, full, 0, ka, g);
           tma_load_3d(buf[0] + 8192, map, full, 0, kb, g);
@@ -893,7 +943,7 @@ __device__ __forceinline__ void attn_body(uint8_t* smem_raw, const CUtensorMap& 
       const TileRef ref = ref_next;
       VsRaw4 raw;
       if (is_vs(PAT)) raw = raw_next;
-      if (t + 1 < T) ref_next = tile_at<PAT>(s, a, n, r, t + 1);
+      if (t + 1 < T) ref_next = next_ref(t + 1);
       if (t >= 1 && !mbar_wait_warp(&s.k_empty, (t - 1) & 1, abort, lim)) break;
       load(ref, &map_k, &map_kr, &s.k_full, s.k);
       if (is_vs(PAT)) {

@@ -22,15 +22,11 @@
 //            columns' K and V rows are then copied side by side
 //            (vs_colgather_kernel), so that the attention kernel loads the
 //            column tiles with plain TMA boxes.
-// Block-expanded mode (every 64x64 block a selected diagonal crosses is kept;
-// 128-aligned tiles):
+// Block-expanded mode (every 64x64 block a selected diagonal crosses is kept):
 //   offbits then holds D64, bit e set for the 64-block distances e = o/64 and
-//            (o % 64 != 0) o/64 + 1 of the selected offsets, and e = 0;
-//   dbits    bit delta set when one of the 64-block distances 2 delta - 1,
-//            2 delta, 2 delta + 1 (those of the four 64x64 sub-blocks of a
-//            128x128 tile at distance delta) is in D64;
-//   dlist    the set distances of dbits in ascending order, dcount of them;
-//   dfull    bit delta (> 0) set when all three are.
+//            (o % 64 != 0) o/64 + 1 of the selected offsets, and e = 0; the
+//            attention kernel derives each row block's needed 64-key blocks
+//            from it and pairs them two per tile (dbits, dlist, dfull unused).
 // All are O(N/32 + k) words per head, the same for every row block.  The
 // entries are validated here: a value out of [0, N) or not strictly above its
 // predecessor raises MI_ERR_INDEX in the status word and is skipped; -1 is
@@ -119,7 +115,6 @@ __device__ int vs_window_chain(const int* runA, const int* runL, int R, int ks, 
 }
 
 __global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ VsIndexArgs a) {
-  __shared__ uint32_t db[512];
   __shared__ int scan[512];
   extern __shared__ int run_smem[];  // exact mode: run first offsets [NT + 1], run last offsets [NT + 1]
   const int n = blockIdx.x, tid = threadIdx.x;
@@ -131,7 +126,6 @@ __global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ V
     col[w] = 0u;
   }
   for (int w = tid; w < a.Dw; w += 512) dbh[w] = 0u;
-  db[tid] = 0u;
   __syncthreads();
   const int32_t* si = a.s_idx + (size_t)n * a.k_s;
   for (int e = tid; e < a.k_s; e += 512) {
@@ -181,37 +175,8 @@ __global__ void __launch_bounds__(512) vs_index_kernel(const __grid_constant__ V
       for (uint32_t m = __ldcg(col + w); m; m &= m - 1) cl[pos++] = 32 * w + __ffs(m) - 1;
     if (tid == 511) a.ccount[n] = cs[511];
   }
-  if (a.expanded) {
-    // 128-tile distance delta: its sub-blocks sit at 64-block distances
-    // 2 delta - 1 .. 2 delta + 1 (read back through L2: built with atomics)
-    const int NB = (a.N + 63) >> 6;
-    if (tid == 0) atomicOr(&db[0], 1u);
-    for (int d = tid; d < a.NT; d += 512) {
-      bool any = false;
-      for (int e = 2 * d - 1; e <= 2 * d + 1; ++e)
-        if (e >= 0 && e < NB && ((__ldcg(off + (e >> 5)) >> (e & 31)) & 1u)) any = true;
-      if (any) atomicOr(&db[d >> 5], 1u << (d & 31));
-    }
-    // tile distances whose three sub-block distances are all kept
-    __shared__ uint32_t dfw[512];
-    dfw[tid] = 0u;
-    __syncthreads();
-    for (int d = 1 + tid; d < a.NT; d += 512) {
-      bool all = true;
-      for (int e = 2 * d - 1; e <= 2 * d + 1 && all; ++e)
-        all = e < NB && ((__ldcg(off + (e >> 5)) >> (e & 31)) & 1u);
-      if (all) atomicOr(&dfw[d >> 5], 1u << (d & 31));
-    }
-    __syncthreads();
-    if (tid < a.NTw) a.dfull[(size_t)n * a.NTw + tid] = dfw[tid];
-    // dbits to global, then the ascending list of set distances
-    const uint32_t word = (tid < a.NTw) ? db[tid] : 0u;
-    if (tid < a.NTw) dbh[tid] = word;
-    int total;
-    int pos = scan512(__popc(word), scan, &total);
-    int* dl = a.dlist + (size_t)n * a.NT;
-    for (uint32_t w = word; w; w &= w - 1) dl[pos++] = tid * 32 + (__ffs(w) - 1);
-    if (tid == 0) a.dcount[n] = total;
+  if (a.expanded) {  // the attention pairs the needed 64-key blocks from offbits alone
+    if (tid == 0) a.dcount[n] = 0;
     return;
   }
   // ---- exact mode: key windows (the bitmap was built with atomics: read through L2)

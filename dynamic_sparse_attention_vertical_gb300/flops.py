@@ -153,15 +153,16 @@ def vs_windows(N: int, s_idx) -> np.ndarray:
     return np.asarray(ws, dtype=np.int64)
 
 
-def _column_tiles(N: int, v_idx, NT: int, residual) -> int:
+def _column_tiles(N: int, v_idx, NT: int, residual, first: int = 128) -> int:
     """Column tiles: chunks of 128 entries of the sorted column list from the first
-    column past tile 0 to the last before the row block; a chunk is issued when one
-    of its columns is residual (residual(rr, t) over the entries' columns t)."""
+    column at or past key `first` (past tile 0, or past block 0) to the last before
+    the row block; a chunk is issued when one of its columns is residual
+    (residual(rr, j) over the entries' columns j)."""
     v = torch.as_tensor(v_idx).long()
     v = torch.unique(v[(v >= 0) & (v < N)]).numpy()
-    lo = int((v < 128).sum())
+    lo = int((v < first).sum())
     col_tiles = 0
-    for rr in range(2, NT):
+    for rr in range(1, NT):
         hi = int(np.searchsorted(v, 128 * rr))  # entries with key < 128 rr
         if hi <= lo:
             continue
@@ -181,17 +182,19 @@ def vs_tiles(N: int, v_idx, s_idx, expanded: bool = False) -> int:
         for p in W:
             cov[p:p + 128] = True
         return int(contig.sum()) + _column_tiles(N, v_idx, NT, lambda rr, j: ~cov[128 * rr - j + 127])
-    # tile distance d holds the 64-blocks at block distances 2d-1 .. 2d+1
-    e = _expanded_dist(N, s_idx, 64)
-    ep = torch.zeros(2 * NT + 2, dtype=torch.bool)
-    ep[1:1 + e.numel()] = e                       # ep[x + 1] = e[x]
-    dd = torch.arange(NT)
-    d = (ep[2 * dd] | ep[2 * dd + 1] | ep[2 * dd + 2]).numpy()
-    dcum = np.cumsum(d)                           # distances <= r
+    # block-expanded: row block r needs key block kb when 2r - kb or 2r + 1 - kb (the
+    # distances from its two 64-row halves) is a kept 64-block distance, and block 0;
+    # with x = 2r + 1 - kb that is f[x] = e[x] | e[x - 1] for x in [0, 2r], plus x = 2r + 1.
+    # The needed blocks are paired two per tile.
+    e = _expanded_dist(N, s_idx, 64).numpy()
+    f = np.zeros(2 * NT + 2, dtype=bool)
+    f[: e.shape[0]] = e
+    f[1: e.shape[0] + 1] |= e
+    pf = np.concatenate([[0], np.cumsum(f)])          # pf[x] = f[0 .. x - 1].sum()
     r = np.arange(NT)
-    has_t0 = ~d[r]                                # tile 0 added unless distance r is set
-    contig = dcum + has_t0
-    return int(contig.sum()) + _column_tiles(N, v_idx, NT, lambda rr, j: ~d[rr - (j >> 7)])
+    n = pf[2 * r + 1] + 1
+    pairs = int(((n + 1) // 2).sum())
+    return pairs + _column_tiles(N, v_idx, NT, lambda rr, j: ~f[2 * rr + 1 - (j >> 6)], first=64)
 
 
 def dense_tiles(N: int) -> int:

@@ -120,31 +120,49 @@ def test_vs_expanded_kept_counts_match_oracle_mask(N, kv, ks, seed):
     np.testing.assert_array_equal(F.vs_expanded_kept_per_row(N, v, s).numpy(), ref)
 
 
-def _column_chunks(v, r, contig):
-    """Column tiles of row block r (aligned key tiles): 128-entry chunks of the sorted column
-    list, counted from the first column past key tile 0, up to the last column before the row
-    block; a chunk is issued when it holds a column whose key tile no contiguous tile covers."""
-    cols = sorted(v)
-    entries = [j for j in cols if 1 <= (j >> 7) < r]
-    lo = sum(1 for j in cols if (j >> 7) < 1)
-    issued = set()
-    for e, j in enumerate(cols):
-        if j in entries and (j >> 7) not in contig:
-            issued.add((e - lo) // 128)
-    return len(issued)
+def _expanded_blocks_brute(r, D):
+    """Key blocks row block r needs in the block-expanded mode: a 64-row half at 64-block
+    row 2r + rh keeps block kb when (2r + rh) - kb is a kept block distance; block 0 always."""
+    return {0} | {kb for kb in range(2 * r + 2) for rh in (0, 1) if (2 * r + rh) - kb in D}
 
 
 def _vs_expanded_tiles_brute(N, v, s):
-    """Enumerate: a 128x128 tile (r, t) is issued when one of its four 64x64 blocks is in the
-    block-expanded mask's block set, or t = 0, or it holds a residual column."""
+    """Enumerate: the needed 64-key blocks of each row block are paired two per tile; a column
+    tile (128 entries of the sorted column list past block 0) is issued when one of its columns
+    lies in a block the row block does not need."""
     NT = (N + 127) // 128
     D = {0} | {o // 64 for o in s} | {o // 64 + 1 for o in s if o % 64}
+    cols = sorted(v)
+    lo = sum(1 for j in cols if j < 64)
     total = 0
     for r in range(NT):
-        contig = {0} | {t for t in range(r + 1)
-                        if any((2 * r + rh) - (2 * t + kh) in D for rh in (0, 1) for kh in (0, 1))}
-        total += len(contig) + _column_chunks(v, r, contig)
+        need = _expanded_blocks_brute(r, D)
+        total += (len(need) + 1) // 2
+        issued = set()
+        for e, j in enumerate(cols):
+            if 64 <= j < 128 * r and (j >> 6) not in need:
+                issued.add((e - lo) // 128)
+        total += len(issued)
     return total
+
+
+@pytest.mark.parametrize("N,kv,ks,seed", [(1500, 40, 60, 5), (2048, 300, 9, 7), (1000, 3, 500, 8)])
+def test_vs_expanded_blocks_cover_every_kept_key_once(N, kv, ks, seed):
+    """Every kept (q, j) of the oracle's block-expanded mask lies in exactly one needed block of
+    its row block or (a column in a block it does not need) in the column tiles."""
+    rng = np.random.default_rng(seed)
+    v = np.sort(rng.choice(N, size=kv, replace=False))
+    s = np.sort(rng.choice(N, size=ks, replace=False))
+    D = {0} | {o // 64 for o in s} | {o // 64 + 1 for o in s if o % 64}
+    mask = O.vs_expanded_mask_rows(N, np.arange(N), v, s)
+    vset = set(v.tolist())
+    for q in range(N):
+        r = q // 128
+        need = _expanded_blocks_brute(r, D)
+        for j in np.nonzero(mask[q])[0]:
+            in_blocks = (j >> 6) in need
+            in_cols = (64 <= j < 128 * r) and (j in vset) and not in_blocks
+            assert in_blocks + in_cols == 1, (q, int(j))
 
 
 @pytest.mark.parametrize("N,kv,ks,seed", [(4096, 300, 7, 0), (8192, 1000, 40, 1), (2112, 50, 0, 2)])

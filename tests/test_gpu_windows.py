@@ -91,3 +91,41 @@ def test_more_runs_than_index_threads():
     rows = np.unique(np.concatenate([np.arange(65_536 - 128, 65_536 + 128), np.arange(N - 200, N),
                                      rng.choice(N, size=200, replace=False)]))
     _run(N, sis, vis, rows)
+
+
+def _run_expanded(N, sis, vis, rows):
+    Hq = len(sis)
+    x = I.literal_inputs(Hq, 1, N, n_cols=0, n_offsets=0, seed=N % 89)
+    q, k, v = x.q.to(DEV), x.k.to(DEV), x.v.to(DEV)
+    ks = max(len(s) for s in sis)
+    kv = max(1, max(len(c) for c in vis))
+    s_idx = torch.full((Hq, ks), -1, dtype=torch.int32)
+    v_idx = torch.full((Hq, kv), -1, dtype=torch.int32)
+    for h in range(Hq):
+        s_idx[h, : len(sis[h])] = torch.as_tensor(sis[h], dtype=torch.int32)
+        v_idx[h, : len(vis[h])] = torch.as_tensor(vis[h], dtype=torch.int32)
+    out = B.mi_vs_sparse_attn(q, k, v, v_idx.to(DEV), s_idx.to(DEV), expanded=True)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    for h in range(Hq):
+        ref, _ = O.attention_rows(x.q[h], x.k[0], x.v[0], rows,
+                                  lambda r, h=h: O.vs_expanded_mask_rows(N, r, vis[h], sis[h]))
+        assert_close(o[h][rows], ref, f"expanded h{h}")
+
+
+def test_expanded_pairs_ragged_n_and_block_one_columns():
+    """Block-expanded slashes, whose needed 64-key blocks are paired two per tile: a ragged
+    last row block (its second own block lies past N), odd block counts, columns in block 1
+    (residual whenever block 1 is not needed), isolated far distances."""
+    N = 4000  # 31.25 row blocks
+    sis = [np.array([1, 64, 65, 200, 1000, 3900]), np.array([5, 3000])]
+    vis = [np.array([64, 70, 127, 128, 500, 3999]), np.array([65, 66, 2000])]
+    _run_expanded(N, sis, vis, np.arange(N))
+
+
+def test_expanded_pairs_dense_band_and_gaps():
+    N = 6000
+    sis = [np.arange(0, 1500, 3), _offsets_from_gaps(7, [64, 65, 128, 129, 200, 640, 1000], N)]
+    rng = np.random.default_rng(3)
+    vis = [np.sort(rng.choice(N, size=300, replace=False)), np.zeros(0, dtype=np.int64)]
+    _run_expanded(N, sis, vis, np.arange(N))

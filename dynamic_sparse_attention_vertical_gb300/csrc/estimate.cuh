@@ -73,7 +73,7 @@ constexpr size_t kEstSmem1 = sizeof(EstSmem) + 1024 + sizeof(float) * 2 * 128 * 
 constexpr size_t kEstSmem2 = sizeof(EstSmem) + 1024 + sizeof(float) * 2 * kSkSlot;
 
 template <int PASS>
-__global__ void __launch_bounds__(kEstThreads, 1)
+__global__ void __launch_bounds__(kEstThreads, PASS == 1 ? 2 : 1)
 est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ EstArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -186,39 +186,47 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       // On a failed (timed-out) wait the loop still runs to the end with zeros, so
       // that the math warps keep meeting at the named barrier below.
       const bool ok = mbar_wait_warp(&s.s_full[b], (t >> 1) & 1, abort, lim);
-      float x[64];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld64(taddr + b * 128, x);
-        tc_fence_before();
-        mbar_arrive(&s.s_empty[b]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = 0.f;
-      }
       const int j0 = k_lo + t * kBN;
-      // keys j0 + 64 ch + c with c <= lim_c are causal; rows of an absent second head are dropped
-      const int lim_c = (slot >= 0) ? p_i - j0 - 64 * ch : -1;
-      if (lim_c < 63) {  // all 64 keys causal (every tile but the last ones): no per-key select
+      // the thread's 64 columns in two halves of 32 (a running max and sum over
+      // them), which keeps the registers within two CTAs per SM
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = (c <= lim_c) ? x[c] : -INFINITY;
+      for (int hf = 0; hf < 2; ++hf) {
+        float x[32];
+        if (ok) {
+          tc_fence_after();
+          tmem_ld32(taddr + b * 128 + 32 * hf, x);
+          if (hf == 1) {
+            tc_fence_before();
+            mbar_arrive(&s.s_empty[b]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[c] = 0.f;
+        }
+        // keys j0 + 64 ch + 32 hf + c with c <= lim_c are causal; rows of an absent
+        // second head are dropped
+        const int lim_c = (slot >= 0) ? p_i - j0 - 64 * ch - 32 * hf : -1;
+        if (lim_c < 31) {  // all 32 keys causal (every tile but the last ones): no per-key select
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[c] = (c <= lim_c) ? x[c] : -INFINITY;
+        }
+        // the scale is positive, so the maximum of the scaled scores is the scaled
+        // maximum (rounding is monotone)
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mx = fmaxf(mx, x[c]);
+        const float mn = fmaxf(m, mx * a.scale_log2);
+        const float mb = (mn == -INFINITY) ? 0.f : mn;
+        const float2 nmb2 = make_float2(-mb, -mb);
+        float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float2 y = fma2(make_float2(x[c], x[c + 1]), sc2, nmb2);
+          acc2 = add2(acc2, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+        }
+        z = z * fast_exp2(m - mb) + (acc2.x + acc2.y);
+        m = mn;
       }
-      // the scale is positive, so the maximum of the scaled scores is the scaled
-      // maximum (rounding is monotone)
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
-      const float mn = fmaxf(m, mx * a.scale_log2);
-      const float mb = (mn == -INFINITY) ? 0.f : mn;
-      const float2 nmb2 = make_float2(-mb, -mb);
-      float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float2 y = fma2(make_float2(x[c], x[c + 1]), sc2, nmb2);
-        acc2 = add2(acc2, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
-      }
-      z = z * fast_exp2(m - mb) + (acc2.x + acc2.y);
-      m = mn;
     }
     // merge the two column halves of each row, in a fixed order
     float(*mz)[128][2] = reinterpret_cast<float(*)[128][2]>(Sk);

@@ -357,7 +357,7 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
   if ((rc = launched("estimation pass 1"))) return rc;
   est_combine<<<cdiv(n_heads * kLastQ, 8), 256, 0, st>>>(a.part, a.stats, L.NC, n_heads * kLastQ);
   if ((rc = launched("estimation combine"))) return rc;
-  est_kernel<2><<<grid, kEstThreads, kEstSmem2, st>>>(mq, mk, a);
+  est_kernel<2><<<dim3(np, cdiv(N, kChunkKeys2)), kEstThreads, kEstSmem2, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 2"))) return rc;
   if (ld_v > 0 || ld_s > 0) {
     vs_topk_kernel<<<dim3(n_heads, 2), 1024, kTopkSmemBytes, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx, ld_v,

@@ -7,7 +7,8 @@
 // diagonal offset o = q - j (slash score s).
 //
 // Layout of the work: one CTA takes a pair of q-heads that share a KV head
-// (128 query rows = 2 x 64, one UMMA M) and a chunk of 1024 keys, and runs
+// (128 query rows = 2 x 64, one UMMA M) and a chunk of keys (1024 in pass 1,
+// 2048 in pass 2), and runs
 // S = Q K^T per 128-key tile on the tensor cores (TMEM accumulator), so each
 // K tile is read once for both heads.  Eight warps do the arithmetic, two
 // threads per row (64 keys of each tile each).
@@ -63,6 +64,9 @@ struct EstSmem {
 // and key column c runs along i -> c + 63 - i.  Positions outside a row's 64
 // keys stay zero (written once).  Two slots: one is written while the other is
 // summed.  Pass 1 uses the same space for the two column halves' (m, z).
+// Pass 2 takes chunks of 2048 keys (its halo tile is then 1/17 of a CTA's tiles,
+// not 1/9); pass 1 keeps 1024 (its partials are per 1024-key chunk).
+constexpr int kChunkKeys2 = 2048;
 constexpr int kSkPitch = 128;
 constexpr int kSkHead = 64 * kSkPitch;
 constexpr int kSkSlot = 2 * kSkHead;
@@ -90,8 +94,9 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int g = ha / a.group;
   const int N = a.N;
   const int R = a.row_end ? min(max(__ldg(a.row_end), kLastQ), N) : N;  // one past the last query row
-  const int k_lo = chunk * kChunkKeys - ((PASS == 2 && chunk > 0) ? kBN : 0);
-  const int k_hi = min(N, (chunk + 1) * kChunkKeys);
+  constexpr int CK = (PASS == 1) ? kChunkKeys : kChunkKeys2;  // keys of this CTA's chunk
+  const int k_lo = chunk * CK - ((PASS == 2 && chunk > 0) ? kBN : 0);
+  const int k_hi = min(N, (chunk + 1) * CK);
   const int T = cdiv(k_hi - k_lo, kBN);
   const bool has_halo = (PASS == 2 && chunk > 0);
 
@@ -246,7 +251,7 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const int mt = tid - 128;  // 0..255
     if (R < N) {
       // offsets R .. N-1 meet no query row: zero, this chunk's share of them
-      for (int o = R + chunk * kChunkKeys + mt; o < min(N, R + (chunk + 1) * kChunkKeys); o += kEstMath) {
+      for (int o = R + chunk * CK + mt; o < min(N, R + (chunk + 1) * CK); o += kEstMath) {
         a.ssc[(size_t)slot_a * N + o] = 0.f;
         if (slot_b >= 0) a.ssc[(size_t)slot_b * N + o] = 0.f;
       }

@@ -54,6 +54,22 @@ def test_varlen_equals_the_layer_call_per_sequence():
         assert torch.equal(lse[:, lo:hi], rl), f"sequence {b} lse"
 
 
+def test_varlen_block_expanded_equals_the_layer_call_per_sequence():
+    """The block-expanded slash mode (needed 64-key blocks paired per tile) over ragged
+    packed lengths: each sequence's rows equal its own layer call, bit for bit."""
+    Hq, Hkv = 2, 1
+    lens = [1500, 130, 2100]
+    seqs, q, k, v, cu = _packed(Hq, Hkv, lens, seed=60)
+    cfg = [H.vs(48, 24, expanded=True), H.vs(16, 64)]
+    out = B.mi_layer_attn_varlen(q, k, v, cu, cfg)
+    torch.cuda.synchronize()
+    for b, n in enumerate(lens):
+        s = seqs[b]
+        ro = B.mi_layer_attn(s.q, s.k, s.v, cfg)
+        torch.cuda.synchronize()
+        assert torch.equal(out[:, cu[b]:cu[b + 1]], ro), f"sequence {b}"
+
+
 def test_varlen_sequences_do_not_see_each_other():
     Hq, Hkv = 2, 1
     lens = [700, 1300]

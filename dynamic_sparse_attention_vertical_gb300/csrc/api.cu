@@ -233,6 +233,18 @@ int set_smem(const void* kernel, size_t bytes) {
   return e == cudaSuccess ? MI_OK : cuda_fail(e, "cudaFuncSetAttribute");
 }
 
+// SMs of the current device, queried once per device.
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
 int launched(const char* what) {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MI_OK : cuda_fail(e, what);
@@ -339,6 +351,7 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
   a.status = status;
   a.wait_limit_ns = kWaitLimitNs;
   a.row_end = row_end;
+  a.chunk2 = est_chunk2(np, N, sm_count());
 
   static std::once_flag once;
   static int once_rc = MI_OK;
@@ -357,7 +370,7 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
   if ((rc = launched("estimation pass 1"))) return rc;
   est_combine<<<cdiv(n_heads * kLastQ, 8), 256, 0, st>>>(a.part, a.stats, L.NC, n_heads * kLastQ);
   if ((rc = launched("estimation combine"))) return rc;
-  est_kernel<2><<<dim3(np, cdiv(N, kChunkKeys2)), kEstThreads, kEstSmem2, st>>>(mq, mk, a);
+  est_kernel<2><<<dim3(np, cdiv(N, a.chunk2)), kEstThreads, kEstSmem2, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 2"))) return rc;
   if (ld_v > 0 || ld_s > 0) {
     vs_topk_kernel<<<dim3(n_heads, 2), 1024, kTopkSmemBytes, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx, ld_v,

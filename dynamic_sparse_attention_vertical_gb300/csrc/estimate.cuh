@@ -8,7 +8,7 @@
 //
 // Layout of the work: one CTA takes a pair of q-heads that share a KV head
 // (128 query rows = 2 x 64, one UMMA M) and a chunk of keys (1024 in pass 1,
-// 2048 in pass 2), and runs
+// 1024-4096 in pass 2), and runs
 // S = Q K^T per 128-key tile on the tensor cores (TMEM accumulator), so each
 // K tile is read once for both heads.  Eight warps do the arithmetic, two
 // threads per row (64 keys of each tile each).
@@ -35,6 +35,7 @@ namespace mi {
 
 struct EstArgs {
   int N, group, n_pairs, NC;
+  int chunk2;    // pass-2 keys per CTA (a multiple of 128)
   float scale_log2;
   float* part;   // [n_heads, 64, NC, 2]  pass-1 partials (m, z)
   float* stats;  // [n_heads, 64, 2]      (m, 1/z)
@@ -64,9 +65,15 @@ struct EstSmem {
 // and key column c runs along i -> c + 63 - i.  Positions outside a row's 64
 // keys stay zero (written once).  Two slots: one is written while the other is
 // summed.  Pass 1 uses the same space for the two column halves' (m, z).
-// Pass 2 takes chunks of 2048 keys (its halo tile is then 1/17 of a CTA's tiles,
-// not 1/9); pass 1 keeps 1024 (its partials are per 1024-key chunk).
-constexpr int kChunkKeys2 = 2048;
+// Pass 2 takes chunks of EstArgs::chunk2 keys, the largest of 4096, 2048 and 1024
+// that still gives every SM a CTA (longer chunks make the halo tile a smaller
+// share: 1/33 of a CTA's tiles at 4096 keys, 1/9 at 1024); pass 1 keeps 1024 (its
+// partials are per 1024-key chunk).
+inline int est_chunk2(int n_pairs, int N, int n_sms) {
+  for (int c = 4096; c > 1024; c >>= 1)
+    if (n_pairs * cdiv(N, c) >= n_sms) return c;
+  return 1024;
+}
 constexpr int kSkPitch = 128;
 constexpr int kSkHead = 64 * kSkPitch;
 constexpr int kSkSlot = 2 * kSkHead;
@@ -94,7 +101,7 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int g = ha / a.group;
   const int N = a.N;
   const int R = a.row_end ? min(max(__ldg(a.row_end), kLastQ), N) : N;  // one past the last query row
-  constexpr int CK = (PASS == 1) ? kChunkKeys : kChunkKeys2;  // keys of this CTA's chunk
+  const int CK = (PASS == 1) ? kChunkKeys : a.chunk2;  // keys of this CTA's chunk
   const int k_lo = chunk * CK - ((PASS == 2 && chunk > 0) ? kBN : 0);
   const int k_hi = min(N, (chunk + 1) * CK);
   const int T = cdiv(k_hi - k_lo, kBN);

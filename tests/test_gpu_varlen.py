@@ -60,7 +60,7 @@ def test_varlen_block_expanded_equals_the_layer_call_per_sequence():
     Hq, Hkv = 2, 1
     lens = [1500, 130, 2100]
     seqs, q, k, v, cu = _packed(Hq, Hkv, lens, seed=60)
-    cfg = [H.vs(48, 24, expanded=True), H.vs(16, 64)]
+    cfg = [H.vs(48, 24, expanded=True), H.vs(16, 64, expanded=True)]  # one slash mode per layer
     out = B.mi_layer_attn_varlen(q, k, v, cu, cfg)
     torch.cuda.synchronize()
     for b, n in enumerate(lens):

@@ -226,10 +226,11 @@ __device__ void warp_topk_sorted(F key_at, int n, int k, int* out, int* hist) {
 // k > N keeps all N indices, and the row is padded with -1 up to the row stride.
 //
 // For k much smaller than N a threshold filter does most of the work in two
-// passes over the scores: the key at rank about 1.5 k S / N of a strided sample
-// of S = 8192 scores is a threshold that about 1.5 k scores reach; the scores at
-// or above it are compacted, in index order, into shared memory, and the exact
-// selection runs on them.  If at least k scores reach the threshold, every
+// passes over the scores: the key at rank about 1.25 k S / N (+ 16) of a strided
+// sample of S scores (one in 64, 2048 to 8192 of them) is a threshold that about
+// 1.25 k scores reach (measured: the radix select over an 8192-score sample took a
+// third of the kernel at 128K); the scores at or above it are compacted, in index
+// order, into shared memory, and the exact selection runs on them.  If at least k scores reach the threshold, every
 // element of the top k (ties at the k-th key included) is among them, so the
 // result is the same as selecting over all N; otherwise, or if they do not fit,
 // the selection runs over all N.
@@ -247,6 +248,7 @@ __device__ __forceinline__ void load_quads(const float* x, int base, int end, in
 }
 
 constexpr int kTopkSample = 8192;
+constexpr int kTopkSampleMin = 2048;
 constexpr int kTopkCand = 20480;
 struct TopkSmem {
   SelectSmem sel;
@@ -273,15 +275,16 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
   int32_t* out = (vert ? v_idx : s_idx) + (size_t)slot * ld;
   auto gkey = [x](int i) { return float_key(__ldg(x + i)); };
   bool done = kk == 0;
-  if (!done && N >= 4 * kTopkSample && 3 * kk <= 2 * kTopkCand) {
-    for (int j = tid; j < kTopkSample; j += NT)
-      sm.samp[j] = gkey(static_cast<int>((static_cast<int64_t>(j) * N) / kTopkSample));
+  // the sample: one score in 64, between 2048 and kTopkSample of them
+  const int S = min(kTopkSample, max(kTopkSampleMin, N >> 6));
+  if (!done && N >= 4 * S && 4 * kk <= 3 * kTopkCand) {
+    for (int j = tid; j < S; j += NT)
+      sm.samp[j] = gkey(static_cast<int>((static_cast<int64_t>(j) * N) / S));
     __syncthreads();
-    const int rs = min(kTopkSample,
-                       static_cast<int>((3ll * kk * kTopkSample) / (2ll * N)) + 16);
+    const int rs = min(S, static_cast<int>((5ll * kk * S) / (4ll * N)) + 16);
     int rem_s;
     const uint32_t* sp = sm.samp;
-    const uint32_t tau = radix_kth_key<NT>([sp](int j) { return sp[j]; }, kTopkSample, rs, sm.sel, &rem_s);
+    const uint32_t tau = radix_kth_key<NT>([sp](int j) { return sp[j]; }, S, rs, sm.sel, &rem_s);
     // count the scores at or above the threshold, warp by warp over contiguous
     // segments; with N a multiple of 4 each lane reads float4 quads, kTopkU of them
     // in flight (the sweeps are bound by load latency), else one score at a time

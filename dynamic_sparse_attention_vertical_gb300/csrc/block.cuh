@@ -57,7 +57,8 @@ block_select_kernel(const float* qbar, const float* kbar, int NB, int group, Hea
                     int topk, int ld, int R, int32_t* blk_idx) {
   extern __shared__ float sig[];  // [R][NB]
   __shared__ int hist[kSelRows][256];
-  const int r0 = blockIdx.x * R, slot = blockIdx.y;
+  // the last query blocks (the most candidates) are scheduled first
+  const int r0 = (gridDim.x - 1 - blockIdx.x) * R, slot = blockIdx.y;
   const int nr = min(R, NB - r0);
   const int rmax = r0 + nr - 1;
   const int g = heads.h[slot] / group;
@@ -69,15 +70,21 @@ block_select_kernel(const float* qbar, const float* kbar, int NB, int group, Hea
                      : make_float4(0.f, 0.f, 0.f, 0.f);
   const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
   const int mine = (b16 ? 4 : 0) + (b8 ? 2 : 0) + (b4 ? 1 : 0);  // the query block this lane ends with
-  // four pooled key blocks in flight per warp (independent loads ahead of their use)
-  for (int c0 = warp; c0 <= rmax; c0 += 32) {
-    float4 kv4[4];
+  // four pooled key blocks per warp and step; the next step's are loaded while
+  // this step's are reduced (the loop is bound by the loads' latency)
+  float4 kv4[4];
+  auto load4 = [&](int c0, float4* dst) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = c0 + 8 * u;
-      kv4[u] = (c <= rmax) ? *reinterpret_cast<const float4*>(kbar + ((size_t)g * NB + c) * kD + lane * 4)
+      dst[u] = (c <= rmax) ? *reinterpret_cast<const float4*>(kbar + ((size_t)g * NB + c) * kD + lane * 4)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  };
+  load4(warp, kv4);
+  for (int c0 = warp; c0 <= rmax; c0 += 32) {
+    float4 nx4[4];
+    load4(c0 + 32, nx4);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = c0 + 8 * u;
@@ -101,6 +108,8 @@ block_select_kernel(const float* qbar, const float* kbar, int NB, int group, Hea
       y += __shfl_xor_sync(0xffffffffu, y, 1);
       if ((lane & 3) == 0 && mine < nr && c <= rmax) sig[(size_t)mine * NB + c] = y;
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) kv4[u] = nx4[u];
   }
   __syncthreads();
   // one query block per warp

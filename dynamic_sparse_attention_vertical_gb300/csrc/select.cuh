@@ -155,17 +155,20 @@ __device__ void warp_topk_sorted(F key_at, int n, int k, int* out, int* hist) {
     const int shift = 24 - 8 * pass;
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
-    for (int base = 0; base < n; base += 32) {
-      const int i = base + lane;
-      bool act = false;
-      uint32_t bin = 0;
-      if (i < n) {
-        const uint32_t u = key_at(i);
-        act = (u & pmask) == prefix;
-        bin = (u >> shift) & 255u;
+    for (int base = 0; base < n; base += 128) {  // four keys per lane read ahead
+      uint32_t u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = base + 32 * q + lane;
+        u[q] = (i < n) ? key_at(i) : 0u;
       }
-      const uint32_t peers = __match_any_sync(0xffffffffu, act ? bin : 256u + lane);
-      if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const bool act = base + 32 * q + lane < n && (u[q] & pmask) == prefix;
+        const uint32_t bin = (u[q] >> shift) & 255u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, act ? bin : 256u + lane);
+        if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+      }
     }
     __syncwarp();
     // lane L covers bins 255-8L .. 248-8L (descending): the bin where the count of
@@ -207,18 +210,26 @@ __device__ void warp_topk_sorted(F key_at, int n, int k, int* out, int* hist) {
   const uint32_t kth = prefix;
   const unsigned lt = (1u << lane) - 1u;
   int gb = 0, eb = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    const uint32_t u = (i < n) ? key_at(i) : 0u;
-    const bool isg = i < n && u > kth;
-    const bool ise = i < n && u == kth;
-    const unsigned bg = __ballot_sync(0xffffffffu, isg);
-    const unsigned be = __ballot_sync(0xffffffffu, ise);
-    const int G = gb + __popc(bg & lt), E = eb + __popc(be & lt);
-    if (isg) out[G + min(E, rem)] = i;
-    else if (ise && E < rem) out[G + E] = i;
-    gb += __popc(bg);
-    eb += __popc(be);
+  for (int base = 0; base < n; base += 128) {
+    uint32_t u[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = base + 32 * q + lane;
+      u[q] = (i < n) ? key_at(i) : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // in index order
+      const int i = base + 32 * q + lane;
+      const bool isg = i < n && u[q] > kth;
+      const bool ise = i < n && u[q] == kth;
+      const unsigned bg = __ballot_sync(0xffffffffu, isg);
+      const unsigned be = __ballot_sync(0xffffffffu, ise);
+      const int G = gb + __popc(bg & lt), E = eb + __popc(be & lt);
+      if (isg) out[G + min(E, rem)] = i;
+      else if (ise && E < rem) out[G + E] = i;
+      gb += __popc(bg);
+      eb += __popc(be);
+    }
   }
 }
 

@@ -3,10 +3,13 @@
 // One CTA computes 128 query rows (one row block r) of one head.  Its key
 // range is a list of 128-key tiles chosen by the head's pattern:
 //   - contiguous tiles, TMA-loaded from K/V ([Hkv, N, 128] bf16, 128-byte
-//     swizzle, 64-key boxes), masked element-wise by the pattern's rule;
-//   - for block-sparse heads, tiles made of two 64-key blocks from anywhere
-//     below the diagonal (two boxes each), paired from the two 64-row halves'
-//     selections;
+//     swizzle, 64-key boxes), masked element-wise by the pattern's rule; for
+//     exact vertical-slash heads these are 128-key windows at any key offset
+//     (the greedy cover of the selected diagonals built by vs_index_kernel);
+//   - for block-sparse heads and block-expanded vertical-slash heads, tiles
+//     made of two 64-key blocks from anywhere below the diagonal (two boxes
+//     each): the two 64-row halves' selections, or the blocks the row block's
+//     kept 64-block distances reach, paired two per tile;
 //   - for vertical-slash heads, "gathered" column tiles: the head's selected
 //     key columns are copied side by side once per call (their K and V rows,
 //     vs_colgather_kernel), and a tile is 128 consecutive entries of that
@@ -284,7 +287,8 @@ __device__ __forceinline__ MaskRaw mask_fetch(const AttnArgs& a, const TileRef& 
 struct VsRaw4 {
   TileRef ref;
   bool whole;
-  int base;         // exact: first offset bit of row q0's window; expanded: first 64-block distance
+  int base;         // exact: first offset bit of row q0's window; expanded: bit h + 2 k when
+                    // 64-row half h keeps block k (0: t, 1: t2)
   uint32_t off[8];
   uint32_t col[4];
 };

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <utility>
 
 #include "attention.cuh"
 #include "block.cuh"
@@ -252,6 +253,26 @@ int launched(const char* what) {
 
 const float kScaleLog2 = 1.4426950408889634f / std::sqrt(static_cast<float>(kD));
 
+// Launch a kernel as the programmatic dependent of the kernel before it in the
+// stream (pdl.cuh): it may be scheduled while that one drains and waits for it
+// on the device.
+template <typename... P, typename... A>
+int launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, const char* what,
+                     A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+  return e == cudaSuccess ? MI_OK : cuda_fail(e, what);
+}
+
 // Test-only fault injection (mi_debug_inject); normal operation: mode 0, 4 s waits.
 std::atomic<int> g_fault_mode{MI_FAULT_NONE};
 std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
@@ -368,14 +389,19 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
   const dim3 grid(np, L.NC);
   est_kernel<1><<<grid, kEstThreads, kEstSmem1, st>>>(mq, mk, a);
   if ((rc = launched("estimation pass 1"))) return rc;
-  est_combine<<<cdiv(n_heads * kLastQ, 8), 256, 0, st>>>(a.part, a.stats, L.NC, n_heads * kLastQ);
-  if ((rc = launched("estimation combine"))) return rc;
-  est_kernel<2><<<dim3(np, cdiv(N, a.chunk2)), kEstThreads, kEstSmem2, st>>>(mq, mk, a);
-  if ((rc = launched("estimation pass 2"))) return rc;
+  // combine, pass 2 and the top-k each start while the kernel before them drains
+  const float* part = a.part;
+  if ((rc = launch_dependent(est_combine, dim3(cdiv(n_heads * kLastQ, 8)), dim3(256), 0, st, "estimation combine",
+                             part, a.stats, L.NC, n_heads * kLastQ)))
+    return rc;
+  if ((rc = launch_dependent(est_kernel<2>, dim3(np, cdiv(N, a.chunk2)), dim3(kEstThreads), kEstSmem2, st,
+                             "estimation pass 2", mq, mk, a)))
+    return rc;
   if (ld_v > 0 || ld_s > 0) {
-    vs_topk_kernel<<<dim3(n_heads, 2), 1024, kTopkSmemBytes, st>>>(a.vsc, a.ssc, N, k_v, k_s, v_idx, s_idx, ld_v,
-                                                      ld_s);
-    if ((rc = launched("top-k"))) return rc;
+    const float *vsc = a.vsc, *ssc = a.ssc;
+    if ((rc = launch_dependent(vs_topk_kernel, dim3(n_heads, 2), dim3(1024), kTopkSmemBytes, st, "top-k", vsc, ssc,
+                               N, k_v, k_s, v_idx, s_idx, ld_v, ld_s)))
+      return rc;
   }
   return MI_OK;
 }

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256)
 block_select_kernel(const float* qbar, const float* kbar, int NB, int group, HeadList heads,
                     int topk, int ld, int R, int32_t* blk_idx) {
   extern __shared__ float sig[];  // [R][NB]
-  __shared__ int hist[kSelRows][256];
+  __shared__ alignas(16) int hist[kSelRows][256];
   // the last query blocks (the most candidates) are scheduled first
   const int r0 = (gridDim.x - 1 - blockIdx.x) * R, slot = blockIdx.y;
   const int nr = min(R, NB - r0);

@@ -29,6 +29,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "pdl.cuh"
 #include "ptx.cuh"
 
 namespace mi {
@@ -106,6 +107,9 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int k_hi = min(N, (chunk + 1) * CK);
   const int T = cdiv(k_hi - k_lo, kBN);
   const bool has_halo = (PASS == 2 && chunk > 0);
+  // the next kernel of the chain (combine after pass 1, top-k after pass 2) may
+  // be scheduled now; it waits for this one to complete before reading its output
+  pdl_trigger();
 
   if (tid == 0) {
     mbar_init(&s.q_full, 1);
@@ -273,8 +277,11 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       const int slot = hs ? slot_b : slot_a;
       const int p_i = R - kLastQ + i;
       const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-      // without a second head: m = 0, 1/z = 0 gives zeros (no inf - inf)
+      // without a second head: m = 0, 1/z = 0 gives zeros (no inf - inf).  The
+      // row statistics come from the combine kernel: wait for it (the MMA and
+      // load warps, which touch only Q, K and this CTA's memory, run ahead)
       float m = 0.f, invz = 0.f;
+      pdl_wait();
       if (slot >= 0) {
         m = a.stats[((size_t)slot * kLastQ + i) * 2 + 0];
         invz = a.stats[((size_t)slot * kLastQ + i) * 2 + 1];
@@ -322,10 +329,16 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         if (!mbar_wait_warp(&s.sk_full[sl], ((u - u0) >> 1) & 1, abort, lim)) break;
         const float* src = Sk + sl * kSkSlot + hh * kSkHead;
         float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
+        // row r of skewed column e holds key r + e - 63 of the half tile, and of
+        // column e + 64 key r + e + 1: only rows with that key in 0..63 hold a
+        // probability, the rest are zeros.  The warp's positions e are 0-31 or
+        // 32-63, so the rows 32-63 (lower half) and 0-62 / 0-30 cover it: the
+        // skipped terms are zeros, and the sums keep their order (bit-identical)
+        const bool e_lo = e < 32;  // warp-uniform
 #pragma unroll
         for (int r = 0; r < 64; ++r) {
-          lo[r & 3] += src[r * kSkPitch + e];
-          hi[r & 3] += src[r * kSkPitch + e + 64];
+          if (r >= 32 || !e_lo) lo[r & 3] += src[r * kSkPitch + e];
+          if (r <= (e_lo ? 62 : 30)) hi[r & 3] += src[r * kSkPitch + e + 64];
           cs[r & 3] += src[r * (kSkPitch - 1) + e + 63];
         }
         mbar_arrive(&s.sk_empty[sl]);
@@ -354,7 +367,10 @@ est_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 // Merge the per-chunk (m, z) partials of every estimation row: one warp per row,
 // lane l takes chunks l, l + 32, ... (coalesced), then the maximum and the
 // rescaled sum are reduced over the warp in a fixed order.
+// Launched as the dependent of pass 1 and followed by pass 2 (pdl.cuh).
 __global__ void est_combine(const float* part, float* stats, int NC, int n_rows) {
+  pdl_trigger();
+  pdl_wait();  // the partials of pass 1
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (row >= n_rows) return;
   const float2* pp = reinterpret_cast<const float2*>(part + (size_t)row * NC * 2);

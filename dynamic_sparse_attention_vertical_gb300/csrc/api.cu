@@ -399,8 +399,9 @@ int est_run(const void* q, const void* k, int Hq, int Hkv, int N, int64_t ld, co
     return rc;
   if (ld_v > 0 || ld_s > 0) {
     const float *vsc = a.vsc, *ssc = a.ssc;
-    if ((rc = launch_dependent(vs_topk_kernel, dim3(n_heads, 2), dim3(1024), kTopkSmemBytes, st, "top-k", vsc, ssc,
-                               N, k_v, k_s, v_idx, s_idx, ld_v, ld_s)))
+    // a cluster of two CTAs per (head, vertical | slash) row
+    if ((rc = launch_dependent(vs_topk_kernel, dim3(2 * n_heads, 2), dim3(1024), kTopkSmemBytes, st, "top-k", vsc,
+                               ssc, N, k_v, k_s, v_idx, s_idx, ld_v, ld_s)))
       return rc;
   }
   return MI_OK;

@@ -32,13 +32,10 @@ __device__ __forceinline__ unsigned match8(uint32_t bin, bool act) {
 
 // The bin holding the rem-th largest key of a 256-bin histogram (bins in
 // ascending key order) and the rank of that key inside the bin, found by one
-// warp: lane L covers bins 255-8L .. 248-8L (descending).  Requires
-// 1 <= rem <= the histogram's total; every lane returns the same values.
-__device__ __forceinline__ void hist_pick(const int* hist, int rem, int* bin_out, int* rem_out) {
+// warp from the counts of bins 255-8L .. 248-8L (descending) in lane L's c[8].
+// Requires 1 <= rem <= the histogram's total; every lane returns the same values.
+__device__ __forceinline__ void pick_bin(const int (&c)[8], int rem, int* bin_out, int* rem_out) {
   const int lane = threadIdx.x & 31;
-  const int4 lo = *reinterpret_cast<const int4*>(hist + 248 - 8 * lane);
-  const int4 hi = *reinterpret_cast<const int4*>(hist + 252 - 8 * lane);
-  const int c[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};  // bins 255-8L down
   int tot = 0;
 #pragma unroll
   for (int e = 0; e < 8; ++e) tot += c[e];
@@ -66,19 +63,42 @@ __device__ __forceinline__ void hist_pick(const int* hist, int rem, int* bin_out
   *rem_out = __shfl_sync(0xffffffffu, r, leader);
 }
 
+// Lane L's counts c[8] of bins 255-8L .. 248-8L of a 16-byte aligned histogram.
+__device__ __forceinline__ void hist_counts(const int* hist, int (&c)[8]) {
+  const int lane = threadIdx.x & 31;
+  const int4 lo = *reinterpret_cast<const int4*>(hist + 248 - 8 * lane);
+  const int4 hi = *reinterpret_cast<const int4*>(hist + 252 - 8 * lane);
+  c[0] = hi.w;
+  c[1] = hi.z;
+  c[2] = hi.y;
+  c[3] = hi.x;
+  c[4] = lo.w;
+  c[5] = lo.z;
+  c[6] = lo.y;
+  c[7] = lo.x;
+}
+
+__device__ __forceinline__ void hist_pick(const int* hist, int rem, int* bin_out, int* rem_out) {
+  int c[8];
+  hist_counts(hist, c);
+  pick_bin(c, rem, bin_out, rem_out);
+}
+
 struct SelectSmem {
   alignas(16) int hist[3][256];  // one per radix pass, rotating
   int wgt[32];
   int weq[32];
+  int pick[2];  // the pass's bin and rank, from warp 0
 };
 
 // The key of the k-th largest of n keys (1 <= k <= n) by a 4-pass 8-bit radix
 // select; *rem_out receives how many elements equal to that key are among the
-// top k.  All NT threads of the block must call it; no early exit.  One block
-// barrier per pass: every warp scans the pass's histogram itself, and the
-// histograms rotate over three buffers, so that a buffer is cleared (after the
-// barrier of the pass that follows its last reading) one barrier before it is
-// filled again.
+// top k.  All NT threads of the block must call it; no early exit.  Per pass:
+// the count, a barrier, warp 0 finds the bin while the other warps clear the
+// histogram of two passes later (three rotating buffers: it was last read one
+// pass earlier), and a barrier before every thread reads the bin.  (Every warp
+// scanning the histogram itself, with one barrier per pass, was slower: 32
+// warps reading and scanning the same 256 bins.)
 template <int NT, class F>
 __device__ uint32_t radix_kth_key(F key_at, int n, int k, SelectSmem& sm, int* rem_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -103,15 +123,21 @@ __device__ uint32_t radix_kth_key(F key_at, int n, int k, SelectSmem& sm, int* r
       if (act && lane == __ffs(peers) - 1) atomicAdd(&h[bin], __popc(peers));
     }
     __syncthreads();
-    if (pass == 0 || pass == 1) {  // the buffer of pass + 2, last read in pass - 1
+    if (warp == 0) {
+      int bin, r;
+      hist_pick(h, rem, &bin, &r);
+      if (lane == 0) {
+        sm.pick[0] = bin;
+        sm.pick[1] = r;
+      }
+    } else if (pass == 0 || pass == 1) {
       int* z = sm.hist[(pass + 2) % 3];
-      for (int i = tid; i < 256; i += NT) z[i] = 0;
+      for (int i = tid - 32; i < 256; i += NT - 32) z[i] = 0;
     }
-    int bin, r;
-    hist_pick(h, rem, &bin, &r);
-    prefix |= static_cast<uint32_t>(bin) << shift;
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(sm.pick[0]) << shift;
     pmask |= 0xFFu << shift;
-    rem = r;
+    rem = sm.pick[1];
   }
   *rem_out = rem;
   return prefix;
@@ -234,18 +260,123 @@ __device__ void warp_topk_sorted(F key_at, int n, int k, int* out, int* hist) {
   }
 }
 
+// ---- the two CTAs of a thread-block cluster (the pair of one score row)
+
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs: shared-memory writes of either CTA before it are
+// visible to both after it (release / acquire); also a barrier of each CTA.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared-memory address of the same object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_st(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int4 cluster_ld4(uint32_t addr) {
+  int4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// The radix select of radix_kth_key over the keys of both CTAs of a pair: n is
+// this CTA's count of keys, k the rank among both CTAs' keys (1 <= k <= both
+// counts).  Each CTA counts its own keys; after a cluster barrier warp 0 of
+// each adds the other CTA's histogram (read through distributed shared memory)
+// to its own and picks the bin, so both pick the same.  The histogram cleared
+// in a pass was last read, by both warps 0, before that pass's cluster barrier.
+// Both CTAs must call it; every thread of them runs every barrier.
+template <int NT, class F>
+__device__ uint32_t radix_kth_pair(F key_at, int n, int k, SelectSmem& sm, uint32_t peer, int* rem_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0, pmask = 0;
+  int rem = k;
+  __syncthreads();  // earlier readers of the buffers are done
+  for (int i = tid; i < 512; i += NT) (&sm.hist[0][0])[i] = 0;
+  __syncthreads();
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    int* h = sm.hist[pass % 3];
+    for (int base = warp * 32; base < n; base += NT) {
+      const int i = base + lane;
+      bool act = false;
+      uint32_t bin = 0;
+      if (i < n) {
+        const uint32_t u = key_at(i);
+        act = (u & pmask) == prefix;
+        bin = (u >> shift) & 255u;
+      }
+      const unsigned peers = match8(bin, act);
+      if (act && lane == __ffs(peers) - 1) atomicAdd(&h[bin], __popc(peers));
+    }
+    cluster_barrier();  // both CTAs' counts of this pass are in
+    if (warp == 0) {
+      int c[8];
+      hist_counts(h, c);
+      const uint32_t ra = cluster_addr(h + 248 - 8 * lane, peer);
+      const int4 lo = cluster_ld4(ra), hi = cluster_ld4(ra + 16);
+      c[0] += hi.w;
+      c[1] += hi.z;
+      c[2] += hi.y;
+      c[3] += hi.x;
+      c[4] += lo.w;
+      c[5] += lo.z;
+      c[6] += lo.y;
+      c[7] += lo.x;
+      int bin, r;
+      pick_bin(c, rem, &bin, &r);
+      if (lane == 0) {
+        sm.pick[0] = bin;
+        sm.pick[1] = r;
+      }
+    } else if (pass == 0 || pass == 1) {
+      int* z = sm.hist[(pass + 2) % 3];
+      for (int i = tid - 32; i < 256; i += NT - 32) z[i] = 0;
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(sm.pick[0]) << shift;
+    pmask |= 0xFFu << shift;
+    rem = sm.pick[1];
+  }
+  *rem_out = rem;
+  return prefix;
+}
+
 // T1: top-k of the vertical (y = 0) or slash (y = 1) scores of every listed head;
 // k > N keeps all N indices, and the row is padded with -1 up to the row stride.
+// Each row is selected by a cluster of two CTAs (x = 2 slot + CTA rank).
 //
 // For k much smaller than N a threshold filter does most of the work in two
 // passes over the scores: the key at rank about 1.25 k S / N (+ 16) of a strided
-// sample of S scores (one in 64, 2048 to 8192 of them) is a threshold that about
-// 1.25 k scores reach (measured: the radix select over an 8192-score sample took a
-// third of the kernel at 128K); the scores at or above it are compacted, in index
-// order, into shared memory, and the exact selection runs on them.  If at least k scores reach the threshold, every
-// element of the top k (ties at the k-th key included) is among them, so the
-// result is the same as selecting over all N; otherwise, or if they do not fit,
-// the selection runs over all N.
+// sample of S scores (one in 64, 2048 to 8192 of them; both CTAs find the same)
+// is a threshold that about 1.25 k scores reach.  Each CTA counts, then compacts
+// in index order into its shared memory, the scores of its half of the row at or
+// above it; the exact selection runs on both halves' candidates (the radix
+// histograms summed over the pair, CTA 1's output placed after CTA 0's).  If at
+// least k scores reach the threshold every element of the top k (ties at the
+// k-th key included) is a candidate, so the result is the same as selecting over
+// all N; otherwise, or if a half's candidates do not fit, CTA 0 alone selects
+// over all N.  (One CTA per row took about 60 us at 128K, most of it in the two
+// sweeps and the candidates' radix, which the pair halves.)
 constexpr int kTopkU = 4;  // float4 quads per lane in flight in the threshold sweeps
 
 // Quads base + 128 u + 4 lane (u < U) of x, each read whole when it starts before
@@ -265,13 +396,15 @@ constexpr int kTopkCand = 20480;
 struct TopkSmem {
   SelectSmem sel;
   uint32_t samp[kTopkSample];
-  uint32_t ckey[kTopkCand];
+  uint32_t ckey[kTopkCand];  // this CTA's candidates, in index order
   int cidx[kTopkCand];
   int wcnt[32];
+  int peer_cnt;  // written by the other CTA of the pair
+  int peer_gt, peer_eq;
 };
 constexpr size_t kTopkSmemBytes = sizeof(TopkSmem);
 
-__global__ void __launch_bounds__(1024, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(1024, 1)
 vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int32_t* v_idx,
                int32_t* s_idx, int ld_v, int ld_s) {
   extern __shared__ uint8_t topk_raw[];
@@ -279,7 +412,8 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
   pdl_wait();  // launched as the dependent of estimation pass 2: its scores
   constexpr int NT = 1024, NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slot = blockIdx.x;
+  const uint32_t rank = cluster_cta_rank(), peer = rank ^ 1u;
+  const int slot = blockIdx.x >> 1;
   const bool vert = blockIdx.y == 0;
   const float* x = (vert ? vsc : ssc) + (size_t)slot * N;
   const int k = vert ? k_v : k_s;
@@ -290,6 +424,8 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
   bool done = kk == 0;
   // the sample: one score in 64, between 2048 and kTopkSample of them
   const int S = min(kTopkSample, max(kTopkSampleMin, N >> 6));
+  // every decision below is the same in both CTAs (the same inputs, or values
+  // both read after a cluster barrier), so both run the same cluster barriers
   if (!done && N >= 4 * S && 4 * kk <= 3 * kTopkCand) {
     for (int j = tid; j < S; j += NT)
       sm.samp[j] = gkey(static_cast<int>((static_cast<int64_t>(j) * N) / S));
@@ -299,12 +435,14 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
     const uint32_t* sp = sm.samp;
     const uint32_t tau = radix_kth_key<NT>([sp](int j) { return sp[j]; }, S, rs, sm.sel, &rem_s);
     // count the scores at or above the threshold, warp by warp over contiguous
-    // segments; with N a multiple of 4 each lane reads float4 quads, kTopkU of them
-    // in flight (the sweeps are bound by load latency), else one score at a time
+    // segments (CTA 0 the first 32, CTA 1 the next 32); with N a multiple of 4
+    // each lane reads float4 quads, kTopkU of them in flight (the sweeps are
+    // bound by load latency), else one score at a time
     const bool vec = (N & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
     constexpr int kSpan = 128 * kTopkU;  // scores per warp and vector step
-    const int seg = cdiv(cdiv(N, NW), kSpan) * kSpan;
-    const int beg = min(warp * seg, N), end = min(beg + seg, N);
+    const int seg = cdiv(cdiv(N, 2 * NW), kSpan) * kSpan;
+    const int gw = static_cast<int>(rank) * NW + warp;
+    const int beg = min(gw * seg, N), end = min(beg + seg, N);
     int c = 0;
     if (vec) {
       for (int base = beg; base < end; base += kSpan) {
@@ -326,12 +464,16 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
     }
     if (lane == 0) sm.wcnt[warp] = c;
     __syncthreads();
-    int before = 0, total = 0;
+    int before = 0, mine = 0;
     for (int w = 0; w < NW; ++w) {
-      total += sm.wcnt[w];
+      mine += sm.wcnt[w];
       if (w < warp) before += sm.wcnt[w];
     }
-    if (total >= kk && total <= kTopkCand) {  // the same for every thread
+    if (tid == 0) cluster_st(cluster_addr(&sm.peer_cnt, peer), mine);
+    cluster_barrier();
+    const int other = sm.peer_cnt;
+    const int total = mine + other;
+    if (total >= kk && mine <= kTopkCand && other <= kTopkCand) {
       const unsigned lt = (1u << lane) - 1u;
       if (vec) {
         for (int base = beg; base < end; base += kSpan) {
@@ -378,15 +520,66 @@ vs_topk_kernel(const float* vsc, const float* ssc, int N, int k_v, int k_s, int3
           before += __popc(b);
         }
       }
-      __syncthreads();
       const uint32_t* ck = sm.ckey;
-      topk_select_sorted<NT>([ck](int j) { return ck[j]; }, total, kk, out, sm.sel);
-      // candidate positions -> score indices (each thread its own entries)
-      for (int j = tid; j < kk; j += NT) out[j] = sm.cidx[out[j]];
+      int rem;  // radix_kth_pair starts with a block barrier: the candidates are in
+      const uint32_t kth = radix_kth_pair<NT>([ck](int j) { return ck[j]; }, mine, kk, sm.sel, peer, &rem);
+      // ordered take over this CTA's candidates, CTA 1's placed after CTA 0's:
+      // each warp counts its segment's keys above and equal to the k-th ...
+      const int tseg = cdiv(cdiv(mine, NW), 32) * 32;
+      const int tb = min(warp * tseg, mine), te = min(tb + tseg, mine);
+      int gt = 0, eq = 0;
+      for (int base = tb; base < te; base += 32) {
+        const int i = base + lane;
+        const uint32_t u = (i < te) ? ck[i] : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, i < te && u > kth));
+        eq += __popc(__ballot_sync(0xffffffffu, i < te && u == kth));
+      }
+      if (lane == 0) {
+        sm.sel.wgt[warp] = gt;
+        sm.sel.weq[warp] = eq;
+      }
+      __syncthreads();
+      int gb = 0, eb = 0, cgt = 0, ceq = 0;
+      for (int w = 0; w < NW; ++w) {
+        if (w < warp) {
+          gb += sm.sel.wgt[w];
+          eb += sm.sel.weq[w];
+        }
+        cgt += sm.sel.wgt[w];
+        ceq += sm.sel.weq[w];
+      }
+      // ... CTA 0 hands its totals to CTA 1 (the last access of the other CTA's
+      // shared memory: after this barrier either CTA may finish)
+      if (rank == 0 && tid == 0) {
+        cluster_st(cluster_addr(&sm.peer_gt, peer), cgt);
+        cluster_st(cluster_addr(&sm.peer_eq, peer), ceq);
+      }
+      cluster_barrier();
+      if (rank == 1) {
+        gb += sm.peer_gt;
+        eb += sm.peer_eq;
+      }
+      // ... and writes, ascending, every score index above it plus the first
+      // `rem` equal to it
+      for (int base = tb; base < te; base += 32) {
+        const int i = base + lane;
+        const uint32_t u = (i < te) ? ck[i] : 0u;
+        const bool isg = i < te && u > kth;
+        const bool ise = i < te && u == kth;
+        const unsigned bg = __ballot_sync(0xffffffffu, isg);
+        const unsigned be = __ballot_sync(0xffffffffu, ise);
+        const int G = gb + __popc(bg & lt), E = eb + __popc(be & lt);
+        // the places are below kk by construction; the bound keeps a wrong
+        // k-th key from writing past the row
+        const int at = isg ? G + min(E, rem) : ((ise && E < rem) ? G + E : kk);
+        if (at < kk) out[at] = sm.cidx[i];
+        gb += __popc(bg);
+        eb += __popc(be);
+      }
       done = true;
     }
-    __syncthreads();
   }
+  if (rank != 0) return;  // the rest is CTA 0's: no cluster barrier follows
   if (!done) topk_select_sorted<NT>(gkey, N, kk, out, sm.sel);
   for (int i = kk + tid; i < ld; i += NT) out[i] = -1;
 }

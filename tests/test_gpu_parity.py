@@ -392,6 +392,36 @@ def test_bounded_wait_expiry_reports_timeout():
     assert_close(out.float().cpu().numpy()[0], ref, "after timeout")
 
 
+@pytest.mark.parametrize("where", ["spread", "first_half", "second_half"])
+def test_topk_ties_across_the_pair_halves(where):
+    """1500 identical key rows along the direction of the last 64 queries: their
+    vertical scores tie exactly (the same column sums in the same order) and lie
+    far above every other column, so the top 1000 are the 1000 lowest-indexed of
+    them.  Each score row is selected by two CTAs, one per half of the row (the
+    boundary is N / 2 here): spread over both halves, the tied keys taken make
+    the second CTA's output start after the first's, and the tie cut falls in the
+    second half; in one half, the other CTA holds no tied key."""
+    N, Hq, Hkv, d = 32768, 2, 1, 128
+    g = torch.Generator().manual_seed(17)
+    rng = np.random.default_rng(17)
+    lo, hi = {"spread": (0, N - 64), "first_half": (0, N // 2), "second_half": (N // 2, N - 64)}[where]
+    T = np.sort(rng.choice(np.arange(lo, hi), size=1500, replace=False))
+    u = torch.randn(d, generator=g)
+    u = u / u.norm()
+    k = torch.randn(Hkv, N, d, generator=g)
+    k[0, torch.from_numpy(T)] = 16.0 * u
+    q = torch.randn(Hq, N, d, generator=g)
+    q[:, N - 64:] = 16.0 * u + 0.01 * torch.randn(Hq, 64, d, generator=g)
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    v_idx, s_idx = B.mi_vs_estimate(q.to(DEV), k.to(DEV), k_v=1000, k_s=256)
+    want = T[:1000]
+    for h in range(Hq):
+        vi_ref, si_ref, _, sc = O.vs_estimate(q[h], k[0], 64, 1000, 256)
+        assert vi_ref.tolist() == want.tolist()  # the construction, checked on the oracle
+        assert v_idx[h].cpu().tolist() == want.tolist()
+        band_agree(s_idx[h].cpu().numpy(), si_ref, sc, 256)
+
+
 def test_estimate_all_ties_takes_lowest_indices():
     """Zero queries: every query weighs its keys uniformly, so the column scores tie
     (each column summed over the same rows in the same order) and the selection must

@@ -1,4 +1,5 @@
-// select.cuh - block-wide top-k selection, returned in ascending index order.
+// select.cuh - top-k selection by a block, a warp or a pair of CTAs (a
+// thread-block cluster), returned in ascending index order.
 //
 // The pages keep the top-k vertical columns and top-k slash diagonals
 // (README mirror, gittoolsai.com, "Kernel-only usage": vertical_topk, slash)
